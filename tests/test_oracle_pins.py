@@ -1,0 +1,503 @@
+"""Pins of the CPU oracle against what the method's definition and mathematics fix.
+
+None of these tests reads an expected value from the oracle itself: they use
+brute-force nearest-value search, library casts (ml_dtypes, torch), exact
+rational arithmetic, hand-worked blocks (tests/golden/hand_blocks.json) and
+layout patterns whose answer follows from power-of-two scaling.
+
+Method: "LongLive-2.0: An NVFP4 Parallel Infrastructure for Long Video
+Generation" (summary page): inference step 7 (K-smoothing, then 4/6 NVFP4 KV
+cache) and the "full-stack NVFP4" paragraph (Four-Over-Six keeps the lower-MSE
+of two FP8 block-scale candidates); training step 4 (2-D weight blocks).
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+E2M1_MAG = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # NVFP4 element values by magnitude code 0..7
+
+
+# ----------------------------------------------------------------- brute force
+def brute_e2m1(y: float) -> int:
+    """Nearest E2M1 value by exhaustive search (exact rational distances); ties go to the even code;
+    sign kept; infinities saturate to 6."""
+    sign = 8 if np.signbit(np.float32(y)) else 0
+    if not np.isfinite(y):
+        return 7 | sign
+    a = abs(Fraction(float(y)))
+    best, bestd = None, None
+    for code, v in enumerate(E2M1_MAG):
+        d = abs(a - Fraction(v))
+        if bestd is None or d < bestd or (d == bestd and code % 2 == 0):
+            best, bestd = code, d
+    return best | sign
+
+
+def e4m3_table():
+    ml = pytest.importorskip("ml_dtypes")
+    vals = np.arange(256, dtype=np.uint8).view(ml.float8_e4m3fn).astype(np.float64)
+    return vals
+
+
+def brute_e4m3(s: float, vals) -> int:
+    """Nearest finite E4M3 magnitude (codes 0..126) with saturation at 448; ties to the even code."""
+    sign = 0x80 if np.signbit(np.float32(s)) else 0
+    if not np.isfinite(s) or abs(s) >= 448.0:
+        return 0x7E | sign
+    a = Fraction(abs(float(s)))
+    d = [abs(Fraction(float(v)) - a) for v in vals[:127]]
+    m = min(d)
+    cands = [c for c in range(127) if d[c] == m]
+    code = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+    return code | sign
+
+
+# ----------------------------------------------------------------- scalar casts
+def _e2m1_points():
+    rng = np.random.default_rng(123)
+    pts = list(np.arange(-8.0, 8.0 + 1e-9, 1.0 / 64.0))
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for m in mids:
+        for s in (1.0, -1.0):
+            f = np.float32(s * m)
+            pts += [f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))]
+    pts += [0.0, -0.0, 1e-30, -1e-30, 6.0, 6.5, 7.0, 8.0, 1e6, -1e6, 3e38, float("inf"), float("-inf")]
+    pts += list(rng.standard_normal(20000) * 3.0)
+    pts += list(rng.standard_normal(2000) * 1e-3)
+    return [float(np.float32(p)) for p in pts]
+
+
+def test_e2m1_encode_matches_bruteforce(oracle):
+    for y in _e2m1_points():
+        assert oracle.e2m1_encode(y) == brute_e2m1(y), y
+
+
+def test_e2m1_encode_matches_ml_dtypes(oracle):
+    ml = pytest.importorskip("ml_dtypes")
+    pts = np.array([p for p in _e2m1_points() if np.isfinite(p)], dtype=np.float32)
+    lib = pts.astype(ml.float4_e2m1fn).view(np.uint8) & 0xF
+    ours = np.array([oracle.e2m1_encode(float(p)) for p in pts], dtype=np.uint8)
+    assert np.array_equal(lib, ours)
+
+
+def test_e2m1_decode_values(oracle):
+    for code in range(16):
+        v = E2M1_MAG[code & 7] * (-1.0 if code & 8 else 1.0)
+        got = oracle.e2m1_decode(code)
+        assert got == v and np.signbit(got) == bool(code & 8)
+
+
+def _e4m3_points(vals):
+    rng = np.random.default_rng(7)
+    mags = vals[:127]
+    pts = list(mags)
+    for a, b in zip(mags[:-1], mags[1:]):
+        m = np.float32((a + b) / 2)
+        pts += [m, np.nextafter(m, np.float32(np.inf)), np.nextafter(m, np.float32(-np.inf))]
+    pts += [448.0, 449.0, 463.99, 464.0, 464.01, 479.0, 480.0, 1e4, 3e38, float("inf"), 0.0, -0.0, 1e-30, 2.0**-10,
+            2.0**-10 * 1.0001, 2.0**-9, 3 * 2.0**-10]
+    pts += list(np.exp2(rng.uniform(-12.0, 10.0, 20000)))
+    return [float(np.float32(p)) for p in pts]
+
+
+def test_e4m3_encode_matches_bruteforce(oracle):
+    vals = e4m3_table()
+    for s in _e4m3_points(vals):
+        assert oracle.e4m3_encode(s) == brute_e4m3(s, vals), s
+
+
+def test_e4m3_encode_matches_ml_dtypes_in_range(oracle):
+    ml = pytest.importorskip("ml_dtypes")
+    vals = e4m3_table()
+    pts = np.array([p for p in _e4m3_points(vals) if np.isfinite(p)], dtype=np.float32)
+    # ml_dtypes does not saturate (values above 464 become NaN): clamp first, as the format's
+    # saturating cast does.
+    clamped = np.clip(pts, -448.0, 448.0).astype(np.float32)
+    lib = clamped.astype(ml.float8_e4m3fn).view(np.uint8)
+    ours = np.array([oracle.e4m3_encode(float(p)) for p in pts], dtype=np.uint8)
+    assert np.array_equal(lib, ours)
+
+
+def test_e4m3_decode_matches_ml_dtypes(oracle):
+    vals = e4m3_table()
+    for code in range(256):
+        got = oracle.e4m3_decode(code)
+        if np.isnan(vals[code]):
+            assert np.isnan(got)
+        else:
+            assert got == vals[code]
+
+
+def test_bf16_rne_matches_torch(oracle):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2**32, size=30000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    extra = np.array([0.0, -0.0, 1.0, 1.00390625, 1.0078125, 1.01171875, 3.3895314e38, 3.4e38, -3.4e38, 1e-40,
+                      -1e-40, 9.2e-41, float("inf"), float("-inf")], dtype=np.float32)
+    x = np.concatenate([x, extra])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = np.array([oracle.bf16_rne(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(ref, ours)
+
+
+# ----------------------------------------------------------------- hand-worked
+def _hand():
+    with open(os.path.join(HERE, "golden", "hand_blocks.json")) as f:
+        return json.load(f)
+
+
+def test_hand_blocks_detail(oracle):
+    h = _hand()
+    g = h["tensor"]["g"]
+    assert oracle.tensor_scale(10.5) == g  # 10.5 / 2688 = 2^-8
+    for b in h["blocks"]:
+        d = oracle.block_detail(np.array(b["values"], dtype=np.float32), g)
+        assert d["scale"] == b["scale"], b["name"]
+        assert d["chose4"] == b["chose4"], b["name"]
+        assert d["codes"].tolist() == b["codes"], b["name"]
+        for key in ("e6", "e4", "err6", "err4", "sum6"):
+            if key in b:
+                assert d[key] == b[key], (b["name"], key)
+
+
+def test_hand_row_packing(oracle):
+    h = _hand()
+    x = np.concatenate([np.array(b["values"], dtype=np.float32) for b in h["blocks"]]).reshape(1, 1, 80)
+    r = oracle.kv_smooth_quant(x, smooth=False)
+    assert r["status"] == 0
+    assert r["g"] == h["tensor"]["g"]
+    assert r["scales"].ravel().tolist() == h["packed_row"]["scales"]
+    assert r["codes"].ravel().tolist() == h["packed_row"]["codes"]
+    # dequant of block B (4 chosen, S = 1.5) reproduces the input exactly
+    out = oracle.bf16_bits_to_f32(oracle.kv_dequant(r["codes"], r["scales"], r["g"]))
+    assert out.ravel()[16:32].tolist() == h["blocks"][1]["values"]
+
+
+# ----------------------------------------------------------------- mean / smoothing
+def _round_fraction_to_f32(q: Fraction) -> np.float32:
+    c = np.float32(float(q))
+    best = None
+    for cand in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        d = abs(Fraction(float(cand)) - q)
+        key = (d, int(np.array(cand, dtype=np.float32).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return best[1]
+
+
+def test_mean_is_exact_mean_rounded_once_fp32(oracle):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K, _ = W.tiny_kv(0)
+    mean = oracle.channel_mean(K.reshape(64, -1))
+    for c in range(K.shape[2]):
+        exact = sum(Fraction(float(v)) for v in K[:, 0, c]) / 64
+        assert mean[c] == _round_fraction_to_f32(exact), c
+
+
+def test_mean_bf16_chunk_exact(oracle):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    Xb = W.to_bf16_bits(W.chunk_k(2000, T=7040, H=1, D=16))
+    mean = oracle.channel_mean(Xb.reshape(7040, -1))
+    Xf = oracle.bf16_bits_to_f32(Xb).reshape(7040, 16)
+    for c in range(16):
+        # bf16 values times 2^133 are integers: exact integer sum
+        s = sum(int(Fraction(float(v)) * 2**133) for v in Xf[:, c])
+        exact = Fraction(s, 7040 * 2**133)
+        assert mean[c] == _round_fraction_to_f32(exact), c
+
+
+def test_smoothing_invariant_tiny(oracle):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K, _ = W.tiny_kv(0)
+    r = oracle.kv_smooth_quant(K, smooth=True)
+    mu = r["mean"].reshape(1, 1, 64)
+    Z = (K - mu).astype(np.float32)  # fp32 subtraction
+    zmean = Z.astype(np.float64).mean(axis=0).ravel()
+    assert np.all(np.abs(zmean) <= 1e-6)  # |mu| < 8 on this config
+    assert np.all(np.abs(zmean) <= 1e-6 * np.maximum(1.0, np.abs(mu.ravel())))
+
+
+def test_smoothing_invariant_chunk_outlier_channels(oracle):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    Xb = W.to_bf16_bits(W.chunk_k(2000, T=7040, H=2, D=128))
+    r = oracle.kv_smooth_quant(Xb, smooth=True)
+    mu = r["mean"].reshape(1, 2, 128)
+    Z = (oracle.bf16_bits_to_f32(Xb) - mu).astype(np.float32)
+    zmean = Z.astype(np.float64).mean(axis=0).ravel()
+    # exact mean of Z is mean(X) - mu_fp32: at most half an ulp of mu
+    assert np.all(np.abs(zmean) <= 1e-6 * np.maximum(1.0, np.abs(mu.ravel())))
+
+
+def test_mean_in_overrides(oracle):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K, _ = W.tiny_kv(0)
+    mi = np.full(64, 0.5, dtype=np.float32)
+    r = oracle.kv_smooth_quant(K, smooth=True, mean_in=mi)
+    assert np.array_equal(r["mean"].ravel(), mi)
+    r2 = oracle.kv_smooth_quant((K - np.float32(0.5)).astype(np.float32), smooth=False)
+    assert np.array_equal(r["codes"], r2["codes"]) and np.array_equal(r["scales"], r2["scales"])
+    assert r["g"] == r2["g"]
+
+
+# ----------------------------------------------------------------- brute-force MSE
+def _bruteforce_err(z, E, g):
+    """Block squared error in the original domain, float64, quantizing each value to its nearest grid point."""
+    S = float(E) * float(g)
+    grid = np.array(sorted(set([v for v in E2M1_MAG] + [-v for v in E2M1_MAG])), dtype=np.float64) * S
+    zz = z.astype(np.float64)[:, None]
+    return float(np.min((zz - grid[None, :]) ** 2, axis=1).sum())
+
+
+def _blocks(rng, n):
+    out = []
+    for i in range(n):
+        kind = i % 5
+        if kind == 0:
+            z = rng.standard_normal(16)
+        elif kind == 1:
+            z = rng.laplace(size=16)
+        elif kind == 2:
+            z = rng.uniform(-1, 1, 16)
+        elif kind == 3:  # values clustered near 75% of the max
+            z = 0.75 * np.sign(rng.standard_normal(16)) * (1 + 0.02 * rng.standard_normal(16))
+            z[0] = 1.0
+        else:  # a single outlier
+            z = 0.05 * rng.standard_normal(16)
+            z[rng.integers(16)] = 1.0
+        out.append((z * np.exp2(rng.uniform(-4, 4))).astype(np.float32))
+    return out
+
+
+def test_choice_minimises_mse_among_the_two(oracle):
+    vals = e4m3_table()
+    rng = np.random.default_rng(5)
+    g = np.float32(8.0 / 2688.0)
+    near_ties = 0
+    n = 4000
+    for z in _blocks(rng, n):
+        d = oracle.block_detail(z, g)
+        if d["scale"] == 0:
+            continue
+        e_chosen = d["e4"] if d["chose4"] else d["e6"]
+        e_other = d["e6"] if d["chose4"] else d["e4"]
+        assert d["scale"] == e_chosen
+        err_c = _bruteforce_err(z, vals[e_chosen], g)
+        err_o = _bruteforce_err(z, vals[e_other], g)
+        if err_c > err_o:
+            rel = (err_c - err_o) / max(err_o, 1e-300)
+            near_ties += 1
+            assert rel <= 1e-5, (z, d)
+        # dequantized chosen block uses the nearest grid point for every element
+        S = float(vals[e_chosen]) * float(g)
+        deq = np.array([oracle.e2m1_decode(c) for c in d["codes"]]) * S
+        nearest = _bruteforce_err(z, vals[e_chosen], g)
+        assert abs(((z.astype(np.float64) - deq) ** 2).sum() - nearest) <= 1e-6 * max(nearest, S * S)
+    assert near_ties <= n * 0.01
+
+
+def test_candidate_scales_map_amax_to_6_and_4(oracle):
+    vals = e4m3_table()
+    rng = np.random.default_rng(9)
+    g = np.float32(3.0 / 2688.0)
+    for z in _blocks(rng, 1000):
+        d = oracle.block_detail(z, g)
+        ab = float(np.abs(z).max())
+        for M, e in ((6, d["e6"]), (4, d["e4"])):
+            target = ab / (M * float(g))
+            if target >= 448:
+                assert e == 0x7E
+                continue
+            # RNE onto the E4M3 grid: no other finite E4M3 value is strictly nearer to the target
+            dist = abs(vals[e] - target)
+            assert np.all(np.abs(vals[:127] - target) >= dist - 1e-9 * target)
+
+
+def test_four_over_six_never_worse_than_six_only(oracle):
+    """Tensor-level: total squared error of 4/6 <= that of plain 6-only NVFP4 (same scales for 6)."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    vals = e4m3_table()
+    X = W.chunk_k(77, T=64, H=2, D=64)
+    r = oracle.kv_smooth_quant(X, smooth=False)
+    g = r["g"]
+    err46 = err6 = 0.0
+    for t in range(64):
+        for h in range(2):
+            for b in range(4):
+                z = X[t, h, 16 * b:16 * b + 16]
+                d = oracle.block_detail(z, g)
+                e_ch = d["e4"] if d["chose4"] else d["e6"]
+                err46 += _bruteforce_err(z, vals[e_ch], g)
+                err6 += _bruteforce_err(z, vals[d["e6"]], g)
+    assert err46 <= err6
+    assert err46 < 0.99 * err6  # the 4-candidate wins often enough to matter on Gaussian data
+
+
+def test_exhaustive_scale_gap_informational(oracle):
+    """Enumerate every positive E4M3 scale on a few blocks: 4/6 is never better than the best single scale."""
+    vals = e4m3_table()
+    rng = np.random.default_rng(3)
+    g = np.float32(1.0 / 2688.0)
+    for z in _blocks(rng, 50):
+        d = oracle.block_detail(z, g)
+        if d["scale"] == 0:
+            continue
+        best = min(_bruteforce_err(z, vals[e], g) for e in range(1, 127))
+        ch = _bruteforce_err(z, vals[d["scale"]], g)
+        assert best <= ch * (1 + 1e-9)
+
+
+# ----------------------------------------------------------------- closed forms / layout
+def test_on_grid_round_trip_exact(oracle):
+    """Blocks whose values are exactly Q * S on the 6-candidate grid come back unchanged."""
+    rng = np.random.default_rng(21)
+    grid = np.array(E2M1_MAG[1:] + [-v for v in E2M1_MAG[1:]], dtype=np.float32)
+    blocks = [np.array([10.5] + [0.0] * 15, dtype=np.float32)]  # sets amax = 10.5, g = 2^-8
+    for _ in range(30):
+        z = rng.choice(grid, 16).astype(np.float32)
+        z[rng.integers(16)] = 6.0  # a_b = 6 -> S6 = 1 exactly
+        blocks.append(z)
+    x = np.concatenate(blocks).reshape(1, 1, -1)
+    r = oracle.kv_smooth_quant(x, smooth=False)
+    assert r["g"] == 2.0**-8
+    out = oracle.bf16_bits_to_f32(oracle.kv_dequant(r["codes"], r["scales"], r["g"])).ravel()
+    assert np.array_equal(out[16:], x.ravel()[16:])
+    assert np.all(r["scales"].ravel()[1:] == 0x78)  # E6 = 256 -> S = 1; err6 = 0 so 6 is kept
+
+
+def test_kv_layout_by_power_of_two_scaling(oracle):
+    """scale[t,h,b] and the codes land where [T][H][D/16] / [T][H][D/2] put them."""
+    h = _hand()
+    pattern = np.array(h["blocks"][4]["values"], dtype=np.float32)  # block E: 6 wins, S6 = 1
+    pat_codes = h["blocks"][4]["codes"]
+    T, H, NBD = 3, 2, 3
+    X = np.zeros((T, H, 16 * NBD), dtype=np.float32)
+    expect_scale = np.zeros((T, H, NBD), dtype=np.int64)
+    for t in range(T):
+        for hh in range(H):
+            for b in range(NBD):
+                n = (t * H + hh) * NBD + b
+                k = n % 9
+                X[t, hh, 16 * b:16 * b + 16] = pattern * np.float32(2.0**-k)
+                expect_scale[t, hh, b] = 0x78 - 8 * k
+    X[2, 1, 32:48] = np.array([10.5] + [0.0] * 15, dtype=np.float32)  # amax = 10.5 -> g = 2^-8
+    expect_scale[2, 1, 2] = 0x7E
+    r = oracle.kv_smooth_quant(X, smooth=False)
+    assert r["g"] == 2.0**-8
+    assert np.array_equal(r["scales"].astype(np.int64), expect_scale)
+    for t in range(T):
+        for hh in range(H):
+            for b in range(NBD):
+                byts = r["codes"][t, hh, 8 * b:8 * b + 8]
+                nib = []
+                for v in byts:
+                    nib += [int(v) & 0xF, int(v) >> 4]
+                if (t, hh, b) == (2, 1, 2):
+                    assert nib == [7] + [0] * 15
+                else:
+                    assert nib == pat_codes, (t, hh, b)
+
+
+def test_weight_2d_tile_layout(oracle):
+    """16x16 tiles: one non-zero per tile; its nibble and the tile's scale land at the right place."""
+    M, N = 32, 48
+    W = np.zeros((M, N), dtype=np.float32)
+    rng = np.random.default_rng(2)
+    expect = {}
+    for i in range(2):
+        for j in range(3):
+            r, c = int(rng.integers(16)), int(rng.integers(16))
+            k = (i * 3 + j) % 6
+            W[16 * i + r, 16 * j + c] = 6.0 * 2.0**-k
+            expect[(i, j)] = (r, c, 0x78 - 8 * k)
+    # the amax tile
+    W[16 * 1 + 5, 16 * 2 + 9] = 0.0
+    W[16 * 1 + 3, 16 * 2 + 4] = 10.5
+    expect[(1, 2)] = (3, 4, 0x7E)
+    res = oracle.weight_quant_2d(W)
+    assert res["g"] == 2.0**-8
+    for (i, j), (r, c, sc) in expect.items():
+        assert res["scales"][i, j] == sc
+    codes = res["codes"]
+    nib = np.zeros((M, N), dtype=np.int64)
+    nib[:, 0::2] = codes & 0xF
+    nib[:, 1::2] = codes >> 4
+    want = np.zeros((M, N), dtype=np.int64)
+    for (i, j), (r, c, sc) in expect.items():
+        want[16 * i + r, 16 * j + c] = 7
+    assert np.array_equal(nib, want)
+
+
+def test_weight_2d_four_wins_on_75_percent_tile(oracle):
+    W = np.zeros((16, 32), dtype=np.float32)
+    W[:, :16] = 4.5 * np.where((np.arange(256).reshape(16, 16) % 2) == 0, 1.0, -1.0)
+    W[0, 0] = 6.0
+    W[0, 16] = 10.5  # second tile sets g = 2^-8
+    res = oracle.weight_quant_2d(W)
+    assert res["g"] == 2.0**-8
+    assert res["scales"][0, 0] == 0x7C and res["chose4"][0, 0] == 1  # S4 = 1.5: every value exact
+    deq = oracle.bf16_bits_to_f32(oracle.weight_dequant_2d(res["codes"], res["scales"], res["g"]))
+    assert np.array_equal(deq[:, :16], W[:, :16])
+
+
+# ----------------------------------------------------------------- degenerate
+def test_all_zero_tensor(oracle):
+    r = oracle.kv_smooth_quant(np.zeros((4, 2, 32), dtype=np.float32), smooth=False)
+    assert r["status"] == 0 and r["g"] == 0.0
+    assert not r["codes"].any() and not r["scales"].any()
+
+
+def test_constant_channels_smooth_to_zero(oracle):
+    X = np.tile(np.arange(32, dtype=np.float32).reshape(1, 1, 32), (5, 3, 1))
+    r = oracle.kv_smooth_quant(X, smooth=True)
+    assert np.array_equal(r["mean"], X[0])
+    assert r["g"] == 0.0 and not r["scales"].any()
+
+
+def test_nonfinite_input_reports_and_fills(oracle):
+    X = np.ones((2, 1, 32), dtype=np.float32)
+    X[1, 0, 3] = np.inf
+    r = oracle.kv_smooth_quant(X, smooth=False)
+    assert r["status"] == 1 and np.isnan(r["g"])
+    assert np.all(r["scales"] == 0x7F) and not r["codes"].any()
+    X[1, 0, 3] = np.nan
+    assert oracle.kv_smooth_quant(X, smooth=True)["status"] == 1
+
+
+def test_empty_chunk(oracle):
+    r = oracle.kv_smooth_quant(np.zeros((0, 2, 16), dtype=np.float32), smooth=True)
+    assert r["status"] == 0 and r["codes"].size == 0 and r["g"] == 0.0
+
+
+def test_invalid_shapes(oracle):
+    with pytest.raises(ValueError):
+        oracle.kv_smooth_quant(np.zeros((2, 1, 24), dtype=np.float32), smooth=False)
+    with pytest.raises(ValueError):
+        oracle.weight_quant_2d(np.zeros((16, 24), dtype=np.float32))
+
+
+def test_dequant_groups_and_mean(oracle):
+    """Each token group uses its own tensor scale and mean."""
+    h = _hand()
+    B = np.array(h["blocks"][1]["values"], dtype=np.float32)
+    A = np.array(h["blocks"][0]["values"], dtype=np.float32)
+    x = np.stack([B, A]).reshape(2, 1, 16)
+    r = oracle.kv_smooth_quant(x, smooth=False)
+    codes = np.concatenate([r["codes"]] * 2)
+    scales = np.concatenate([r["scales"]] * 2)
+    g = np.array([r["g"], r["g"] * 2], dtype=np.float32)  # second group: everything doubled
+    mean = np.stack([np.zeros((1, 16), np.float32), np.full((1, 16), 0.5, np.float32)])
+    out = oracle.bf16_bits_to_f32(oracle.kv_dequant(codes, scales, g, mean=mean, tokens_per_group=2))
+    assert np.array_equal(out[0, 0], B)
+    assert np.array_equal(out[2, 0], 2 * B + 0.5)

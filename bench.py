@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 KV-cache quantizer on GB300.
+
+Metric: NVFP4 smooth+quantize GB/s (and fraction of HBM peak) per KV chunk.
+Workload (one step): one layer's chunk of the LongLive-2.0 KV write -- K and V,
+each 7040 tokens (8 frames x 880) x 24 heads x 128 channels, bf16, resident in
+HBM -- K smoothed and both quantized with Four-Over-Six NVFP4 scales in one
+batched enqueue.  Algorithmic bytes per element: 2 read + 0.5 codes + 1/16
+scale = 2.5625 B.
+
+Timed region: K steps replayed from a CUDA graph over rotating input/output
+sets whose footprint exceeds 2x L2 (reads come from HBM), bracketed by a
+barrier and cudaDeviceSynchronize, measured with CUDA events on the launching
+stream, max over ranks.  N > 1 runs independent replicas (weak scaling).
+
+--impl reference times the CPU oracle (the plain C statement of the method)
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+T_CHUNK, HEADS, HEAD_DIM = 7040, 24, 128
+QUANT_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 16.0      # bf16 in, nibble codes out, one E4M3 scale per 16
+DEQUANT_BYTES_PER_ELEM = 0.5 + 1.0 / 16.0 + 2.0    # codes + scales in, bf16 out
+W2D_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 256.0       # bf16 in, codes out, one scale per 16x16 tile
+METRIC = "NVFP4 smooth+quantize GB/s and fraction of GB300 HBM peak per KV chunk"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch measured with ncu for the kernels below (None until captured for the
+# current kernel version; see profiles/).
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-rows", action="store_true", help="skip the secondary rows (dequant, weights, 30 layers)")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    p.add_argument("--e2e-steps", type=int, default=30)
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- distributed
+def dist_setup():
+    import torch
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(ws, v: float) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_run(tokens: int, reps: int = 1):
+    """Time the oracle on K and V of the first `tokens` tokens of the chunk; returns (GB/s, seconds, elems)."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    oracle.build()
+    K = W.to_bf16_bits(W.chunk_k(2000))[:tokens].copy()
+    V = W.to_bf16_bits(W.chunk_v(2001))[:tokens].copy()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.kv_smooth_quant(K, smooth=True)
+        oracle.kv_smooth_quant(V, smooth=False)
+    dt = time.perf_counter() - t0
+    elems = 2 * K.size * reps
+    return elems * QUANT_BYTES_PER_ELEM / dt / 1e9, dt, elems
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    # Each step is a bounded sample (the first n tokens of K and V) sized so the whole run stays
+    # within about 90 s of single-core oracle time.
+    probe_gbs, probe_s, probe_el = cpu_oracle_run(64)
+    el_per_s = probe_el / probe_s
+    steps_total = args.steps + args.warmup
+    tokens = int(max(1, min(T_CHUNK, 90.0 * el_per_s / max(steps_total, 1) / (2 * HEADS * HEAD_DIM))))
+    import oracle
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K = W.to_bf16_bits(W.chunk_k(2000))[:tokens].copy()
+    V = W.to_bf16_bits(W.chunk_v(2001))[:tokens].copy()
+    for _ in range(args.warmup):
+        oracle.kv_smooth_quant(K, smooth=True)
+        oracle.kv_smooth_quant(V, smooth=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kv_smooth_quant(K, smooth=True)
+        oracle.kv_smooth_quant(V, smooth=False)
+    dt = time.perf_counter() - t0
+    step_bytes = 2 * K.size * QUANT_BYTES_PER_ELEM
+    value = step_bytes * args.steps / dt / 1e9
+    sample = f"K and V of tokens 0..{tokens - 1} of the 7040x24x128 bf16 chunk per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "kv_chunk_7040x24x128_bf16_K_smooth+V", "tokens": T_CHUNK, "heads": HEADS,
+                   "head_dim": HEAD_DIM, "input": "bf16", "parallelism": f"replicas{args.gpus}"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU (ours)
+def run_ours(args, ws, rank):
+    import numpy as np
+    import torch
+
+    import nvfp4_block_quantization_gb300 as nv
+    from nvfp4_block_quantization_gb300 import workloads as W
+    from nvfp4_block_quantization_gb300.build import build
+
+    build()
+    nv.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+
+    # ---- inputs: one chunk's K and V (seeded), replicated into rotating sets
+    Kb, Vb = W.chunk_kv_bf16(2000, 2001)
+    K0 = torch.from_numpy(Kb.view(np.int16)).view(torch.bfloat16).to(dev)
+    V0 = torch.from_numpy(Vb.view(np.int16)).view(torch.bfloat16).to(dev)
+    n_el = K0.numel()
+    step_bytes = 2 * n_el * QUANT_BYTES_PER_ELEM
+    rot = max(4, int(np.ceil(2.0 * l2 / step_bytes)) + 1)
+    sets = []
+    for _ in range(rot):
+        xs = [K0.clone(), V0.clone()]
+        outs, status = nv.kv_smooth_quant_batched(xs, [True, False])  # allocates outputs + status
+        ws_t = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 2, dev)
+        sets.append((xs, outs, status, ws_t))
+    torch.cuda.synchronize()
+
+    def step(i):
+        xs, outs, status, ws_t = sets[i % rot]
+        nv.kv_smooth_quant_batched(xs, [True, False], workspace=ws_t, outs=outs, status=status)
+
+    # ---- capture one round (rot steps) in a CUDA graph
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(rot):
+            step(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(rot):
+            step(i)
+    rounds_w = max(1, -(-args.warmup // rot))
+    rounds = max(1, -(-args.steps // rot))
+    steps = rounds * rot
+    for _ in range(rounds_w):
+        g.replay()
+    torch.cuda.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        ev0.record()
+        for _ in range(rounds):
+            g.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ws, ms)
+    ms_per_step = ms / steps
+    value = ws * steps * step_bytes / (ms * 1e-3) / 1e9
+    per_gpu_gbs = steps * step_bytes / (ms * 1e-3) / 1e9
+
+    # status check: every set must report finite inputs
+    for xs, outs, status, _ in sets:
+        assert int(status.item()) == 0
+
+    # ---- end to end through the public API with host buffers
+    kh = torch.empty_like(K0, device="cpu").pin_memory()
+    vh = torch.empty_like(V0, device="cpu").pin_memory()
+    kh.copy_(K0.cpu())
+    vh.copy_(V0.cpu())
+    xs_d = [torch.empty_like(K0), torch.empty_like(V0)]
+    outs_d, status_d = nv.kv_smooth_quant_batched(xs_d, [True, False])
+    ws_d = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 2, dev)
+    host_out = [(torch.empty_like(o.codes, device="cpu").pin_memory(),
+                 torch.empty_like(o.scales, device="cpu").pin_memory(),
+                 torch.empty_like(o.tensor_scale, device="cpu").pin_memory()) for o in outs_d]
+    mean_h = torch.empty_like(outs_d[0].mean, device="cpu").pin_memory()
+    status_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    d2h_bytes = sum(o.codes.numel() + o.scales.numel() + 4 for o in outs_d) + outs_d[0].mean.numel() * 4 + 4
+    h2d_bytes = (K0.numel() + V0.numel()) * 2
+
+    def e2e_step():
+        xs_d[0].copy_(kh, non_blocking=True)
+        xs_d[1].copy_(vh, non_blocking=True)
+        nv.kv_smooth_quant_batched(xs_d, [True, False], workspace=ws_d, outs=outs_d, status=status_d)
+        for o, (hc, hs, hg) in zip(outs_d, host_out):
+            hc.copy_(o.codes, non_blocking=True)
+            hs.copy_(o.scales, non_blocking=True)
+            hg.copy_(o.tensor_scale, non_blocking=True)
+        mean_h.copy_(outs_d[0].mean, non_blocking=True)
+        status_h.copy_(status_d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1))
+    e2e_value = ws * args.e2e_steps * step_bytes / (e2e_ms * 1e-3) / 1e9
+    assert int(status_h.item()) == 0
+
+    peak, peak_kind = measured_peaks()
+    clocks = clk.summary()
+    kern = "kv_smooth_quant_batched (kv_stats + kv_finalize + kv_quant, K and V)"
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": rounds_w * rot,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded numpy PCG64; K offsets N(0,9)+N(0,1) with 0.5% x16 channels, V N(0,1))",
+        "config": {"workload": "kv_chunk_7040x24x128_bf16_K_smooth+V", "tokens": T_CHUNK, "frames": 8,
+                   "tokens_per_frame": 880, "heads": HEADS, "head_dim": HEAD_DIM, "input": "bf16",
+                   "tensors_per_step": 2, "bytes_per_step": step_bytes,
+                   "l2": f"rotating {rot} input/output sets ({rot * step_bytes / 1e6:.0f} MB > 2x L2 {l2 / 1e6:.0f} MB)",
+                   "graph": "CUDA graph of one rotation round", "parallelism": f"replicas{ws}"},
+        "elements_per_s": ws * steps * 2 * n_el / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": per_gpu_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": per_gpu_gbs / peak, "traffic": NCU_TRAFFIC.get("kv_quant_chunk"),
+                     "kernel": kern, "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": step_bytes},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": steps * 3,
+        "clocks": clocks,
+    }
+
+    if not args.no_rows:
+        line["rows"] = secondary_rows(nv, W, torch, dev, l2, peak)
+    if not args.no_cpu and rank == 0:
+        gbs, secs, elems = cpu_oracle_run(T_CHUNK)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"the whole step: K (smoothed) and V of the 7040x24x128 chunk, "
+                                          f"{elems} elements, {secs:.1f} s single-threaded"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _time_graph(torch, fn, reps_in_graph, replays, warm=2):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(reps_in_graph):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps_in_graph):
+            fn(i)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (reps_in_graph * replays)  # ms per fn call
+
+
+def secondary_rows(nv, W, torch, dev, l2, peak):
+    """The other hot-path rows, each on its own seeded synthetic workload (device-generated)."""
+    rows = {}
+    gen = torch.Generator(device=dev)
+
+    # 30-layer full-model chunk write: K and V of every layer in one batched call
+    gen.manual_seed(3000)
+    L = 30
+    xs, flags = [], []
+    for layer in range(L):
+        off = torch.randn((HEADS, HEAD_DIM), generator=gen, device=dev) * 3.0
+        k = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev) + off
+        ch = torch.randperm(HEADS * HEAD_DIM, generator=gen, device=dev)[:15]
+        k.view(T_CHUNK, -1)[:, ch] *= 16.0
+        v = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev)
+        xs += [k.to(torch.bfloat16), v.to(torch.bfloat16)]
+        flags += [True, False]
+        del k, v
+    outs, status = nv.kv_smooth_quant_batched(xs, flags)
+    wsb = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 2 * L, dev)
+    ms = _time_graph(torch, lambda i: nv.kv_smooth_quant_batched(xs, flags, workspace=wsb, outs=outs, status=status),
+                     1, 20)
+    b = 2 * L * T_CHUNK * HEADS * HEAD_DIM * QUANT_BYTES_PER_ELEM
+    rows["kv_write_30_layers"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+
+    # cache read: 21 frames (3 global-sink frames of chunk 0 + the 18 most recent frames of chunks
+    # 0..2) x 880 tokens, K and V of layers 0 and 1, packed by the quantizer; per-frame groups carry
+    # each frame's chunk tensor scale and mean.
+    Tc, F = 21 * 880, 880
+    frame_src = [(0, f) for f in range(3)] + [(0, 6), (0, 7)] + [(1, f) for f in range(8)] + [(2, f) for f in range(8)]
+    caches = []
+    for t in range(4):  # (layer, K/V) pairs
+        chunk_q = []
+        for c in range(3):
+            x = xs[(c * 2 + t) % len(xs)]  # seeded chunk tensors reused as the cache's source chunks
+            chunk_q.append(nv.kv_smooth_quant(x, True))
+        codes = torch.cat([chunk_q[c].codes[f * F:(f + 1) * F] for c, f in frame_src])
+        scales = torch.cat([chunk_q[c].scales[f * F:(f + 1) * F] for c, f in frame_src])
+        gs = torch.cat([chunk_q[c].tensor_scale for c, f in frame_src])
+        means = torch.stack([chunk_q[c].mean for c, f in frame_src])
+        out = torch.empty((Tc, HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        caches.append((codes, scales, gs, means, out))
+    ms = _time_graph(torch, lambda i: nv.kv_dequant(*caches[i % 4][:3], mean=caches[i % 4][3],
+                                                    tokens_per_group=F, out=caches[i % 4][4]), 8, 20)
+    b = Tc * HEADS * HEAD_DIM * DEQUANT_BYTES_PER_ELEM
+    rows["kv_cache_read_dequant"] = {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+
+    # weights: 4 x 3072x3072 and 2 x 3072x14336 with 16x16 tiles
+    ws_ = []
+    for i, (M, N) in enumerate(W.WEIGHT_SHAPES):
+        gen.manual_seed(5000 + i)
+        w = (torch.randn((M, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        ws_.append((w, nv.weight_quant_2d(w), nv.w2d_workspace(M, N, dev)))
+    ms = _time_graph(torch, lambda i: [nv.weight_quant_2d(w, workspace=wk, out=o) for (w, o, wk) in ws_], 1, 10)
+    b = sum(M * N for (M, N) in W.WEIGHT_SHAPES) * W2D_BYTES_PER_ELEM
+    rows["weight_quant_2d"] = {"GB/s": b / ms / 1e6, "ms_all_six": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+
+    # activations 7040 x 3072, 1-D blocks
+    gen.manual_seed(5100)
+    acts = [torch.randn((T_CHUNK, 1, 3072), generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
+    aouts = [nv.kv_smooth_quant(a, False) for a in acts]
+    aws = nv.kv_workspace(T_CHUNK, 1, 3072, 1, dev)
+    ms = _time_graph(torch, lambda i: nv.kv_smooth_quant(acts[i % 4], False, workspace=aws, out=aouts[i % 4]), 8, 20)
+    b = T_CHUNK * 3072 * QUANT_BYTES_PER_ELEM
+    rows["activation_quant_1d"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+
+    # single K tensor (smooth+quant alone, no V to overlap with)
+    kx = [xs[2 * i] for i in range(4)]
+    kouts = [nv.kv_smooth_quant(k, True) for k in kx]
+    kws = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 1, dev)
+    ms = _time_graph(torch, lambda i: nv.kv_smooth_quant(kx[i % 4], True, workspace=kws, out=kouts[i % 4]), 8, 20)
+    b = T_CHUNK * HEADS * HEAD_DIM * QUANT_BYTES_PER_ELEM
+    rows["k_only_smooth_quant"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    torch.cuda.synchronize()
+    return rows
+
+
+def main():
+    args = parse()
+    ws, rank, _ = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

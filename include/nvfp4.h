@@ -1,0 +1,184 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 KV-cache quantizer.
+ *
+ * The method is the KV-cache write of "LongLive-2.0: An NVFP4 Parallel
+ * Infrastructure for Long Video Generation" (summary page,
+ * paper.rainbus.top/paper/2605.18739):
+ *   - inference pipeline, step 7: each chunk of F_c = 8 latent frames
+ *     (T_c = F_c * L_f tokens) has K smoothed, K <- K - mean(K) over the
+ *     chunk's tokens, and is then quantized into the NVFP4 KV cache with
+ *     4/6 adaptive block scales;
+ *   - "full-stack NVFP4" paragraph: Four-Over-Six compares the MSE of two
+ *     candidate FP8 block scales, keeping the +-6 range or switching to +-4;
+ *   - training pipeline, step 4: 2-D block scales for weights, 1-D block
+ *     scales for activations.
+ * NVFP4: E2M1 elements {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6} in blocks of
+ * 16, one E4M3 scale per block (round-to-nearest-even, saturating at 448) and
+ * one fp32 scale per tensor, g = amax / 2688 (2688 = 6 * 448).  Per block the
+ * candidate scales e_M = E4M3(a_b * fl(1 / fl(M * g))), M in {6, 4}, map the
+ * block's absolute maximum a_b to 6 and to 4; the block is quantized under
+ * both (y = Z * fl(1 / fl(E_M * g)), codes round to nearest even, sign kept),
+ * each candidate's error is E_M^2 * sum (y - Q)^2 (fused multiply-add per
+ * element, element order), and the lower error wins, ties going to 6.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers name GPU global memory owned by the caller; the library
+ *     never allocates, frees, synchronizes or prints, and keeps no mutable
+ *     global state (it is safe to call from several host threads).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously; outputs are valid once the stream
+ *     reaches that point.
+ *   - Argument errors are returned synchronously and nothing is enqueued.
+ *     A failed launch returns NVFP4_ECUDA (cudaGetLastError is consumed).
+ *   - Data-dependent conditions are written by the kernels to *dev_status (a
+ *     device int, optional): NVFP4_DEV_OK, or NVFP4_DEV_NONFINITE when a
+ *     smoothed value is NaN or infinite.  Then every scale byte is 0x7F
+ *     (E4M3 NaN), every code 0 and the tensor scale NaN, so a later dequant
+ *     yields NaN rather than plausible numbers.
+ *   - Pointers to element data, codes, scales and outputs must be 16-byte
+ *     aligned (NVFP4_EALIGN otherwise); float pointers 4-byte aligned.
+ *   - Sizes are 64-bit; T may be 0 (nothing but the tensor scale, 0, and the
+ *     mean, 0, is written).
+ *
+ * Layouts (row-major):
+ *   input  x       [T][H][D]   bf16 or fp32, D contiguous, D % 16 == 0
+ *   codes          [T][H][D/2] byte j of a row = element 2j (low nibble) and
+ *                              element 2j+1 (high nibble), E2M1 sign-magnitude
+ *   scales         [T][H][D/16] one E4M3 byte per 16 consecutive d
+ *   tensor_scale   one fp32 per quantized tensor (g)
+ *   mean           [H][D] fp32 per chunk (the mean that K-smoothing removed)
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_EINVAL = 1,     /* a required pointer is NULL, or an enum/flag is out of range */
+  NVFP4_ESHAPE = 2,     /* a size is out of range (D % 16, H <= 0, T < 0, M/N % 16, ...) */
+  NVFP4_EALIGN = 3,     /* a pointer is not aligned as required */
+  NVFP4_EWORKSPACE = 4, /* workspace NULL, too small, or not 256-byte aligned */
+  NVFP4_ECUDA = 5       /* a CUDA runtime call or kernel launch failed */
+} nvfp4_status;
+
+typedef enum nvfp4_in_dtype {
+  NVFP4_IN_BF16 = 0, /* bfloat16 elements, widened to fp32 exactly */
+  NVFP4_IN_FP32 = 1  /* fp32 elements */
+} nvfp4_in_dtype;
+
+#define NVFP4_DEV_OK 0
+#define NVFP4_DEV_NONFINITE 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4_status_string(nvfp4_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int nvfp4_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* KV chunk quantizer (LongLive-2.0 summary page, inference step 7, and the */
+/* "full-stack NVFP4" paragraph).                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace one nvfp4_kv_smooth_quant call needs for this
+ * shape on the current device.  Returns 0 for invalid shapes. */
+size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D);
+
+/* Quantize one chunk tensor x[T][H][D] into NVFP4 with Four-Over-Six scales.
+ *   x            device, [T][H][D] of `dt`, 16-byte aligned
+ *   smooth       1: K-smoothing -- subtract mean[h][d] = (sum over the chunk's
+ *                T tokens of x[t][h][d]) / T, rounded once to fp32, before
+ *                quantizing (keys); 0: no smoothing (values, activations)
+ *   mean_in      device [H*D] or NULL; when set (smooth must be 1) it is used
+ *                as the mean instead of computing it
+ *   mean_out     device [H*D] or NULL (smooth must be 1); receives the mean used
+ *   codes        device [T*H*D/2] output, packed E2M1 nibbles
+ *   scales       device [T*H*D/16] output, E4M3 bytes
+ *   tensor_scale device [1] output, g = amax / 2688 of the smoothed tensor
+ *   dev_status   device int or NULL, see the conventions above
+ *   workspace    device scratch of at least nvfp4_kv_workspace_bytes(T, H, D)
+ *                bytes, 256-byte aligned; contents need no initialization
+ *   stream       cudaStream_t
+ * Errors: NVFP4_EINVAL (NULL x/codes/scales/tensor_scale, bad dt or smooth,
+ * mean pointers with smooth == 0), NVFP4_ESHAPE, NVFP4_EALIGN,
+ * NVFP4_EWORKSPACE, NVFP4_ECUDA. */
+nvfp4_status nvfp4_kv_smooth_quant(const void* x, nvfp4_in_dtype dt, int64_t T, int H, int D, int smooth,
+                                   const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
+                                   float* tensor_scale, int* dev_status, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* One tensor of a batched call (all tensors of a batch share T, H, D, dt). */
+typedef struct nvfp4_kv_job {
+  const void* x;        /* device [T][H][D] input */
+  int smooth;           /* 1 = K (smoothed), 0 = V */
+  const float* mean_in; /* device [H*D] or NULL */
+  float* mean_out;      /* device [H*D] or NULL */
+  uint8_t* codes;       /* device [T*H*D/2] */
+  uint8_t* scales;      /* device [T*H*D/16] */
+  float* tensor_scale;  /* device [1] */
+} nvfp4_kv_job;
+
+/* Workspace for nvfp4_kv_smooth_quant_batched with n_jobs tensors. */
+size_t nvfp4_kv_batched_workspace_bytes(int n_jobs, int64_t T, int H, int D);
+
+/* Quantize n_jobs independent chunk tensors (e.g. K and V of every layer of
+ * one chunk) in one enqueue; each job gets exactly the result the single
+ * call would give it.  `jobs` is a HOST array read before the call returns.
+ * *dev_status is the OR over jobs.  Errors as nvfp4_kv_smooth_quant, plus
+ * NVFP4_EINVAL for n_jobs < 1 or a bad job. */
+nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt,
+                                           int64_t T, int H, int D, int* dev_status, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/* Dequantize an NVFP4 KV cache back to bf16 (the cache read that attention
+ * performs; LongLive-2.0 summary page, inference steps 7 and 9).
+ *   codes, scales     device, layouts above, for T tokens
+ *   tensor_scale      device [G], G = ceil(T / tokens_per_group): token t uses
+ *                     tensor_scale[t / tokens_per_group] (one chunk: pass
+ *                     tokens_per_group = T; a cache assembled from frames of
+ *                     different chunks: per-frame groups, e.g. 880)
+ *   mean              device [G][H][D] or NULL; when set the group's mean is
+ *                     added back (undoes K-smoothing)
+ *   out_bf16          device [T][H][D] bf16 output:
+ *                     bf16_rne(fl(fl(Q * fl(E * g)) + mean))
+ * Errors: NVFP4_EINVAL, NVFP4_ESHAPE (tokens_per_group < 1 ...), NVFP4_EALIGN,
+ * NVFP4_ECUDA. */
+nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                              const float* mean, int64_t tokens_per_group, int64_t T, int H, int D,
+                              void* out_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weights with 16x16 2-D blocks (LongLive-2.0 summary page, training        */
+/* pipeline step 4: "2-D block scales for weights").                         */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace for nvfp4_weight_quant_2d on an M x N matrix (current device). */
+size_t nvfp4_w2d_workspace_bytes(int64_t M, int64_t N);
+
+/* Quantize w[M][N] (M, N multiples of 16) with one E4M3 scale per 16x16 tile
+ * and Four-Over-Six selection; each tile's error sums its 256 elements in
+ * row-major order.  No smoothing.
+ *   codes        device [M][N/2], same nibble packing as the KV codes
+ *   scales       device [M/16][N/16] E4M3 bytes
+ *   tensor_scale device [1]
+ * Errors as nvfp4_kv_smooth_quant. */
+nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,
+                                   uint8_t* scales, float* tensor_scale, int* dev_status, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Dequantize 16x16-tiled NVFP4 weights to bf16 out[M][N]
+ * (bf16_rne(fl(Q * fl(E * g)))).  tensor_scale is device [1]. */
+nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                                     int64_t M, int64_t N, void* out_bf16, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,215 @@
+"""NVFP4 KV-cache quantizer for GB300 (sm_103a): thin PyTorch-facing binding.
+
+Every computation runs in the CUDA library (``_build/libnvfp4_gb300.so``,
+C ABI in ``include/nvfp4.h``); this module only allocates output tensors with
+torch, marshals pointers and sizes, and raises on a non-OK status.  There is no
+CPU path: without the built library every call raises.
+
+Method: "LongLive-2.0: An NVFP4 Parallel Infrastructure for Long Video
+Generation" (summary page) -- inference step 7 (per-chunk K-smoothing, then
+Four-Over-Six NVFP4 KV cache) and training step 4 (2-D block scales for
+weights, 1-D for activations).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import NamedTuple, Optional, Sequence
+
+from . import _lib
+from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job
+
+__all__ = [
+    "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
+    "kv_dequant", "w2d_workspace", "weight_quant_2d", "weight_dequant_2d", "load_library",
+]
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    return _lib.load()
+
+
+class KvQuantized(NamedTuple):
+    codes: "torch.Tensor"         # uint8 [T, H, D/2]
+    scales: "torch.Tensor"        # uint8 [T, H, D/16] (E4M3 bytes)
+    tensor_scale: "torch.Tensor"  # float32 [1]
+    mean: Optional["torch.Tensor"]  # float32 [H, D] (smoothed tensors) or None
+    status: "torch.Tensor"        # int32 [1] device status word
+
+
+class W2dQuantized(NamedTuple):
+    codes: "torch.Tensor"         # uint8 [M, N/2]
+    scales: "torch.Tensor"        # uint8 [M/16, N/16]
+    tensor_scale: "torch.Tensor"  # float32 [1]
+    status: "torch.Tensor"        # int32 [1]
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(x) -> int:
+    torch = _torch()
+    if x.dtype == torch.bfloat16:
+        return NVFP4_IN_BF16
+    if x.dtype == torch.float32:
+        return NVFP4_IN_FP32
+    raise TypeError(f"input must be bfloat16 or float32, got {x.dtype}")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def kv_workspace(T: int, H: int, D: int, n_jobs: int = 1, device=None):
+    """Allocate (with torch) the device workspace a KV quantize call of this shape needs."""
+    torch = _torch()
+    nbytes = _lib.nvfp4_kv_batched_workspace_bytes(n_jobs, T, H, D)
+    if nbytes == 0:
+        raise NVFP4Error(_lib.NVFP4_ESHAPE, "kv_workspace")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _kv_outputs(T, H, D, smooth, device):
+    torch = _torch()
+    codes = torch.empty((T, H, D // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty((T, H, D // 16), dtype=torch.uint8, device=device)
+    g = torch.empty(1, dtype=torch.float32, device=device)
+    mean = torch.empty((H, D), dtype=torch.float32, device=device) if smooth else None
+    return codes, scales, g, mean
+
+
+def kv_smooth_quant(x, smooth: bool, mean_in=None, workspace=None, out: Optional[KvQuantized] = None,
+                    stream=None) -> KvQuantized:
+    """Quantize x[T, H, D] (bf16 or fp32, CUDA) into NVFP4 with Four-Over-Six block scales.
+
+    smooth=True subtracts the per-(head, channel) token mean first (keys); the mean used is
+    returned.  Asynchronous on `stream`; `status` is a device int (NVFP4_DEV_*).
+    """
+    torch = _torch()
+    _check_cuda(x, mean_in)
+    T, H, D = x.shape
+    if out is None:
+        codes, scales, g, mean = _kv_outputs(T, H, D, smooth, x.device)
+        status = torch.empty(1, dtype=torch.int32, device=x.device)
+    else:
+        codes, scales, g, mean, status = out
+    if workspace is None:
+        workspace = kv_workspace(T, H, D, 1, x.device)
+    st = _lib.nvfp4_kv_smooth_quant(_ptr(x), _dt(x), T, H, D, int(bool(smooth)), _ptr(mean_in),
+                                    _ptr(mean) if smooth else None, _ptr(codes), _ptr(scales), _ptr(g),
+                                    _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_kv_smooth_quant")
+    return KvQuantized(codes, scales, g, mean, status)
+
+
+def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None, outs=None, status=None,
+                            stream=None):
+    """Quantize several same-shape chunk tensors (e.g. K and V of every layer) in one enqueue.
+
+    Returns (list of KvQuantized, status) with one shared device status word (OR over tensors).
+    """
+    torch = _torch()
+    n = len(xs)
+    if n == 0 or len(smooth) != n:
+        raise ValueError("need one smooth flag per tensor")
+    x0 = xs[0]
+    T, H, D = x0.shape
+    for x in xs:
+        _check_cuda(x)
+        if tuple(x.shape) != (T, H, D) or x.dtype != x0.dtype:
+            raise ValueError("all tensors of a batch share shape and dtype")
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=x0.device)
+    if outs is None:
+        outs = []
+        for sm in smooth:
+            c, s, g, m = _kv_outputs(T, H, D, sm, x0.device)
+            outs.append(KvQuantized(c, s, g, m, status))
+    if workspace is None:
+        workspace = kv_workspace(T, H, D, n, x0.device)
+    jobs = (nvfp4_kv_job * n)()
+    for i, (x, sm, o) in enumerate(zip(xs, smooth, outs)):
+        jobs[i].x = x.data_ptr()
+        jobs[i].smooth = int(bool(sm))
+        jobs[i].mean_in = None
+        jobs[i].mean_out = o.mean.data_ptr() if (sm and o.mean is not None) else None
+        jobs[i].codes = o.codes.data_ptr()
+        jobs[i].scales = o.scales.data_ptr()
+        jobs[i].tensor_scale = o.tensor_scale.data_ptr()
+    st = _lib.nvfp4_kv_smooth_quant_batched(jobs, n, _dt(x0), T, H, D, _ptr(status), _ptr(workspace),
+                                            workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_kv_smooth_quant_batched")
+    return outs, status
+
+
+def kv_dequant(codes, scales, tensor_scale, mean=None, tokens_per_group: Optional[int] = None, out=None,
+               stream=None):
+    """Dequantize NVFP4 codes/scales [T, H, D/2] / [T, H, D/16] to bf16 [T, H, D]."""
+    torch = _torch()
+    _check_cuda(codes, scales, tensor_scale, mean)
+    T, H, D2 = codes.shape
+    D = 2 * D2
+    tpg = T if tokens_per_group is None else int(tokens_per_group)
+    tpg = max(tpg, 1)
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=codes.device)
+    st = _lib.nvfp4_kv_dequant(_ptr(codes), _ptr(scales), _ptr(tensor_scale), _ptr(mean), tpg, T, H, D, _ptr(out),
+                               _stream(stream))
+    _lib.check(st, "nvfp4_kv_dequant")
+    return out
+
+
+def w2d_workspace(M: int, N: int, device=None):
+    torch = _torch()
+    nbytes = _lib.nvfp4_w2d_workspace_bytes(M, N)
+    if nbytes == 0:
+        raise NVFP4Error(_lib.NVFP4_ESHAPE, "w2d_workspace")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def weight_quant_2d(w, workspace=None, out: Optional[W2dQuantized] = None, stream=None) -> W2dQuantized:
+    """Quantize a weight matrix w[M, N] with 16x16 NVFP4 tiles and Four-Over-Six scales."""
+    torch = _torch()
+    _check_cuda(w)
+    M, N = w.shape
+    if out is None:
+        codes = torch.empty((M, N // 2), dtype=torch.uint8, device=w.device)
+        scales = torch.empty((M // 16, N // 16), dtype=torch.uint8, device=w.device)
+        g = torch.empty(1, dtype=torch.float32, device=w.device)
+        status = torch.empty(1, dtype=torch.int32, device=w.device)
+    else:
+        codes, scales, g, status = out
+    if workspace is None:
+        workspace = w2d_workspace(M, N, w.device)
+    st = _lib.nvfp4_weight_quant_2d(_ptr(w), _dt(w), M, N, _ptr(codes), _ptr(scales), _ptr(g), _ptr(status),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_weight_quant_2d")
+    return W2dQuantized(codes, scales, g, status)
+
+
+def weight_dequant_2d(codes, scales, tensor_scale, out=None, stream=None):
+    """Dequantize 16x16-tiled NVFP4 weights to bf16 [M, N]."""
+    torch = _torch()
+    _check_cuda(codes, scales, tensor_scale)
+    M, N2 = codes.shape
+    if out is None:
+        out = torch.empty((M, 2 * N2), dtype=torch.bfloat16, device=codes.device)
+    st = _lib.nvfp4_weight_dequant_2d(_ptr(codes), _ptr(scales), _ptr(tensor_scale), M, 2 * N2, _ptr(out),
+                                      _stream(stream))
+    _lib.check(st, "nvfp4_weight_dequant_2d")
+    return out

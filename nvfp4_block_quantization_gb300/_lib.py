@@ -1,0 +1,136 @@
+"""ctypes binding of the C ABI in include/nvfp4.h (argument marshalling only).
+
+Every function here has the name and argument order of its C entry point.  The
+library must have been built (``nvfp4_block_quantization_gb300.build.build()``
+or ``__graft_entry__.build()``); there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+NVFP4_OK, NVFP4_EINVAL, NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA = range(6)
+NVFP4_IN_BF16, NVFP4_IN_FP32 = 0, 1
+NVFP4_DEV_OK, NVFP4_DEV_NONFINITE = 0, 1
+
+# Every entry point declared in include/nvfp4.h.
+EXPORTS = (
+    "nvfp4_status_string",
+    "nvfp4_version",
+    "nvfp4_kv_workspace_bytes",
+    "nvfp4_kv_smooth_quant",
+    "nvfp4_kv_batched_workspace_bytes",
+    "nvfp4_kv_smooth_quant_batched",
+    "nvfp4_kv_dequant",
+    "nvfp4_w2d_workspace_bytes",
+    "nvfp4_weight_quant_2d",
+    "nvfp4_weight_dequant_2d",
+)
+
+
+class nvfp4_kv_job(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("smooth", ctypes.c_int),
+        ("mean_in", ctypes.c_void_p),
+        ("mean_out", ctypes.c_void_p),
+        ("codes", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+    ]
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the CUDA library; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"NVFP4 CUDA library not built ({path} missing): run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.nvfp4_status_string.argtypes = [i32]
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_version.argtypes = []
+    lib.nvfp4_version.restype = i32
+    lib.nvfp4_kv_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.nvfp4_kv_workspace_bytes.restype = sz
+    lib.nvfp4_kv_smooth_quant.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.nvfp4_kv_smooth_quant.restype = i32
+    lib.nvfp4_kv_batched_workspace_bytes.argtypes = [i32, i64, i32, i32]
+    lib.nvfp4_kv_batched_workspace_bytes.restype = sz
+    lib.nvfp4_kv_smooth_quant_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp,
+                                                  sz, vp]
+    lib.nvfp4_kv_smooth_quant_batched.restype = i32
+    lib.nvfp4_kv_dequant.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, vp]
+    lib.nvfp4_kv_dequant.restype = i32
+    lib.nvfp4_w2d_workspace_bytes.argtypes = [i64, i64]
+    lib.nvfp4_w2d_workspace_bytes.restype = sz
+    lib.nvfp4_weight_quant_2d.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
+    lib.nvfp4_weight_quant_2d.restype = i32
+    lib.nvfp4_weight_dequant_2d.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    lib.nvfp4_weight_dequant_2d.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().nvfp4_status_string(int(status)).decode()
+
+
+def check(status: int, what: str):
+    if status != NVFP4_OK:
+        raise NVFP4Error(status, what)
+
+
+def nvfp4_version():
+    return load().nvfp4_version()
+
+
+def nvfp4_kv_workspace_bytes(T, H, D):
+    return load().nvfp4_kv_workspace_bytes(T, H, D)
+
+
+def nvfp4_kv_smooth_quant(x, dt, T, H, D, smooth, mean_in, mean_out, codes, scales, tensor_scale, dev_status,
+                          workspace, workspace_bytes, stream):
+    return load().nvfp4_kv_smooth_quant(x, dt, T, H, D, smooth, mean_in, mean_out, codes, scales, tensor_scale,
+                                        dev_status, workspace, workspace_bytes, stream)
+
+
+def nvfp4_kv_batched_workspace_bytes(n_jobs, T, H, D):
+    return load().nvfp4_kv_batched_workspace_bytes(n_jobs, T, H, D)
+
+
+def nvfp4_kv_smooth_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream):
+    return load().nvfp4_kv_smooth_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes,
+                                                stream)
+
+
+def nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream):
+    return load().nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream)
+
+
+def nvfp4_w2d_workspace_bytes(M, N):
+    return load().nvfp4_w2d_workspace_bytes(M, N)
+
+
+def nvfp4_weight_quant_2d(w, dt, M, N, codes, scales, tensor_scale, dev_status, workspace, workspace_bytes, stream):
+    return load().nvfp4_weight_quant_2d(w, dt, M, N, codes, scales, tensor_scale, dev_status, workspace,
+                                        workspace_bytes, stream)
+
+
+def nvfp4_weight_dequant_2d(codes, scales, tensor_scale, M, N, out_bf16, stream):
+    return load().nvfp4_weight_dequant_2d(codes, scales, tensor_scale, M, N, out_bf16, stream)

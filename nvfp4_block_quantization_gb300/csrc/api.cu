@@ -1,0 +1,242 @@
+// api.cu -- the extern "C" entry points declared in include/nvfp4.h.
+//
+// Every entry point validates its arguments synchronously (nothing is
+// enqueued on an error), carves its workspace, and enqueues the kernels on the
+// caller's stream.  No allocation, no synchronization, no printing.
+#include <algorithm>
+#include <cstring>
+
+#include "../../include/nvfp4.h"
+#include "kv_kernels.cuh"
+
+namespace {
+
+using namespace nvfp4;
+
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool kv_shape_ok(int64_t T, int H, int D) {
+  if (T < 0 || H < 1 || D < 16 || (D % 16) != 0) return false;
+  const int64_t C = (int64_t)H * D;
+  if (C > (1 << 26)) return false;                       // channel index fits in int comfortably
+  if (T > 0 && C > ((int64_t)1 << 60) / T) return false;  // element count fits in int64 with headroom
+  return true;
+}
+
+struct KvPlan {
+  KvGeom geo;
+  size_t part_bytes, amax_bytes, mean_bytes, job_bytes;
+};
+
+KvPlan kv_plan(int64_t T, int H, int D, int sms) {
+  KvPlan p;
+  KvGeom& g = p.geo;
+  g.T = T;
+  g.C = H * D;
+  const int ctile = std::min(g.C, kCTile);
+  g.nctiles = (g.C + kCTile - 1) / kCTile;
+  g.ctile_threads = std::max(32, ((ctile / 8) + 31) / 32 * 32);
+  const int64_t target = std::max<int64_t>(1, (int64_t)std::max(sms, 1) / g.nctiles);
+  const int64_t want = std::min<int64_t>(std::max<int64_t>(T, 1), target);
+  g.rows_per_chunk = (int)((std::max<int64_t>(T, 1) + want - 1) / want);
+  g.nchunks = (int)((std::max<int64_t>(T, 1) + g.rows_per_chunk - 1) / g.rows_per_chunk);
+  g.nfin = (g.C + 255) / 256;
+  p.part_bytes = align_up((size_t)g.nchunks * g.C * sizeof(float4), kWsAlign);
+  p.amax_bytes = align_up((size_t)std::max(g.nchunks * g.nctiles, g.nfin) * sizeof(float), kWsAlign);
+  p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);
+  p.job_bytes = p.part_bytes + p.amax_bytes + p.mean_bytes;
+  return p;
+}
+
+int quant_grid(int64_t nblocks, int sms) {
+  const int64_t per_cta = 256;
+  const int64_t need = (nblocks + per_cta - 1) / per_cta;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)std::max(sms, 1) * 8));
+}
+
+nvfp4_status check_job(const nvfp4_kv_job& j, int64_t T) {
+  if (!j.tensor_scale) return NVFP4_EINVAL;
+  if (T > 0 && (!j.x || !j.codes || !j.scales)) return NVFP4_EINVAL;
+  if (j.smooth != 0 && j.smooth != 1) return NVFP4_EINVAL;
+  if (!j.smooth && (j.mean_in || j.mean_out)) return NVFP4_EINVAL;
+  if (!aligned(j.x, 16) || !aligned(j.codes, 16) || !aligned(j.scales, 16)) return NVFP4_EALIGN;
+  if (!aligned(j.tensor_scale, 4) || !aligned(j.mean_in, 4) || !aligned(j.mean_out, 4)) return NVFP4_EALIGN;
+  return NVFP4_OK;
+}
+
+nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H, int D,
+                    int* dev_status, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!jobs || n_jobs < 1) return NVFP4_EINVAL;
+  if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
+  if (!kv_shape_ok(T, H, D)) return NVFP4_ESHAPE;
+  for (int i = 0; i < n_jobs; ++i) {
+    nvfp4_status st = check_job(jobs[i], T);
+    if (st != NVFP4_OK) return st;
+  }
+  if (!aligned(dev_status, 4)) return NVFP4_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ECUDA;
+  const KvPlan plan = kv_plan(T, H, D, sms);
+  const size_t need = plan.job_bytes * (size_t)n_jobs;
+  if (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)) return NVFP4_EWORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nblocks = T * (int64_t)(plan.geo.C / 16);
+  const int qctas = quant_grid(nblocks, sms);
+  char* ws = static_cast<char*>(workspace);
+  for (int first = 0; first < n_jobs; first += kMaxJobs) {
+    KvBatch b;
+    std::memset(&b, 0, sizeof(b));
+    b.n = std::min(kMaxJobs, n_jobs - first);
+    for (int i = 0; i < b.n; ++i) {
+      const nvfp4_kv_job& src = jobs[first + i];
+      KvJob& j = b.job[i];
+      char* base = ws + plan.job_bytes * (size_t)(first + i);
+      j.x = src.x;
+      j.smooth = src.smooth;
+      j.mean_in = src.mean_in;
+      j.mean_out = src.mean_out;
+      j.codes = src.codes;
+      j.scales = src.scales;
+      j.tensor_scale = src.tensor_scale;
+      j.part = reinterpret_cast<float4*>(base);
+      j.amax_part = reinterpret_cast<float*>(base + plan.part_bytes);
+      j.mean = reinterpret_cast<float*>(base + plan.part_bytes + plan.amax_bytes);
+      j.namax = src.smooth ? plan.geo.nfin : plan.geo.nchunks * plan.geo.nctiles;
+    }
+    // The status word is reset by the first group's first kernel; every group ORs its flags into it.
+    cudaError_t e = launch_kv_quant(b, plan.geo, dt == NVFP4_IN_BF16, first == 0 ? dev_status : nullptr,
+                                    dev_status, qctas, s);
+    if (e != cudaSuccess) return NVFP4_ECUDA;
+  }
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_EINVAL: return "NVFP4_EINVAL: invalid argument";
+    case NVFP4_ESHAPE: return "NVFP4_ESHAPE: unsupported shape";
+    case NVFP4_EALIGN: return "NVFP4_EALIGN: misaligned pointer";
+    case NVFP4_EWORKSPACE: return "NVFP4_EWORKSPACE: workspace missing, too small or misaligned";
+    case NVFP4_ECUDA: return "NVFP4_ECUDA: CUDA error";
+  }
+  return "NVFP4_UNKNOWN";
+}
+
+int nvfp4_version(void) { return 100; }
+
+size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D) {
+  if (!kv_shape_ok(T, H, D)) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  return kv_plan(T, H, D, sms).job_bytes;
+}
+
+size_t nvfp4_kv_batched_workspace_bytes(int n_jobs, int64_t T, int H, int D) {
+  if (n_jobs < 1) return 0;
+  return nvfp4_kv_workspace_bytes(T, H, D) * (size_t)n_jobs;
+}
+
+nvfp4_status nvfp4_kv_smooth_quant(const void* x, nvfp4_in_dtype dt, int64_t T, int H, int D, int smooth,
+                                   const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
+                                   float* tensor_scale, int* dev_status, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  nvfp4_kv_job j;
+  j.x = x;
+  j.smooth = smooth;
+  j.mean_in = mean_in;
+  j.mean_out = mean_out;
+  j.codes = codes;
+  j.scales = scales;
+  j.tensor_scale = tensor_scale;
+  return kv_run(&j, 1, dt, T, H, D, dev_status, workspace, workspace_bytes, stream);
+}
+
+nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T,
+                                           int H, int D, int* dev_status, void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream);
+}
+
+nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                              const float* mean, int64_t tokens_per_group, int64_t T, int H, int D, void* out_bf16,
+                              void* stream) {
+  if (!kv_shape_ok(T, H, D)) return NVFP4_ESHAPE;
+  if (tokens_per_group < 1) return NVFP4_ESHAPE;
+  if (!tensor_scale) return NVFP4_EINVAL;
+  if (T > 0 && (!codes || !scales || !out_bf16)) return NVFP4_EINVAL;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(out_bf16, 16)) return NVFP4_EALIGN;
+  if (!aligned(tensor_scale, 4) || !aligned(mean, 4)) return NVFP4_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ECUDA;
+  const int C = H * D;
+  const int64_t nblocks = T * (int64_t)(C / 16);
+  const int ctas = quant_grid(nblocks, sms);
+  cudaError_t e = launch_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, C, out_bf16, ctas,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
+}
+
+size_t nvfp4_w2d_workspace_bytes(int64_t M, int64_t N) {
+  if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  return align_up((size_t)sms * 4 * sizeof(float), kWsAlign);
+}
+
+nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,
+                                   uint8_t* scales, float* tensor_scale, int* dev_status, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
+  if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return NVFP4_ESHAPE;
+  if (M > 0 && N > ((int64_t)1 << 60) / M) return NVFP4_ESHAPE;
+  if (!tensor_scale) return NVFP4_EINVAL;
+  if (M > 0 && (!w || !codes || !scales)) return NVFP4_EINVAL;
+  if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVFP4_EALIGN;
+  if (!aligned(tensor_scale, 4) || !aligned(dev_status, 4)) return NVFP4_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ECUDA;
+  const size_t need = align_up((size_t)sms * 4 * sizeof(float), kWsAlign);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)) return NVFP4_EWORKSPACE;
+  W2dGeom geo;
+  geo.M = M;
+  geo.N = N;
+  geo.amax_ctas = sms * 4;
+  const int64_t ntiles = (M / 16) * (N / 16);
+  const int qctas = quant_grid(ntiles, sms);
+  cudaError_t e = launch_w2d_quant(w, dt == NVFP4_IN_BF16, geo, codes, scales, tensor_scale, dev_status,
+                                   static_cast<float*>(workspace), qctas, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
+}
+
+nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                                     int64_t M, int64_t N, void* out_bf16, void* stream) {
+  if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return NVFP4_ESHAPE;
+  if (!tensor_scale) return NVFP4_EINVAL;
+  if (M > 0 && (!codes || !scales || !out_bf16)) return NVFP4_EINVAL;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(out_bf16, 16) || !aligned(tensor_scale, 4))
+    return NVFP4_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ECUDA;
+  const int ctas = quant_grid(M * N / 16, sms);
+  cudaError_t e = launch_w2d_dequant(codes, scales, tensor_scale, M, N, out_bf16, ctas,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
+}
+
+}  // extern "C"

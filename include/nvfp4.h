@@ -35,8 +35,9 @@
  *     smoothed value is NaN or infinite.  Then every scale byte is 0x7F
  *     (E4M3 NaN), every code 0 and the tensor scale NaN, so a later dequant
  *     yields NaN rather than plausible numbers.
- *   - Pointers to element data, codes, scales and outputs must be 16-byte
- *     aligned (NVFP4_EALIGN otherwise); float pointers 4-byte aligned.
+ *   - Quantizer inputs x must be 32-byte aligned; codes, scales and dequant
+ *     outputs 16-byte aligned (NVFP4_EALIGN otherwise); float pointers 4-byte
+ *     aligned.
  *   - Sizes are 64-bit; T may be 0 (nothing but the tensor scale, 0, and the
  *     mean, 0, is written).
  *
@@ -73,7 +74,8 @@ typedef enum nvfp4_in_dtype {
 } nvfp4_in_dtype;
 
 #define NVFP4_DEV_OK 0
-#define NVFP4_DEV_NONFINITE 1
+#define NVFP4_DEV_NONFINITE 1 /* bit: a smoothed value was NaN or infinite */
+#define NVFP4_DEV_TIMEOUT 2   /* bit: a bounded cross-CTA wait ran out */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvfp4_status_string(nvfp4_status s);
@@ -91,7 +93,7 @@ int nvfp4_version(void);
 size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D);
 
 /* Quantize one chunk tensor x[T][H][D] into NVFP4 with Four-Over-Six scales.
- *   x            device, [T][H][D] of `dt`, 16-byte aligned
+ *   x            device, [T][H][D] of `dt`, 32-byte aligned
  *   smooth       1: K-smoothing -- subtract mean[h][d] = (sum over the chunk's
  *                T tokens of x[t][h][d]) / T, rounded once to fp32, before
  *                quantizing (keys); 0: no smoothing (values, activations)
@@ -103,11 +105,19 @@ size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D);
  *   tensor_scale device [1] output, g = amax / 2688 of the smoothed tensor
  *   dev_status   device int or NULL, see the conventions above
  *   workspace    device scratch of at least nvfp4_kv_workspace_bytes(T, H, D)
- *                bytes, 256-byte aligned; contents need no initialization
+ *                bytes, 256-byte aligned, ZERO-FILLED before its first use
+ *                (e.g. cudaMemset).  It holds the cross-CTA counters of the
+ *                fused kernel, which every completed call returns to zero, so
+ *                the same workspace serves later calls on one stream without
+ *                clearing.  Calls that share a workspace must not overlap.
  *   stream       cudaStream_t
+ * Implementation: one persistent cooperative kernel (one CTA per SM).  Its
+ * cross-CTA waits are bounded (about 2 s); if one runs out, *dev_status gets
+ * NVFP4_DEV_TIMEOUT, the affected outputs are left unwritten and the
+ * workspace must be zero-filled again before reuse.
  * Errors: NVFP4_EINVAL (NULL x/codes/scales/tensor_scale, bad dt or smooth,
- * mean pointers with smooth == 0), NVFP4_ESHAPE, NVFP4_EALIGN,
- * NVFP4_EWORKSPACE, NVFP4_ECUDA. */
+ * mean pointers with smooth == 0), NVFP4_ESHAPE (also T*H*D > 2^46),
+ * NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA. */
 nvfp4_status nvfp4_kv_smooth_quant(const void* x, nvfp4_in_dtype dt, int64_t T, int H, int D, int smooth,
                                    const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
                                    float* tensor_scale, int* dev_status, void* workspace,

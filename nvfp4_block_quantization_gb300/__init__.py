@@ -76,12 +76,16 @@ def _check_cuda(*ts):
 
 
 def kv_workspace(T: int, H: int, D: int, n_jobs: int = 1, device=None):
-    """Allocate (with torch) the device workspace a KV quantize call of this shape needs."""
+    """Allocate (with torch) the zero-filled device workspace a KV quantize call of this shape needs.
+
+    The library's counters in it return to zero at the end of every call, so it can be reused by
+    later calls on the same stream without clearing.
+    """
     torch = _torch()
     nbytes = _lib.nvfp4_kv_batched_workspace_bytes(n_jobs, T, H, D)
     if nbytes == 0:
         raise NVFP4Error(_lib.NVFP4_ESHAPE, "kv_workspace")
-    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
 def _kv_outputs(T, H, D, smooth, device):

@@ -6,7 +6,7 @@
 #include <algorithm>
 #include <cstring>
 
-#include "../../include/nvfp4.h"
+#include "nvfp4.h"
 #include "kv_kernels.cuh"
 
 namespace {
@@ -28,35 +28,55 @@ int device_sms() {
 bool kv_shape_ok(int64_t T, int H, int D) {
   if (T < 0 || H < 1 || D < 16 || (D % 16) != 0) return false;
   const int64_t C = (int64_t)H * D;
-  if (C > (1 << 26)) return false;                       // channel index fits in int comfortably
-  if (T > 0 && C > ((int64_t)1 << 60) / T) return false;  // element count fits in int64 with headroom
+  if (C > (1 << 24)) return false;                        // channel indices fit in int with headroom
+  if (T > 0 && C > ((int64_t)1 << 46) / T) return false;  // unit arithmetic (units * CTAs) fits in int64
+  if (T > (int64_t)0x7fffff00) return false;               // TMA row coordinates are 32-bit
   return true;
 }
 
+// Plan of one fused launch: partition geometry and the workspace layout.
+//   header (256 B): exit counter, status flags
+//   per job: counters (2 + ngroups words), mean [C], partials [P][smax][W] float4
 struct KvPlan {
-  KvGeom geo;
-  size_t part_bytes, amax_bytes, mean_bytes, job_bytes;
+  FusedGeom geo;
+  size_t ctr_bytes, mean_bytes, part_bytes, job_bytes, header_bytes;
 };
 
-KvPlan kv_plan(int64_t T, int H, int D, int sms) {
+int channel_group_width(int C) {
+  for (int w = kFusedMaxW; w >= 16; w >>= 1)
+    if (C % w == 0) return w;
+  return 16;
+}
+
+KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   KvPlan p;
-  KvGeom& g = p.geo;
+  std::memset(&p, 0, sizeof(p));
+  FusedGeom& g = p.geo;
   g.T = T;
   g.C = H * D;
-  const int ctile = std::min(g.C, kCTile);
-  g.nctiles = (g.C + kCTile - 1) / kCTile;
-  g.ctile_threads = std::max(32, ((ctile / 8) + 31) / 32 * 32);
-  const int64_t target = std::max<int64_t>(1, (int64_t)std::max(sms, 1) / g.nctiles);
-  const int64_t want = std::min<int64_t>(std::max<int64_t>(T, 1), target);
-  g.rows_per_chunk = (int)((std::max<int64_t>(T, 1) + want - 1) / want);
-  g.nchunks = (int)((std::max<int64_t>(T, 1) + g.rows_per_chunk - 1) / g.rows_per_chunk);
-  g.nfin = (g.C + 255) / 256;
-  p.part_bytes = align_up((size_t)g.nchunks * g.C * sizeof(float4), kWsAlign);
-  p.amax_bytes = align_up((size_t)std::max(g.nchunks * g.nctiles, g.nfin) * sizeof(float), kWsAlign);
+  g.W = channel_group_width(g.C);
+  g.ngroups = g.C / g.W;
+  g.U = (int64_t)g.ngroups * T;
+  g.P = std::max(ctas, 1);
+  const int64_t per_cta = (g.U + g.P - 1) / g.P;
+  g.smax = (g.U >= g.P && T > 0) ? (int)((per_cta + T - 1) / T + 1) : 1;
+  g.spin_limit = 1u << 24;
+  p.header_bytes = kWsAlign;
+  p.ctr_bytes = align_up((size_t)(2 + g.ngroups) * sizeof(unsigned), kWsAlign);
   p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);
-  p.job_bytes = p.part_bytes + p.amax_bytes + p.mean_bytes;
+  p.part_bytes = align_up((size_t)g.P * g.smax * g.W * sizeof(float4), kWsAlign);
+  p.job_bytes = p.ctr_bytes + p.mean_bytes + p.part_bytes;
   return p;
 }
+
+int fused_grid(bool bf16) {
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  const int per_sm = fused_ctas_per_sm(bf16);
+  return per_sm > 0 ? sms * std::min(per_sm, 1) : 0;
+}
+
+size_t kv_batch_workspace(const KvPlan& p, int n_jobs) { return p.header_bytes + p.job_bytes * (size_t)n_jobs; }
 
 int quant_grid(int64_t nblocks, int sms) {
   const int64_t per_cta = 256;
@@ -69,7 +89,7 @@ nvfp4_status check_job(const nvfp4_kv_job& j, int64_t T) {
   if (T > 0 && (!j.x || !j.codes || !j.scales)) return NVFP4_EINVAL;
   if (j.smooth != 0 && j.smooth != 1) return NVFP4_EINVAL;
   if (!j.smooth && (j.mean_in || j.mean_out)) return NVFP4_EINVAL;
-  if (!aligned(j.x, 16) || !aligned(j.codes, 16) || !aligned(j.scales, 16)) return NVFP4_EALIGN;
+  if (!aligned(j.x, 32) || !aligned(j.codes, 16) || !aligned(j.scales, 16)) return NVFP4_EALIGN;
   if (!aligned(j.tensor_scale, 4) || !aligned(j.mean_in, 4) || !aligned(j.mean_out, 4)) return NVFP4_EALIGN;
   return NVFP4_OK;
 }
@@ -84,24 +104,23 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
     if (st != NVFP4_OK) return st;
   }
   if (!aligned(dev_status, 4)) return NVFP4_EALIGN;
-  const int sms = device_sms();
-  if (sms <= 0) return NVFP4_ECUDA;
-  const KvPlan plan = kv_plan(T, H, D, sms);
-  const size_t need = plan.job_bytes * (size_t)n_jobs;
+  const bool bf16 = dt == NVFP4_IN_BF16;
+  const int ctas = fused_grid(bf16);
+  if (ctas <= 0) return NVFP4_ECUDA;
+  const KvPlan plan = kv_plan(T, H, D, ctas);
+  const size_t need = kv_batch_workspace(plan, n_jobs);
   if (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)) return NVFP4_EWORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t nblocks = T * (int64_t)(plan.geo.C / 16);
-  const int qctas = quant_grid(nblocks, sms);
   char* ws = static_cast<char*>(workspace);
   for (int first = 0; first < n_jobs; first += kMaxJobs) {
-    KvBatch b;
+    FusedBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxJobs, n_jobs - first);
     for (int i = 0; i < b.n; ++i) {
       const nvfp4_kv_job& src = jobs[first + i];
-      KvJob& j = b.job[i];
-      char* base = ws + plan.job_bytes * (size_t)(first + i);
+      FusedJob& j = b.job[i];
+      char* base = ws + plan.header_bytes + plan.job_bytes * (size_t)(first + i);
       j.x = src.x;
       j.smooth = src.smooth;
       j.mean_in = src.mean_in;
@@ -109,14 +128,18 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.codes = src.codes;
       j.scales = src.scales;
       j.tensor_scale = src.tensor_scale;
-      j.part = reinterpret_cast<float4*>(base);
-      j.amax_part = reinterpret_cast<float*>(base + plan.part_bytes);
-      j.mean = reinterpret_cast<float*>(base + plan.part_bytes + plan.amax_bytes);
-      j.namax = src.smooth ? plan.geo.nfin : plan.geo.nchunks * plan.geo.nctiles;
+      j.ctr = reinterpret_cast<unsigned*>(base);
+      j.mean = reinterpret_cast<float*>(base + plan.ctr_bytes);
+      j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
+      if (T > 0 && make_tile_map(&b.map[i], src.x, bf16, T, plan.geo.C, plan.geo.W) != cudaSuccess)
+        return NVFP4_ECUDA;
     }
-    // The status word is reset by the first group's first kernel; every group ORs its flags into it.
-    cudaError_t e = launch_kv_quant(b, plan.geo, dt == NVFP4_IN_BF16, first == 0 ? dev_status : nullptr,
-                                    dev_status, qctas, s);
+    FusedGeom g = plan.geo;
+    g.header = reinterpret_cast<unsigned*>(ws);
+    g.dev_status = dev_status;
+    g.first_launch = first == 0 ? 1 : 0;
+    cudaError_t e = (T == 0) ? launch_kv_empty(b, g.C, dev_status, g.first_launch, s)
+                             : launch_kv_fused(b, g, bf16, s);
     if (e != cudaSuccess) return NVFP4_ECUDA;
   }
   return NVFP4_OK;
@@ -140,16 +163,13 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 int nvfp4_version(void) { return 100; }
 
-size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D) {
-  if (!kv_shape_ok(T, H, D)) return 0;
-  const int sms = device_sms();
-  if (sms <= 0) return 0;
-  return kv_plan(T, H, D, sms).job_bytes;
-}
+size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D) { return nvfp4_kv_batched_workspace_bytes(1, T, H, D); }
 
 size_t nvfp4_kv_batched_workspace_bytes(int n_jobs, int64_t T, int H, int D) {
-  if (n_jobs < 1) return 0;
-  return nvfp4_kv_workspace_bytes(T, H, D) * (size_t)n_jobs;
+  if (n_jobs < 1 || !kv_shape_ok(T, H, D)) return 0;
+  const int ctas = fused_grid(true);
+  if (ctas <= 0) return 0;
+  return kv_batch_workspace(kv_plan(T, H, D, ctas), n_jobs);
 }
 
 nvfp4_status nvfp4_kv_smooth_quant(const void* x, nvfp4_in_dtype dt, int64_t T, int H, int D, int smooth,

@@ -66,6 +66,18 @@ __device__ __forceinline__ float min_nan(float a, float b) {
 
 __device__ __forceinline__ bool finite_f(float x) { return fabsf(x) <= 3.402823466e38f; }
 
+// Lane-wise min / max of two bf16 pairs; a NaN in either input makes that lane NaN.
+__device__ __forceinline__ uint32_t bf16x2_min_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Error-free transformation of an addition (Knuth's TwoSum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
@@ -94,6 +106,65 @@ __device__ __forceinline__ void build_table(QuantTable* tab, float g) {
     tab->inv[e] = ok ? inv : 0.0f;
     tab->e2[e] = ok ? __fmul_rn(E, E) : 0.0f;
   }
+}
+
+// Eight fp32 values -> one word of eight E2M1 codes (byte j = y[2j] low nibble,
+// y[2j+1] high nibble) plus the four decoded f16x2 pairs (low half = even element).
+__device__ __forceinline__ uint32_t e2m1x8(const float y[8], uint32_t q[4]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %8, %7;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %10, %9;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %12, %11;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, b3;\n\t}"
+      : "=r"(w), "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return w;
+}
+
+// (Q_lo - y0, Q_hi - y1) for the f16 pair q2: one rounding each (mixed-precision subtract).
+// The sign is opposite to y - Q; only the square of the difference is used.
+__device__ __forceinline__ void f16x2_minus(uint32_t q2, float y0, float y1, float& d0, float& d1) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "sub.rn.f32.f16 %0, l, %3;\n\tsub.rn.f32.f16 %1, h, %4;\n\t}"
+      : "=f"(d0), "=f"(d1) : "r"(q2), "f"(y0), "f"(y1));
+}
+
+// fl(x_lo - m0), fl(x_hi - m1) for the bf16 pair w (exact widening, one rounding).
+__device__ __forceinline__ void bf16x2_minus(uint32_t w, float m0, float m1, float& z0, float& z1) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(z0), "=f"(z1) : "r"(w), "f"(m0), "f"(m1));
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Named barrier over `n` threads (a multiple of 32) of the block.
+__device__ __forceinline__ void named_barrier(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// 32-byte read-only streaming load (no L1 allocation).
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t v[8]) {
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
 }
 
 }  // namespace nvfp4

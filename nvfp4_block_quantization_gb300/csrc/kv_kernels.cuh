@@ -4,48 +4,55 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
 
-constexpr int kCTile = 4096;       // channels covered by one stats CTA (8 per thread, <= 512 threads)
-constexpr int kMaxJobs = 64;       // tensors per batched launch
+constexpr int kMaxJobs = 64;          // tensors per fused launch
+constexpr int kFusedStatsWarps = 8;   // warps streaming the statistics pass
+constexpr int kFusedQuantWarps = 16;  // warps quantizing (one 16-element block per thread per tile)
+constexpr int kFusedMaxW = 128;       // channels per group
 constexpr int NVFP4_DEV_NONFINITE_FLAG = 1;
 
-// One tensor of a launch: the caller's pointers plus its workspace slices.
-struct KvJob {
+// One tensor of a fused launch: the caller's pointers plus its workspace slices.
+struct FusedJob {
   const void* x;
   const float* mean_in;
   float* mean_out;
   uint8_t* codes;
   uint8_t* scales;
   float* tensor_scale;
-  float4* part;      // [nchunks][C] {sum, compensation, min, max} (smoothed tensors)
-  float* amax_part;  // per-CTA maxima feeding the tensor amax
-  float* mean;       // [C] mean used for smoothing
+  float4* part;   // [P][smax][W] {sum, low part, min, max} per CTA segment (smoothed tensors)
+  float* mean;    // [C] mean used for smoothing
+  unsigned* ctr;  // [0] amax bits, [1] ready count, [2 + k] arrivals at channel group k
   int smooth;
-  int namax;         // number of valid amax_part entries
 };
 
-struct KvBatch {
-  KvJob job[kMaxJobs];
+struct FusedBatch {
+  CUtensorMap map[kMaxJobs];  // 2-D TMA map of each job's x: box W channels x 64 rows
+  FusedJob job[kMaxJobs];
   int n;
 };
 
-// Launch geometry shared by the three kernels.
-struct KvGeom {
+struct FusedGeom {
   int64_t T;
-  int C;               // H * D
-  int nchunks;         // token chunks of the stats pass
-  int rows_per_chunk;
-  int nctiles;         // channel tiles of the stats pass
-  int ctile_threads;   // threads per stats CTA
-  int nfin;            // finalize CTAs (256 channels each)
+  int64_t U;       // ngroups * T (group, row) units
+  int C;           // H * D
+  int W;           // channels per group
+  int ngroups;
+  int P;           // CTAs (all resident)
+  int smax;        // row segments per CTA, upper bound
+  unsigned spin_limit;
+  unsigned* header;  // [0] exit counter, [1] status flags
+  int* dev_status;
+  int first_launch;  // 1: write *dev_status, 0: OR into it
 };
 
-// status_reset (may be NULL) is set to 0 before anything else; status_or (may be NULL) receives flags.
-cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& geo, bool bf16, int* status_reset, int* status_or,
-                            int quant_ctas, cudaStream_t s);
+cudaError_t launch_kv_fused(const FusedBatch& b, const FusedGeom& g, bool bf16, cudaStream_t s);
+cudaError_t make_tile_map(CUtensorMap* map, const void* x, bool bf16, int64_t T, int C, int W);
+int fused_ctas_per_sm(bool bf16);
+cudaError_t launch_kv_empty(const FusedBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s);
 cudaError_t launch_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* g, const float* mean,
                               int64_t tpg, int64_t T, int C, void* out, int ctas, cudaStream_t s);
 

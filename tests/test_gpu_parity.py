@@ -193,8 +193,8 @@ def test_shape_sweep(nv, oracle, shape, dtype, smooth):
     assert np.array_equal(got["codes"], ref["codes"])
     if smooth:
         e2e = gpu_quant(nv, x, smooth)
-        mism = (e2e["mean"].view(np.uint32) != ref["mean"].view(np.uint32)).sum()
-        assert mism <= 1
+        mism = e2e["mean"].view(np.uint32).astype(np.int64) - ref["mean"].view(np.uint32).astype(np.int64)
+        assert int((mism != 0).sum()) <= 3 and int(np.abs(mism).max()) <= 1
         nbad, nblk = compare_end_to_end(e2e, ref, D)
         assert nbad <= max(1, 1e-5 * nblk)
 

@@ -611,61 +611,46 @@ __device__ void quant_role(const FusedBatch& b, const FusedGeom& G, int64_t u0, 
   }
 }
 
-// ------------------------------------------------------------------ producer
-// One thread keeps both TMA rings full: a stage is refilled as soon as every
-// consumer warp of its role has released it.  Stats tiles of job j are held
-// back until this CTA's quant warps have finished job j - 2, so at most two
-// tensors are in flight per CTA and the quant re-read stays in L2.
-template <bool kBF16>
-__device__ void producer(const FusedBatch& b, const FusedGeom& G, int64_t u0, int64_t u1, Smem& sm,
-                         uint8_t* stages_s, uint8_t* stages_q) {
+// ------------------------------------------------------------------ producers
+// One thread per ring keeps it full: a stage is refilled as soon as every
+// consumer warp of its role has released it (blocking, hardware-suspended
+// mbarrier wait, so the producer issues nothing while it waits).  Stats tiles
+// of job j are held back until this CTA's quant warps have finished job j - 2,
+// so at most two tensors are in flight per CTA and the quant re-read stays in L2.
+template <bool kBF16, bool kStatsRing>
+__device__ void producer(const FusedBatch& b, const FusedGeom& G, int64_t u0, int64_t u1, Smem& sm, uint8_t* stages) {
   using CF = Cfg<kBF16>;
+  constexpr int NS = kStatsRing ? CF::kStagesS : CF::kStagesQ;
+  uint64_t* full = kStatsRing ? sm.full_s : sm.full_q;
+  uint64_t* empty = kStatsRing ? sm.empty_s : sm.empty_q;
   const int total = b.n * tiles_per_job(G, u0, u1);
-  if (total == 0) return;
   const unsigned box_bytes = (unsigned)(kTileRows * G.W * CF::kEsize);
-  TileCursor cs, cq;
-  cursor_init(cs, G, u0, u1);
-  cursor_init(cq, G, u0, u1);
-  int fs = 0, fq = 0;
-  uint64_t t_progress = global_timer_ns();
-  for (unsigned it = 1; fs < total || fq < total; ++it) {
-    bool progress = false;
-    if (fs < total) {
-      const int st = fs % CF::kStagesS;
-      const bool free_stage =
-          fs < CF::kStagesS || mbar_test(&sm.empty_s[st], (unsigned)(fs / CF::kStagesS - 1) & 1u);
-      if (free_stage && (cs.j < 2 || sm.quant_done >= cs.j - 1)) {
-        issue_next(b, G, u0, u1, cs, stages_s, st, CF::kStageBytes, box_bytes, sm.full_s);
-        ++fs;
-        progress = true;
+  TileCursor c;
+  cursor_init(c, G, u0, u1);
+  for (int f = 0; f < total; ++f) {
+    const int st = f % NS;
+    if (f >= NS && !mbar_wait(&empty[st], (unsigned)(f / NS - 1) & 1u, G.spin_limit)) {
+      atomicOr(&sm.status, kStatusTimeout);
+      return;
+    }
+    if (kStatsRing && c.j >= 2 && sm.quant_done < c.j - 1) {
+      const uint64_t t0 = global_timer_ns();
+      while (sm.quant_done < c.j - 1) {
+        if (global_timer_ns() - t0 > kWaitNs) {
+          atomicOr(&sm.status, kStatusTimeout);
+          return;
+        }
+        __nanosleep(128);
       }
     }
-    if (fq < total) {
-      const int st = fq % CF::kStagesQ;
-      const bool free_stage =
-          fq < CF::kStagesQ || mbar_test(&sm.empty_q[st], (unsigned)(fq / CF::kStagesQ - 1) & 1u);
-      if (free_stage) {
-        issue_next(b, G, u0, u1, cq, stages_q, st, CF::kStageBytes, box_bytes, sm.full_q);
-        ++fq;
-        progress = true;
-      }
-    }
-    if (progress) {
-      if ((it & 255u) == 0) t_progress = global_timer_ns();
-    } else if ((it & 1023u) == 0) {
-      const uint64_t now = global_timer_ns();
-      if (now - t_progress > kWaitNs) {
-        atomicOr(&sm.status, kStatusTimeout);
-        return;
-      }
-    }
+    issue_next(b, G, u0, u1, c, stages, st, CF::kStageBytes, box_bytes, full);
   }
 }
 
 }  // namespace
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kST + kQT + 32, 1) kv_fused_kernel(const __grid_constant__ FusedBatch b,
+__global__ void __launch_bounds__(kST + kQT + 64, 1) kv_fused_kernel(const __grid_constant__ FusedBatch b,
                                                                 const FusedGeom G) {
   __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -694,7 +679,8 @@ __global__ void __launch_bounds__(kST + kQT + 32, 1) kv_fused_kernel(const __gri
 
   if (threadIdx.x < kST) stats_role<kBF16>(b, G, u0, u1, sm, stages_s);
   else if (threadIdx.x < kST + kQT) quant_role<kBF16>(b, G, u0, u1, sm, stages_q);
-  else if (threadIdx.x == kST + kQT) producer<kBF16>(b, G, u0, u1, sm, stages_s, stages_q);
+  else if (threadIdx.x == kST + kQT) producer<kBF16, true>(b, G, u0, u1, sm, stages_s);
+  else if (threadIdx.x == kST + kQT + 32) producer<kBF16, false>(b, G, u0, u1, sm, stages_q);
 
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -736,7 +722,7 @@ cudaError_t launch_kv_fused(const FusedBatch& b, const FusedGeom& g, bool bf16, 
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.P);
-  cfg.blockDim = dim3(kST + kQT + 32);
+  cfg.blockDim = dim3(kST + kQT + 64);
   cfg.dynamicSmemBytes = bf16 ? Cfg<true>::kDynSmem : Cfg<false>::kDynSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -752,9 +738,9 @@ int fused_ctas_per_sm(bool bf16) {
   int n = 0;
   if ((bf16 ? prepare_kernel<true>() : prepare_kernel<false>()) != cudaSuccess) return 0;
   if (bf16)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_fused_kernel<true>, kST + kQT + 32, Cfg<true>::kDynSmem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_fused_kernel<true>, kST + kQT + 64, Cfg<true>::kDynSmem);
   else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_fused_kernel<false>, kST + kQT + 32, Cfg<false>::kDynSmem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_fused_kernel<false>, kST + kQT + 64, Cfg<false>::kDynSmem);
   return n;
 }
 

@@ -30,28 +30,32 @@ bool kv_shape_ok(int64_t T, int H, int D) {
   const int64_t C = (int64_t)H * D;
   if (C > (1 << 24)) return false;                        // channel indices fit in int with headroom
   if (T > 0 && C > ((int64_t)1 << 46) / T) return false;  // unit arithmetic (units * CTAs) fits in int64
-  if (T > (int64_t)0x7fffff00) return false;               // TMA row coordinates are 32-bit
   return true;
 }
 
-// Plan of one fused launch: partition geometry and the workspace layout.
-//   header (256 B): exit counter, status flags
-//   per job: counters (2 + ngroups words), mean [C], partials [P][smax][W] float4
+// Plan of one KV launch pair: statistics partition and the workspace layout.
+//   header (256 B): quant CTAs finished, status flags
+//   per job: counters (1 + ngroups words), mean [C], partials [P][smax][W] float4
 struct KvPlan {
-  FusedGeom geo;
+  KvGeom geo;
   size_t ctr_bytes, mean_bytes, part_bytes, job_bytes, header_bytes;
 };
 
 int channel_group_width(int C) {
-  for (int w = kFusedMaxW; w >= 16; w >>= 1)
+  for (int w = kMaxGroupW; w >= 16; w >>= 1)
     if (C % w == 0) return w;
   return 16;
+}
+
+int stats_ctas() {
+  const int sms = device_sms();
+  return sms > 0 ? sms * kStatsCtasPerSm : 0;
 }
 
 KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   KvPlan p;
   std::memset(&p, 0, sizeof(p));
-  FusedGeom& g = p.geo;
+  KvGeom& g = p.geo;
   g.T = T;
   g.C = H * D;
   g.W = channel_group_width(g.C);
@@ -60,20 +64,12 @@ KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   g.P = std::max(ctas, 1);
   const int64_t per_cta = (g.U + g.P - 1) / g.P;
   g.smax = (g.U >= g.P && T > 0) ? (int)((per_cta + T - 1) / T + 1) : 1;
-  g.spin_limit = 1u << 24;
   p.header_bytes = kWsAlign;
-  p.ctr_bytes = align_up((size_t)(2 + g.ngroups) * sizeof(unsigned), kWsAlign);
+  p.ctr_bytes = align_up((size_t)(1 + g.ngroups) * sizeof(unsigned), kWsAlign);
   p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);
   p.part_bytes = align_up((size_t)g.P * g.smax * g.W * sizeof(float4), kWsAlign);
   p.job_bytes = p.ctr_bytes + p.mean_bytes + p.part_bytes;
   return p;
-}
-
-int fused_grid(bool bf16) {
-  const int sms = device_sms();
-  if (sms <= 0) return 0;
-  const int per_sm = fused_ctas_per_sm(bf16);
-  return per_sm > 0 ? sms * std::min(per_sm, 1) : 0;
 }
 
 size_t kv_batch_workspace(const KvPlan& p, int n_jobs) { return p.header_bytes + p.job_bytes * (size_t)n_jobs; }
@@ -105,7 +101,7 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
   }
   if (!aligned(dev_status, 4)) return NVFP4_EALIGN;
   const bool bf16 = dt == NVFP4_IN_BF16;
-  const int ctas = fused_grid(bf16);
+  const int ctas = stats_ctas();
   if (ctas <= 0) return NVFP4_ECUDA;
   const KvPlan plan = kv_plan(T, H, D, ctas);
   const size_t need = kv_batch_workspace(plan, n_jobs);
@@ -114,12 +110,12 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   for (int first = 0; first < n_jobs; first += kMaxJobs) {
-    FusedBatch b;
+    KvBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxJobs, n_jobs - first);
     for (int i = 0; i < b.n; ++i) {
       const nvfp4_kv_job& src = jobs[first + i];
-      FusedJob& j = b.job[i];
+      KvJob& j = b.job[i];
       char* base = ws + plan.header_bytes + plan.job_bytes * (size_t)(first + i);
       j.x = src.x;
       j.smooth = src.smooth;
@@ -131,16 +127,18 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.ctr = reinterpret_cast<unsigned*>(base);
       j.mean = reinterpret_cast<float*>(base + plan.ctr_bytes);
       j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
-      if (T > 0 && make_tile_map(&b.map[i], src.x, bf16, T, plan.geo.C, plan.geo.W) != cudaSuccess)
-        return NVFP4_ECUDA;
     }
-    FusedGeom g = plan.geo;
+    KvGeom g = plan.geo;
     g.header = reinterpret_cast<unsigned*>(ws);
     g.dev_status = dev_status;
     g.first_launch = first == 0 ? 1 : 0;
-    cudaError_t e = (T == 0) ? launch_kv_empty(b, g.C, dev_status, g.first_launch, s)
-                             : launch_kv_fused(b, g, bf16, s);
-    if (e != cudaSuccess) return NVFP4_ECUDA;
+    if (T == 0) {
+      if (launch_kv_empty(b, g.C, dev_status, g.first_launch, s) != cudaSuccess) return NVFP4_ECUDA;
+      continue;
+    }
+    if (launch_kv_stats(b, g, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
+    const KvQuantShape q = kv_quant_shape(T, g.C, b.n, device_sms());
+    if (launch_kv_quant(b, g, q, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
   }
   return NVFP4_OK;
 }
@@ -167,7 +165,7 @@ size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D) { return nvfp4_kv_batch
 
 size_t nvfp4_kv_batched_workspace_bytes(int n_jobs, int64_t T, int H, int D) {
   if (n_jobs < 1 || !kv_shape_ok(T, H, D)) return 0;
-  const int ctas = fused_grid(true);
+  const int ctas = stats_ctas();
   if (ctas <= 0) return 0;
   return kv_batch_workspace(kv_plan(T, H, D, ctas), n_jobs);
 }

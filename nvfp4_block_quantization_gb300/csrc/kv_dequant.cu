@@ -12,8 +12,8 @@
 namespace nvfp4 {
 
 // Empty chunk: nothing to quantize; the tensor scale and the mean are 0.
-__global__ void kv_empty_kernel(const FusedBatch b, int C, int* dev_status, int first_launch) {
-  const FusedJob& J = b.job[blockIdx.x];
+__global__ void kv_empty_kernel(const __grid_constant__ KvBatch b, int C, int* dev_status, int first_launch) {
+  const KvJob& J = b.job[blockIdx.x];
   for (int c = threadIdx.x; c < C; c += blockDim.x)
     if (J.mean_out) J.mean_out[c] = J.mean_in ? J.mean_in[c] : 0.0f;
   if (threadIdx.x == 0) {
@@ -22,7 +22,7 @@ __global__ void kv_empty_kernel(const FusedBatch b, int C, int* dev_status, int 
   }
 }
 
-cudaError_t launch_kv_empty(const FusedBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s) {
+cudaError_t launch_kv_empty(const KvBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s) {
   kv_empty_kernel<<<b.n, 256, 0, s>>>(b, C, dev_status, first_launch);
   return cudaGetLastError();
 }

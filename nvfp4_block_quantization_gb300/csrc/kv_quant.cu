@@ -1,0 +1,241 @@
+// kv_quant.cu -- Four-Over-Six NVFP4 quantization pass of the KV chunk
+// quantizer (sm_103a).
+//
+// Method: "LongLive-2.0: An NVFP4 Parallel Infrastructure for Long Video
+// Generation" (summary page), inference step 7 (smoothed K and V go into the
+// NVFP4 KV cache with 4/6 adaptive block scales) and the "full-stack NVFP4"
+// paragraph: per 16-element block, two FP8 (E4M3) block-scale candidates map
+// the block's absolute maximum to 6 and to 4; the block is quantized to E2M1
+// under both and the candidate with the lower squared error is kept, ties to 6.
+//
+// Launch: grid (gx, gy, jobs), CTAs of cw * rpp threads.  Thread (c, r) of a CTA
+// owns block column blockIdx.x * cw + c (16 channels) and the rows
+// blockIdx.y * rpp + r + i * gy * rpp, so the column's 16 channel means stay in
+// registers for the whole loop; the next row's block is loaded before the
+// current one is quantized.  A warp reads 32 consecutive blocks of a row
+// (coalesced) and writes their codes and scale bytes contiguously.
+//
+// Each CTA waits for the statistics grid (programmatic dependent launch), reads
+// the job's amax, and builds the per-tensor table: g = fl(amax / 2688) and, per
+// E4M3 code E, fl(1 / fl(E * g)) and E * E.  The last CTA to finish resets the
+// amax words in the workspace and publishes the status word.
+#include "common.cuh"
+#include "kv_kernels.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr unsigned kStatusNonfinite = 1u;
+
+struct QuantConst {
+  float2 tab[128];  // {fl(1 / fl(E * g)) or 0 when unusable, E * E} per E4M3 code
+  float k6, k4;     // fl(1 / fl(6 g)), fl(1 / fl(4 g))
+  int nonfinite;
+  int last;
+};
+
+// Four-Over-Six on one block z[16].  The two candidates' sequential error
+// chains run side by side in one packed f32x2 accumulator (lane x: scale 6,
+// lane y: scale 4); each lane is exactly the element-order fused chain
+// acc = fma(d, d, acc) of its candidate, d = fl(Q - y) (exact here: y and Q are
+// within a factor of two of each other), err = fl(E^2 * acc).
+__device__ __forceinline__ void quant_block(const float z[16], const QuantConst& qc, uint2& code, uint32_t& sc) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fmaxf(fabsf(z[2 * i]), fabsf(z[2 * i + 1]));
+  const float ma = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+  const float2 s2 = __fmul2_rn(make_float2(ma, ma), make_float2(qc.k6, qc.k4));
+  const uint32_t e = e4m3x2(s2.x, s2.y);
+  const uint32_t e6 = e & 0x7Fu, e4 = (e >> 8) & 0x7Fu;
+  const float2 t6 = qc.tab[e6], t4 = qc.tab[e4];
+  const float2 i6 = make_float2(t6.x, t6.x), i4 = make_float2(t4.x, t4.x);
+  float2 acc = make_float2(0.0f, 0.0f);
+  uint32_t c6[2], c4[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float y6[8], y4[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 zz = make_float2(z[8 * h + 2 * p], z[8 * h + 2 * p + 1]);
+      const float2 a6 = __fmul2_rn(zz, i6), a4 = __fmul2_rn(zz, i4);
+      y6[2 * p] = a6.x; y6[2 * p + 1] = a6.y;
+      y4[2 * p] = a4.x; y4[2 * p + 1] = a4.y;
+    }
+    uint32_t q6[4], q4[4];
+    c6[h] = e2m1x8(y6, q6);
+    c4[h] = e2m1x8(y4, q4);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      float d60, d61, d40, d41;
+      f16x2_minus(q6[p], y6[2 * p], y6[2 * p + 1], d60, d61);
+      f16x2_minus(q4[p], y4[2 * p], y4[2 * p + 1], d40, d41);
+      const float2 d0 = make_float2(d60, d40);
+      acc = __ffma2_rn(d0, d0, acc);
+      const float2 d1 = make_float2(d61, d41);
+      acc = __ffma2_rn(d1, d1, acc);
+    }
+  }
+  const float2 err = __fmul2_rn(make_float2(t6.y, t4.y), acc);
+  const bool ok6 = t6.x > 0.0f, ok4 = t4.x > 0.0f;
+  const bool pick4 = ok4 && (!ok6 || err.y < err.x);
+  code = pick4 ? make_uint2(c4[0], c4[1]) : (ok6 ? make_uint2(c6[0], c6[1]) : make_uint2(0u, 0u));
+  sc = qc.nonfinite ? 0x7Fu : (pick4 ? e4 : (ok6 ? e6 : 0u));
+}
+
+// One block's 16 inputs minus the channel means: z = fl(x - mu) (mu = 0 for
+// unsmoothed tensors gives z = x exactly).
+template <bool kBF16>
+struct RawBlock {
+  uint4 v[kBF16 ? 2 : 4];
+};
+
+template <bool kBF16>
+__device__ __forceinline__ void load_block(const uint8_t* p, RawBlock<kBF16>& r) {
+#pragma unroll
+  for (int i = 0; i < (kBF16 ? 2 : 4); ++i) r.v[i] = ld_nc_v4(p + 16 * i);
+}
+
+template <bool kBF16>
+__device__ __forceinline__ void smooth_block(const RawBlock<kBF16>& r, const float mu[16], float z[16]) {
+  if (kBF16) {
+    const uint32_t w[8] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bf16x2_minus(w[i], mu[2 * i], mu[2 * i + 1], z[2 * i], z[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < (kBF16 ? 2 : 4); ++q) {
+      z[4 * q] = __fsub_rn(__uint_as_float(r.v[q].x), mu[4 * q]);
+      z[4 * q + 1] = __fsub_rn(__uint_as_float(r.v[q].y), mu[4 * q + 1]);
+      z[4 * q + 2] = __fsub_rn(__uint_as_float(r.v[q].z), mu[4 * q + 2]);
+      z[4 * q + 3] = __fsub_rn(__uint_as_float(r.v[q].w), mu[4 * q + 3]);
+    }
+  }
+}
+
+}  // namespace
+
+template <bool kBF16>
+__global__ void __launch_bounds__(256) kv_quant_kernel(const __grid_constant__ KvBatch b, const KvGeom G,
+                                                       const KvQuantShape S) {
+  __shared__ QuantConst qc;
+  const KvJob& J = b.job[blockIdx.z];
+  // the statistics grid must have finished (its amax and means are read below)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const unsigned amax_bits = *reinterpret_cast<volatile const unsigned*>(J.ctr);
+  const float amax = __uint_as_float(amax_bits);
+  const bool nonfinite = !finite_f(amax);
+  const float g = nonfinite ? __int_as_float(0x7fc00000) : __fdiv_rn(amax, kTensorDenom);
+  for (int e = threadIdx.x; e < 128; e += blockDim.x) {
+    const float E = e4m3_value((uint32_t)e);
+    const float Sc = __fmul_rn(E, g);
+    const float inv = __frcp_rn(Sc);
+    const bool ok = (E > 0.0f) && (Sc > 0.0f) && finite_f(inv);
+    qc.tab[e] = make_float2(ok ? inv : 0.0f, ok ? __fmul_rn(E, E) : 0.0f);
+  }
+  if (threadIdx.x == 0) {
+    qc.k6 = __frcp_rn(__fmul_rn(6.0f, g));
+    qc.k4 = __frcp_rn(__fmul_rn(4.0f, g));
+    qc.nonfinite = nonfinite ? 1 : 0;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      *J.tensor_scale = g;
+      if (nonfinite) atomicOr(G.header + 1, kStatusNonfinite);
+    }
+  }
+  __syncthreads();
+
+  const int nbr = G.C / 16;  // blocks per row
+  const int c = threadIdx.x % S.cw, rl = threadIdx.x / S.cw;
+  const int cb = blockIdx.x * S.cw + c;
+  if (cb < nbr) {
+    float mu[16];
+    if (J.smooth) {
+      const float4* m4 = reinterpret_cast<const float4*>(J.mean + 16 * cb);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = __ldg(m4 + i);
+        mu[4 * i] = v.x; mu[4 * i + 1] = v.y; mu[4 * i + 2] = v.z; mu[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mu[i] = 0.0f;
+    }
+    constexpr int es = kBF16 ? 2 : 4;
+    const uint8_t* x = static_cast<const uint8_t*>(J.x) + (size_t)16 * cb * es;
+    const int64_t stride = (int64_t)S.gy * S.rpp;
+    int64_t r = (int64_t)blockIdx.y * S.rpp + rl;
+    RawBlock<kBF16> cur;
+    if (r < G.T) load_block<kBF16>(x + (size_t)r * G.C * es, cur);
+    for (; r < G.T; r += stride) {
+      const int64_t rn = r + stride;
+      RawBlock<kBF16> nxt;
+      if (rn < G.T) load_block<kBF16>(x + (size_t)rn * G.C * es, nxt);
+      float z[16];
+      smooth_block<kBF16>(cur, mu, z);
+      uint2 code;
+      uint32_t sc;
+      quant_block(z, qc, code, sc);
+      const int64_t blk = r * nbr + cb;
+      reinterpret_cast<uint2*>(J.codes)[blk] = code;
+      J.scales[blk] = (uint8_t)sc;
+      cur = nxt;
+    }
+  }
+
+  // the last CTA of the launch returns the workspace to its idle state
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    qc.last = (atomicAdd(G.header + 0, 1u) + 1u == total);
+  }
+  __syncthreads();
+  if (qc.last) {
+    __threadfence();
+    for (int j = threadIdx.x; j < b.n; j += blockDim.x) b.job[j].ctr[0] = 0u;
+    if (threadIdx.x == 0) {
+      const unsigned st = atomicAdd(G.header + 1, 0u);
+      if (G.dev_status) {
+        if (G.first_launch) *G.dev_status = (int)st;
+        else atomicOr(G.dev_status, (int)st);
+      }
+      G.header[1] = 0u;
+      G.header[0] = 0u;
+    }
+  }
+}
+
+KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms) {
+  KvQuantShape q;
+  const int nbr = C / 16;
+  q.cw = nbr < 256 ? nbr : 256;
+  q.rpp = 256 / q.cw;
+  q.gx = (nbr + q.cw - 1) / q.cw;
+  // about 8 CTAs per SM over all jobs, at least one row per thread group
+  const int64_t want = (int64_t)8 * (sms > 0 ? sms : 1);
+  int64_t per_job = (want + n_jobs - 1) / n_jobs;
+  int64_t gy = (per_job + q.gx - 1) / q.gx;
+  const int64_t max_gy = (T + q.rpp - 1) / q.rpp;
+  if (gy > max_gy) gy = max_gy;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  q.gy = (int)gy;
+  return q;
+}
+
+cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& g, const KvQuantShape& q, bool bf16, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(q.gx, q.gy, b.n);
+  cfg.blockDim = dim3(q.cw * q.rpp);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16) return cudaLaunchKernelEx(&cfg, kv_quant_kernel<true>, b, g, q);
+  return cudaLaunchKernelEx(&cfg, kv_quant_kernel<false>, b, g, q);
+}
+
+}  // namespace nvfp4

@@ -30,6 +30,7 @@ bool kv_shape_ok(int64_t T, int H, int D) {
   const int64_t C = (int64_t)H * D;
   if (C > (1 << 24)) return false;                        // channel indices fit in int with headroom
   if (T > 0 && C > ((int64_t)1 << 46) / T) return false;  // unit arithmetic (units * CTAs) fits in int64
+  if (T > (int64_t)0x7fffff00) return false;               // TMA row coordinates are 32-bit
   return true;
 }
 
@@ -113,10 +114,16 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
     KvBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxJobs, n_jobs - first);
+    // smoothed tensors first: the statistics kernel walks the jobs in batch order and
+    // their segment reductions then overlap the streaming of the unsmoothed ones
+    int order[kMaxJobs], no = 0;
+    for (int pass = 1; pass >= 0; --pass)
+      for (int i = 0; i < b.n; ++i)
+        if ((jobs[first + i].smooth != 0) == (pass == 1)) order[no++] = first + i;
     for (int i = 0; i < b.n; ++i) {
-      const nvfp4_kv_job& src = jobs[first + i];
+      const nvfp4_kv_job& src = jobs[order[i]];
       KvJob& j = b.job[i];
-      char* base = ws + plan.header_bytes + plan.job_bytes * (size_t)(first + i);
+      char* base = ws + plan.header_bytes + plan.job_bytes * (size_t)order[i];
       j.x = src.x;
       j.smooth = src.smooth;
       j.mean_in = src.mean_in;
@@ -127,6 +134,8 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.ctr = reinterpret_cast<unsigned*>(base);
       j.mean = reinterpret_cast<float*>(base + plan.ctr_bytes);
       j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
+      if (T > 0 && make_tile_map(&b.map[i], src.x, bf16, T, plan.geo.C, plan.geo.W) != cudaSuccess)
+        return NVFP4_ECUDA;
     }
     KvGeom g = plan.geo;
     g.header = reinterpret_cast<unsigned*>(ws);

@@ -4,13 +4,15 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
 
 constexpr int kMaxJobs = 64;      // tensors per launch
 constexpr int kMaxGroupW = 128;   // channels per statistics group
-constexpr int kStatsThreads = 256;
+constexpr int kStatsConsumers = 256;  // statistics threads per CTA (plus one producer warp)
+constexpr int kStatsTileRows = 64;
 constexpr int kStatsCtasPerSm = 2;
 constexpr int NVFP4_DEV_NONFINITE_FLAG = 1;
 
@@ -29,6 +31,7 @@ struct KvJob {
 };
 
 struct KvBatch {
+  CUtensorMap map[kMaxJobs];  // 2-D TMA map of each job's x[T][C]: box W channels x kStatsTileRows rows
   KvJob job[kMaxJobs];
   int n;
 };
@@ -55,6 +58,7 @@ struct KvQuantShape {
 };
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s);
+cudaError_t make_tile_map(CUtensorMap* map, const void* x, bool bf16, int64_t T, int C, int W);
 cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& g, const KvQuantShape& q, bool bf16, cudaStream_t s);
 KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms);
 cudaError_t launch_kv_empty(const KvBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s);

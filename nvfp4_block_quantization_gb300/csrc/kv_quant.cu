@@ -30,8 +30,6 @@ constexpr unsigned kStatusNonfinite = 1u;
 
 struct QuantConst {
   float2 tab[128];  // {fl(1 / fl(E * g)) or 0 when unusable, E * E} per E4M3 code
-  float k6, k4;     // fl(1 / fl(6 g)), fl(1 / fl(4 g))
-  int nonfinite;
   int last;
 };
 
@@ -40,15 +38,16 @@ struct QuantConst {
 // lane y: scale 4); each lane is exactly the element-order fused chain
 // acc = fma(d, d, acc) of its candidate, d = fl(Q - y) (exact here: y and Q are
 // within a factor of two of each other), err = fl(E^2 * acc).
-__device__ __forceinline__ void quant_block(const float z[16], const QuantConst& qc, uint2& code, uint32_t& sc) {
+__device__ __forceinline__ void quant_block(const float z[16], const float2* tab, float k6, float k4, bool nonfinite,
+                                            uint2& code, uint32_t& sc) {
   float a[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = fmaxf(fabsf(z[2 * i]), fabsf(z[2 * i + 1]));
   const float ma = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
-  const float2 s2 = __fmul2_rn(make_float2(ma, ma), make_float2(qc.k6, qc.k4));
+  const float2 s2 = __fmul2_rn(make_float2(ma, ma), make_float2(k6, k4));
   const uint32_t e = e4m3x2(s2.x, s2.y);
   const uint32_t e6 = e & 0x7Fu, e4 = (e >> 8) & 0x7Fu;
-  const float2 t6 = qc.tab[e6], t4 = qc.tab[e4];
+  const float2 t6 = tab[e6], t4 = tab[e4];
   const float2 i6 = make_float2(t6.x, t6.x), i4 = make_float2(t4.x, t4.x);
   float2 acc = make_float2(0.0f, 0.0f);
   uint32_t c6[2], c4[2];
@@ -80,7 +79,7 @@ __device__ __forceinline__ void quant_block(const float z[16], const QuantConst&
   const bool ok6 = t6.x > 0.0f, ok4 = t4.x > 0.0f;
   const bool pick4 = ok4 && (!ok6 || err.y < err.x);
   code = pick4 ? make_uint2(c4[0], c4[1]) : (ok6 ? make_uint2(c6[0], c6[1]) : make_uint2(0u, 0u));
-  sc = qc.nonfinite ? 0x7Fu : (pick4 ? e4 : (ok6 ? e6 : 0u));
+  sc = nonfinite ? 0x7Fu : (pick4 ? e4 : (ok6 ? e6 : 0u));
 }
 
 // One block's 16 inputs minus the channel means: z = fl(x - mu) (mu = 0 for
@@ -116,10 +115,27 @@ __device__ __forceinline__ void smooth_block(const RawBlock<kBF16>& r, const flo
 }  // namespace
 
 template <bool kBF16>
-__global__ void __launch_bounds__(256) kv_quant_kernel(const __grid_constant__ KvBatch b, const KvGeom G,
-                                                       const KvQuantShape S) {
+__global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant__ KvBatch b, const KvGeom G,
+                                                          const KvQuantShape S) {
   __shared__ QuantConst qc;
+  constexpr int es = kBF16 ? 2 : 4;
   const KvJob& J = b.job[blockIdx.z];
+  const int nbr = G.C / 16;  // blocks per row
+  const int c = threadIdx.x % S.cw, rl = threadIdx.x / S.cw;
+  const int cb = blockIdx.x * S.cw + c;
+  const bool active = cb < nbr;
+  // rows r, r + step, r + 2 step, ... in pairs (r, r + step)
+  const int64_t step = (int64_t)S.gy * S.rpp;
+  const size_t row_bytes = (size_t)G.C * es;
+  int64_t r = (int64_t)blockIdx.y * S.rpp + rl;
+  const uint8_t* px = static_cast<const uint8_t*>(J.x) + (size_t)16 * cb * es + (size_t)r * row_bytes;
+  const size_t px_step = (size_t)step * row_bytes;
+
+  // the inputs do not depend on the statistics grid: fetch the first pair now
+  RawBlock<kBF16> a0 = {}, a1 = {};
+  if (active && r < G.T) load_block<kBF16>(px, a0);
+  if (active && r + step < G.T) load_block<kBF16>(px + px_step, a1);
+
   // the statistics grid must have finished (its amax and means are read below)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const unsigned amax_bits = *reinterpret_cast<volatile const unsigned*>(J.ctr);
@@ -133,52 +149,53 @@ __global__ void __launch_bounds__(256) kv_quant_kernel(const __grid_constant__ K
     const bool ok = (E > 0.0f) && (Sc > 0.0f) && finite_f(inv);
     qc.tab[e] = make_float2(ok ? inv : 0.0f, ok ? __fmul_rn(E, E) : 0.0f);
   }
-  if (threadIdx.x == 0) {
-    qc.k6 = __frcp_rn(__fmul_rn(6.0f, g));
-    qc.k4 = __frcp_rn(__fmul_rn(4.0f, g));
-    qc.nonfinite = nonfinite ? 1 : 0;
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
-      *J.tensor_scale = g;
-      if (nonfinite) atomicOr(G.header + 1, kStatusNonfinite);
-    }
+  if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+    *J.tensor_scale = g;
+    if (nonfinite) atomicOr(G.header + 1, kStatusNonfinite);
   }
+  const float k6 = __frcp_rn(__fmul_rn(6.0f, g)), k4 = __frcp_rn(__fmul_rn(4.0f, g));
   __syncthreads();
 
-  const int nbr = G.C / 16;  // blocks per row
-  const int c = threadIdx.x % S.cw, rl = threadIdx.x / S.cw;
-  const int cb = blockIdx.x * S.cw + c;
-  if (cb < nbr) {
+  if (active) {
     float mu[16];
     if (J.smooth) {
       const float4* m4 = reinterpret_cast<const float4*>(J.mean + 16 * cb);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldg(m4 + i);
+        const float4 v = __ldcg(m4 + i);
         mu[4 * i] = v.x; mu[4 * i + 1] = v.y; mu[4 * i + 2] = v.z; mu[4 * i + 3] = v.w;
       }
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) mu[i] = 0.0f;
     }
-    constexpr int es = kBF16 ? 2 : 4;
-    const uint8_t* x = static_cast<const uint8_t*>(J.x) + (size_t)16 * cb * es;
-    const int64_t stride = (int64_t)S.gy * S.rpp;
-    int64_t r = (int64_t)blockIdx.y * S.rpp + rl;
-    RawBlock<kBF16> cur;
-    if (r < G.T) load_block<kBF16>(x + (size_t)r * G.C * es, cur);
-    for (; r < G.T; r += stride) {
-      const int64_t rn = r + stride;
-      RawBlock<kBF16> nxt;
-      if (rn < G.T) load_block<kBF16>(x + (size_t)rn * G.C * es, nxt);
-      float z[16];
-      smooth_block<kBF16>(cur, mu, z);
-      uint2 code;
-      uint32_t sc;
-      quant_block(z, qc, code, sc);
-      const int64_t blk = r * nbr + cb;
-      reinterpret_cast<uint2*>(J.codes)[blk] = code;
-      J.scales[blk] = (uint8_t)sc;
-      cur = nxt;
+    uint2* pc = reinterpret_cast<uint2*>(J.codes) + (size_t)r * nbr + cb;
+    uint8_t* ps = J.scales + (size_t)r * nbr + cb;
+    const size_t pq_step = (size_t)step * nbr;
+    for (; r < G.T; r += 2 * step) {
+      // next pair in flight while this pair is quantized
+      RawBlock<kBF16> n0 = {}, n1 = {};
+      if (r + 2 * step < G.T) load_block<kBF16>(px + 2 * px_step, n0);
+      if (r + 3 * step < G.T) load_block<kBF16>(px + 3 * px_step, n1);
+      const bool second = r + step < G.T;
+      float z0[16], z1[16];
+      smooth_block<kBF16>(a0, mu, z0);
+      smooth_block<kBF16>(a1, mu, z1);
+      uint2 c0, c1;
+      uint32_t s0, s1;
+      quant_block(z0, qc.tab, k6, k4, nonfinite, c0, s0);
+      quant_block(z1, qc.tab, k6, k4, nonfinite, c1, s1);
+      *pc = c0;
+      *ps = (uint8_t)s0;
+      if (second) {
+        pc[pq_step] = c1;
+        ps[pq_step] = (uint8_t)s1;
+      }
+      a0 = n0;
+      a1 = n1;
+      px += 2 * px_step;
+      pc += 2 * pq_step;
+      ps += 2 * pq_step;
     }
   }
 
@@ -211,8 +228,8 @@ KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms) {
   q.cw = nbr < 256 ? nbr : 256;
   q.rpp = 256 / q.cw;
   q.gx = (nbr + q.cw - 1) / q.cw;
-  // about 8 CTAs per SM over all jobs, at least one row per thread group
-  const int64_t want = (int64_t)8 * (sms > 0 ? sms : 1);
+  // one wave: 2 CTAs per SM over all jobs
+  const int64_t want = (int64_t)2 * (sms > 0 ? sms : 1);
   int64_t per_job = (want + n_jobs - 1) / n_jobs;
   int64_t gy = (per_job + q.gx - 1) / q.gx;
   const int64_t max_gy = (T + q.rpp - 1) / q.rpp;

@@ -38,8 +38,8 @@ W2D_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 256.0       # bf16 in, codes out, one sca
 METRIC = "NVFP4 smooth+quantize GB/s and fraction of GB300 HBM peak per KV chunk"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch measured with ncu for the kernels below (None until captured for the
-# current kernel version; see profiles/).
+# DRAM bytes (read + write) per launch of each kernel on this step's workload, from one ncu
+# capture of this script (profiles/); None until captured for the current kernel version.
 NCU_TRAFFIC = {}
 
 
@@ -338,9 +338,36 @@ def run_ours(args, ws, rank):
     e2e_value = ws * args.e2e_steps * step_bytes / (e2e_ms * 1e-3) / 1e9
     assert int(status_h.item()) == 0
 
+    # ---- per-kernel launch durations, live: the same step as its two enqueues with CUDA events
+    # between them on the launching stream (queue kept ahead of the GPU)
+    ka, kb = [], []
+    n_k = min(400, max(40, steps // 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    torch.cuda.synchronize()
+    for i, (ea, eb, ec) in enumerate(evs):
+        xs, outs, status, ws_t = sets[i % rot]
+        ea.record()
+        nv.kv_stats_batched(xs, [True, False], ws_t, outs)
+        eb.record()
+        nv.kv_quant_batched(xs, [True, False], ws_t, outs, status)
+        ec.record()
+    torch.cuda.synchronize()
+    for ea, eb, ec in evs[4:]:
+        ka.append(ea.elapsed_time(eb))
+        kb.append(eb.elapsed_time(ec))
+    stats_ms, quant_ms = statistics.mean(ka), statistics.mean(kb)
+    stats_bytes = 2 * n_el * 2.0       # K and V read once
+    quant_bytes = step_bytes           # K and V read again, codes and scales written
+    kernels = {"kv_stats": {"ms_per_launch": stats_ms, "algorithmic_bytes": stats_bytes,
+                            "GB/s": stats_bytes / (stats_ms * 1e-3) / 1e9},
+               "kv_quant": {"ms_per_launch": quant_ms, "algorithmic_bytes": quant_bytes,
+                            "GB/s": quant_bytes / (quant_ms * 1e-3) / 1e9},
+               "launches_timed": len(ka)}
+    dom = "kv_quant" if quant_ms >= stats_ms else "kv_stats"
+
     peak, peak_kind = measured_peaks()
     clocks = clk.summary()
-    kern = "kv_smooth_quant_batched (kv_stats + kv_finalize + kv_quant, K and V)"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": rounds_w * rot,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -351,13 +378,15 @@ def run_ours(args, ws, rank):
                    "l2": f"rotating {rot} input/output sets ({rot * step_bytes / 1e6:.0f} MB > 2x L2 {l2 / 1e6:.0f} MB)",
                    "graph": "CUDA graph of one rotation round", "parallelism": f"replicas{ws}"},
         "elements_per_s": ws * steps * 2 * n_el / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": per_gpu_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": per_gpu_gbs / peak, "traffic": NCU_TRAFFIC.get("kv_quant_chunk"),
-                     "kernel": kern, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": step_bytes},
+        "roofline": {"bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": peak, "unit": "GB/s",
+                     "frac": kernels[dom]["GB/s"] / peak, "traffic": NCU_TRAFFIC.get(dom),
+                     "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"],
+                     "step_frac": per_gpu_gbs / peak},
+        "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": e2e_ms / args.e2e_steps},
-        "gpu_launches": steps * 3,
+        "gpu_launches": steps * 2,
         "clocks": clocks,
     }
 

@@ -146,6 +146,24 @@ nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs,
                                            int64_t T, int H, int D, int* dev_status, void* workspace,
                                            size_t workspace_bytes, void* stream);
 
+/* The two passes of nvfp4_kv_smooth_quant_batched as separate enqueues, for a
+ * caller that wants to schedule them apart (e.g. the statistics of one tensor
+ * on one stream while another tensor is quantized on a second stream).
+ * nvfp4_kv_stats_batched computes, for every job, the channel means (written to
+ * mean_out when set) and the tensor's absolute maximum, and leaves them in the
+ * workspace; nvfp4_kv_quant_batched then quantizes with them, writes codes,
+ * scales and tensor scales, publishes *dev_status (covering both passes) and
+ * returns the workspace to its idle state.  The quantization call must follow
+ * the statistics call on the same stream (or after an event that orders it),
+ * with the same jobs in the same order, the same shape and dtype, and the same
+ * workspace; nothing else may use that workspace in between.  A statistics call
+ * without its quantization call leaves the workspace dirty (zero-fill it
+ * again).  Arguments and errors as nvfp4_kv_smooth_quant_batched. */
+nvfp4_status nvfp4_kv_stats_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H,
+                                    int D, void* workspace, size_t workspace_bytes, void* stream);
+nvfp4_status nvfp4_kv_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H,
+                                    int D, int* dev_status, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Dequantize an NVFP4 KV cache back to bf16 (the cache read that attention
  * performs; LongLive-2.0 summary page, inference steps 7 and 9).
  *   codes, scales     device, layouts above, for T tokens

@@ -20,6 +20,7 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job
 
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
+    "kv_stats_batched", "kv_quant_batched",
     "kv_dequant", "w2d_workspace", "weight_quant_2d", "weight_dequant_2d", "load_library",
 ]
 
@@ -121,12 +122,7 @@ def kv_smooth_quant(x, smooth: bool, mean_in=None, workspace=None, out: Optional
     return KvQuantized(codes, scales, g, mean, status)
 
 
-def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None, outs=None, status=None,
-                            stream=None):
-    """Quantize several same-shape chunk tensors (e.g. K and V of every layer) in one enqueue.
-
-    Returns (list of KvQuantized, status) with one shared device status word (OR over tensors).
-    """
+def _batch_jobs(xs, smooth, outs, status):
     torch = _torch()
     n = len(xs)
     if n == 0 or len(smooth) != n:
@@ -144,8 +140,6 @@ def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None
         for sm in smooth:
             c, s, g, m = _kv_outputs(T, H, D, sm, x0.device)
             outs.append(KvQuantized(c, s, g, m, status))
-    if workspace is None:
-        workspace = kv_workspace(T, H, D, n, x0.device)
     jobs = (nvfp4_kv_job * n)()
     for i, (x, sm, o) in enumerate(zip(xs, smooth, outs)):
         jobs[i].x = x.data_ptr()
@@ -155,9 +149,42 @@ def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None
         jobs[i].codes = o.codes.data_ptr()
         jobs[i].scales = o.scales.data_ptr()
         jobs[i].tensor_scale = o.tensor_scale.data_ptr()
-    st = _lib.nvfp4_kv_smooth_quant_batched(jobs, n, _dt(x0), T, H, D, _ptr(status), _ptr(workspace),
+    return jobs, outs, status, (T, H, D)
+
+
+def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None, outs=None, status=None,
+                            stream=None):
+    """Quantize several same-shape chunk tensors (e.g. K and V of every layer) in one enqueue.
+
+    Returns (list of KvQuantized, status) with one shared device status word (OR over tensors).
+    """
+    jobs, outs, status, (T, H, D) = _batch_jobs(xs, smooth, outs, status)
+    if workspace is None:
+        workspace = kv_workspace(T, H, D, len(xs), xs[0].device)
+    st = _lib.nvfp4_kv_smooth_quant_batched(jobs, len(xs), _dt(xs[0]), T, H, D, _ptr(status), _ptr(workspace),
                                             workspace.numel(), _stream(stream))
     _lib.check(st, "nvfp4_kv_smooth_quant_batched")
+    return outs, status
+
+
+def kv_stats_batched(xs: Sequence, smooth: Sequence[bool], workspace, outs, stream=None):
+    """First pass of kv_smooth_quant_batched alone: channel means (into outs[i].mean) and amax, kept in `workspace`.
+
+    Must be followed by kv_quant_batched with the same tensors, outputs and workspace.
+    """
+    jobs, outs, _, (T, H, D) = _batch_jobs(xs, smooth, outs, outs[0].status)
+    st = _lib.nvfp4_kv_stats_batched(jobs, len(xs), _dt(xs[0]), T, H, D, _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    _lib.check(st, "nvfp4_kv_stats_batched")
+    return outs
+
+
+def kv_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace, outs, status, stream=None):
+    """Second pass of kv_smooth_quant_batched: quantize with the statistics kv_stats_batched left in `workspace`."""
+    jobs, outs, status, (T, H, D) = _batch_jobs(xs, smooth, outs, status)
+    st = _lib.nvfp4_kv_quant_batched(jobs, len(xs), _dt(xs[0]), T, H, D, _ptr(status), _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_kv_quant_batched")
     return outs, status
 
 

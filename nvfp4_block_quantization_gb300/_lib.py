@@ -23,6 +23,8 @@ EXPORTS = (
     "nvfp4_kv_smooth_quant",
     "nvfp4_kv_batched_workspace_bytes",
     "nvfp4_kv_smooth_quant_batched",
+    "nvfp4_kv_stats_batched",
+    "nvfp4_kv_quant_batched",
     "nvfp4_kv_dequant",
     "nvfp4_w2d_workspace_bytes",
     "nvfp4_weight_quant_2d",
@@ -75,6 +77,10 @@ def load(path: str | None = None):
     lib.nvfp4_kv_smooth_quant_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp,
                                                   sz, vp]
     lib.nvfp4_kv_smooth_quant_batched.restype = i32
+    lib.nvfp4_kv_stats_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, sz, vp]
+    lib.nvfp4_kv_stats_batched.restype = i32
+    lib.nvfp4_kv_quant_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp, sz, vp]
+    lib.nvfp4_kv_quant_batched.restype = i32
     lib.nvfp4_kv_dequant.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.nvfp4_kv_dequant.restype = i32
     lib.nvfp4_w2d_workspace_bytes.argtypes = [i64, i64]
@@ -117,6 +123,14 @@ def nvfp4_kv_batched_workspace_bytes(n_jobs, T, H, D):
 def nvfp4_kv_smooth_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream):
     return load().nvfp4_kv_smooth_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes,
                                                 stream)
+
+
+def nvfp4_kv_stats_batched(jobs, n_jobs, dt, T, H, D, workspace, workspace_bytes, stream):
+    return load().nvfp4_kv_stats_batched(jobs, n_jobs, dt, T, H, D, workspace, workspace_bytes, stream)
+
+
+def nvfp4_kv_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream):
+    return load().nvfp4_kv_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream)
 
 
 def nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream):

@@ -30,28 +30,18 @@ bool kv_shape_ok(int64_t T, int H, int D) {
   const int64_t C = (int64_t)H * D;
   if (C > (1 << 24)) return false;                        // channel indices fit in int with headroom
   if (T > 0 && C > ((int64_t)1 << 46) / T) return false;  // unit arithmetic (units * CTAs) fits in int64
-  if (T > (int64_t)0x7fffff00) return false;               // TMA row coordinates are 32-bit
   return true;
 }
 
 // Plan of one KV launch pair: statistics partition and the workspace layout.
 //   header (256 B): quant CTAs finished, status flags
-//   per job: counters (1 + ngroups words), mean [C], partials [P][smax][W] float4
+//   per job: counters (2 words), mean [C], partials [P][rpp][C] float4
 struct KvPlan {
   KvGeom geo;
   size_t ctr_bytes, mean_bytes, part_bytes, job_bytes, header_bytes;
 };
 
-int channel_group_width(int C) {
-  for (int w = kMaxGroupW; w >= 16; w >>= 1)
-    if (C % w == 0) return w;
-  return 16;
-}
-
-int stats_ctas() {
-  const int sms = device_sms();
-  return sms > 0 ? sms * kStatsCtasPerSm : 0;
-}
+int stats_ctas() { return device_sms(); }
 
 KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   KvPlan p;
@@ -59,16 +49,13 @@ KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   KvGeom& g = p.geo;
   g.T = T;
   g.C = H * D;
-  g.W = channel_group_width(g.C);
-  g.ngroups = g.C / g.W;
-  g.U = (int64_t)g.ngroups * T;
   g.P = std::max(ctas, 1);
-  const int64_t per_cta = (g.U + g.P - 1) / g.P;
-  g.smax = (g.U >= g.P && T > 0) ? (int)((per_cta + T - 1) / T + 1) : 1;
+  g.tpr = std::min(g.C / 8, kStatsThreads);
+  g.rpp = kStatsThreads / g.tpr;
   p.header_bytes = kWsAlign;
-  p.ctr_bytes = align_up((size_t)(1 + g.ngroups) * sizeof(unsigned), kWsAlign);
+  p.ctr_bytes = kWsAlign;
   p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);
-  p.part_bytes = align_up((size_t)g.P * g.smax * g.W * sizeof(float4), kWsAlign);
+  p.part_bytes = align_up((size_t)g.P * g.rpp * g.C * sizeof(float4), kWsAlign);
   p.job_bytes = p.ctr_bytes + p.mean_bytes + p.part_bytes;
   return p;
 }
@@ -91,8 +78,10 @@ nvfp4_status check_job(const nvfp4_kv_job& j, int64_t T) {
   return NVFP4_OK;
 }
 
+enum KvPhase : int { kPhaseStats = 1, kPhaseQuant = 2, kPhaseBoth = 3 };
+
 nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H, int D,
-                    int* dev_status, void* workspace, size_t workspace_bytes, void* stream) {
+                    int* dev_status, void* workspace, size_t workspace_bytes, void* stream, int phases) {
   if (!jobs || n_jobs < 1) return NVFP4_EINVAL;
   if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
   if (!kv_shape_ok(T, H, D)) return NVFP4_ESHAPE;
@@ -114,8 +103,8 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
     KvBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxJobs, n_jobs - first);
-    // smoothed tensors first: the statistics kernel walks the jobs in batch order and
-    // their segment reductions then overlap the streaming of the unsmoothed ones
+    // smoothed tensors first: the statistics kernel streams the jobs in batch order and
+    // reduces the smoothed ones at the end, when their partials are long published
     int order[kMaxJobs], no = 0;
     for (int pass = 1; pass >= 0; --pass)
       for (int i = 0; i < b.n; ++i)
@@ -134,20 +123,21 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.ctr = reinterpret_cast<unsigned*>(base);
       j.mean = reinterpret_cast<float*>(base + plan.ctr_bytes);
       j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
-      if (T > 0 && make_tile_map(&b.map[i], src.x, bf16, T, plan.geo.C, plan.geo.W) != cudaSuccess)
-        return NVFP4_ECUDA;
     }
     KvGeom g = plan.geo;
     g.header = reinterpret_cast<unsigned*>(ws);
     g.dev_status = dev_status;
     g.first_launch = first == 0 ? 1 : 0;
     if (T == 0) {
-      if (launch_kv_empty(b, g.C, dev_status, g.first_launch, s) != cudaSuccess) return NVFP4_ECUDA;
+      if ((phases & kPhaseStats) && launch_kv_empty(b, g.C, dev_status, g.first_launch, s) != cudaSuccess)
+        return NVFP4_ECUDA;
       continue;
     }
-    if (launch_kv_stats(b, g, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
-    const KvQuantShape q = kv_quant_shape(T, g.C, b.n, device_sms());
-    if (launch_kv_quant(b, g, q, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
+    if ((phases & kPhaseStats) && launch_kv_stats(b, g, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
+    if (phases & kPhaseQuant) {
+      const KvQuantShape q = kv_quant_shape(T, g.C, b.n, device_sms());
+      if (launch_kv_quant(b, g, q, bf16, s) != cudaSuccess) return NVFP4_ECUDA;
+    }
   }
   return NVFP4_OK;
 }
@@ -191,13 +181,23 @@ nvfp4_status nvfp4_kv_smooth_quant(const void* x, nvfp4_in_dtype dt, int64_t T, 
   j.codes = codes;
   j.scales = scales;
   j.tensor_scale = tensor_scale;
-  return kv_run(&j, 1, dt, T, H, D, dev_status, workspace, workspace_bytes, stream);
+  return kv_run(&j, 1, dt, T, H, D, dev_status, workspace, workspace_bytes, stream, kPhaseBoth);
 }
 
 nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T,
                                            int H, int D, int* dev_status, void* workspace, size_t workspace_bytes,
                                            void* stream) {
-  return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream);
+  return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream, kPhaseBoth);
+}
+
+nvfp4_status nvfp4_kv_stats_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H,
+                                    int D, void* workspace, size_t workspace_bytes, void* stream) {
+  return kv_run(jobs, n_jobs, dt, T, H, D, nullptr, workspace, workspace_bytes, stream, kPhaseStats);
+}
+
+nvfp4_status nvfp4_kv_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H,
+                                    int D, int* dev_status, void* workspace, size_t workspace_bytes, void* stream) {
+  return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream, kPhaseQuant);
 }
 
 nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,

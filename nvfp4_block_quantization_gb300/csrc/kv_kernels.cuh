@@ -4,16 +4,12 @@
 
 #include <cstddef>
 #include <cstdint>
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
 
-constexpr int kMaxJobs = 64;      // tensors per launch
-constexpr int kMaxGroupW = 128;   // channels per statistics group
-constexpr int kStatsConsumers = 256;  // statistics threads per CTA (plus one producer warp)
-constexpr int kStatsTileRows = 64;
-constexpr int kStatsCtasPerSm = 2;
+constexpr int kMaxJobs = 64;        // tensors per launch
+constexpr int kStatsThreads = 512;  // statistics threads per CTA, upper bound
 constexpr int NVFP4_DEV_NONFINITE_FLAG = 1;
 
 // One tensor of a launch: the caller's pointers plus its workspace slices.
@@ -24,28 +20,25 @@ struct KvJob {
   uint8_t* codes;
   uint8_t* scales;
   float* tensor_scale;
-  float4* part;   // [P][smax][W] {sum, low part, min, max} per CTA segment (smoothed tensors)
+  float4* part;   // [P][rpp][C] {sum, low part, min, max} per statistics thread (smoothed tensors)
   float* mean;    // [C] mean used for smoothing
-  unsigned* ctr;  // [0] amax bits, [1 + k] arrivals at channel group k
+  unsigned* ctr;  // [0] amax bits, [1] statistics CTAs that published their partials
   int smooth;
 };
 
 struct KvBatch {
-  CUtensorMap map[kMaxJobs];  // 2-D TMA map of each job's x[T][C]: box W channels x kStatsTileRows rows
   KvJob job[kMaxJobs];
   int n;
 };
 
-// Statistics partition: the ngroups * T (channel group, row) units of a tensor
-// are cut into P contiguous ranges, one per statistics CTA.
+// Statistics partition: CTA c of P owns rows [c T / P, (c + 1) T / P); its
+// tpr * rpp threads each own an 8-channel chunk (tpr per row) of every rpp-th row.
 struct KvGeom {
   int64_t T;
-  int64_t U;     // ngroups * T units
-  int C;         // H * D
-  int W;         // channels per group
-  int ngroups;
-  int P;         // statistics CTAs per tensor
-  int smax;      // row segments per CTA, upper bound
+  int C;    // H * D
+  int P;    // statistics CTAs (one per SM)
+  int tpr;  // threads per row: min(C / 8, kStatsThreads)
+  int rpp;  // rows in parallel: kStatsThreads / tpr
   unsigned* header;  // [0] quant CTAs finished, [1] status flags
   int* dev_status;
   int first_launch;  // 1: write *dev_status, 0: OR into it
@@ -58,7 +51,6 @@ struct KvQuantShape {
 };
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s);
-cudaError_t make_tile_map(CUtensorMap* map, const void* x, bool bf16, int64_t T, int C, int W);
 cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& g, const KvQuantShape& q, bool bf16, cudaStream_t s);
 KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms);
 cudaError_t launch_kv_empty(const KvBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s);

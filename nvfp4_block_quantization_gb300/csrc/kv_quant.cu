@@ -18,7 +18,7 @@
 // Each CTA waits for the statistics grid (programmatic dependent launch), reads
 // the job's amax, and builds the per-tensor table: g = fl(amax / 2688) and, per
 // E4M3 code E, fl(1 / fl(E * g)) and E * E.  The last CTA to finish resets the
-// amax words in the workspace and publishes the status word.
+// jobs' counters in the workspace and publishes the status word.
 #include "common.cuh"
 #include "kv_kernels.cuh"
 
@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
   __syncthreads();
   if (qc.last) {
     __threadfence();
-    for (int j = threadIdx.x; j < b.n; j += blockDim.x) b.job[j].ctr[0] = 0u;
+    for (int j = threadIdx.x; j < b.n; j += blockDim.x) {
+      b.job[j].ctr[0] = 0u;
+      b.job[j].ctr[1] = 0u;
+    }
     if (threadIdx.x == 0) {
       const unsigned st = atomicAdd(G.header + 1, 0u);
       if (G.dev_status) {

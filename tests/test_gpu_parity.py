@@ -338,3 +338,62 @@ def test_batched_equals_single_calls(nv):
         assert torch.equal(o.tensor_scale, s.tensor_scale)
         if f:
             assert torch.equal(o.mean, s.mean)
+
+
+# ------------------------------------------------------------------ split passes
+def test_split_passes_match_combined(nv):
+    """kv_stats_batched + kv_quant_batched give the combined call's bits, also across two streams."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    Kb, Vb = W.chunk_kv_bf16(2000, 2001)
+    K, V = dev(Kb[:1000]), dev(Vb[:1000])
+    T, H, D = K.shape
+    ref, st = nv.kv_smooth_quant_batched([K, V], [True, False])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+    def fresh(smooth_flags):
+        outs, status = [], torch.zeros(1, dtype=torch.int32, device="cuda")
+        for sm in smooth_flags:
+            outs.append(nv.KvQuantized(torch.empty((T, H, D // 2), dtype=torch.uint8, device="cuda"),
+                                       torch.empty((T, H, D // 16), dtype=torch.uint8, device="cuda"),
+                                       torch.empty(1, dtype=torch.float32, device="cuda"),
+                                       torch.empty((H, D), dtype=torch.float32, device="cuda") if sm else None,
+                                       status))
+        return outs, status
+
+    def same(a, b):
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+        assert torch.equal(a.tensor_scale.view(torch.int32), b.tensor_scale.view(torch.int32))
+        if a.mean is not None:
+            assert torch.equal(a.mean.view(torch.int32), b.mean.view(torch.int32))
+
+    # same batch, two enqueues, twice on one workspace
+    ws = nv.kv_workspace(T, H, D, 2)
+    for _ in range(2):
+        outs, status = fresh([True, False])
+        nv.kv_stats_batched([K, V], [True, False], ws, outs)
+        nv.kv_quant_batched([K, V], [True, False], ws, outs, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        same(outs[0], ref[0])
+        same(outs[1], ref[1])
+
+    # K and V as separate one-job batches on two streams: V's statistics run beside K's quantization
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    wk, wv = nv.kv_workspace(T, H, D, 1), nv.kv_workspace(T, H, D, 1)
+    ok_, sk = fresh([True])
+    ov, sv = fresh([False])
+    for _ in range(2):
+        with torch.cuda.stream(s1):
+            nv.kv_stats_batched([K], [True], wk, ok_, stream=s1)
+            nv.kv_quant_batched([K], [True], wk, ok_, sk, stream=s1)
+        with torch.cuda.stream(s2):
+            nv.kv_stats_batched([V], [False], wv, ov, stream=s2)
+            nv.kv_quant_batched([V], [False], wv, ov, sv, stream=s2)
+        torch.cuda.synchronize()
+        assert int(sk.item()) == 0 and int(sv.item()) == 0
+        same(ok_[0], ref[0])
+        same(ov[0], ref[1])

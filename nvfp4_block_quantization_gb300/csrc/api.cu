@@ -50,14 +50,21 @@ KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   g.T = T;
   g.C = H * D;
   g.P = std::max(ctas, 1);
-  g.tpr = std::min(g.C / 8, kStatsThreads);
-  g.rpp = kStatsThreads / g.tpr;
+  g.tpr = std::min(g.C / 8, kStatsConsumers);
+  g.rpp = kStatsConsumers / g.tpr;
+  g.rows_per_stage = g.rpp;  // set per element size at launch (stats_stage_rows)
   p.header_bytes = kWsAlign;
   p.ctr_bytes = kWsAlign;
   p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);
   p.part_bytes = align_up((size_t)g.P * g.rpp * g.C * sizeof(float4), kWsAlign);
   p.job_bytes = p.ctr_bytes + p.mean_bytes + p.part_bytes;
   return p;
+}
+
+// Rows per statistics stage: a multiple of rpp whose slabs fill a stage.
+int stats_stage_rows(const KvGeom& g, bool bf16) {
+  const size_t slab_bytes = (size_t)8 * g.tpr * (bf16 ? 2 : 4);
+  return g.rpp * (int)std::max<size_t>(1, (size_t)kStatsStageBytes / (slab_bytes * g.rpp));
 }
 
 size_t kv_batch_workspace(const KvPlan& p, int n_jobs) { return p.header_bytes + p.job_bytes * (size_t)n_jobs; }
@@ -125,6 +132,7 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
     }
     KvGeom g = plan.geo;
+    g.rows_per_stage = stats_stage_rows(g, bf16);
     g.header = reinterpret_cast<unsigned*>(ws);
     g.dev_status = dev_status;
     g.first_launch = first == 0 ? 1 : 0;

@@ -8,8 +8,10 @@
 
 namespace nvfp4 {
 
-constexpr int kMaxJobs = 64;        // tensors per launch
-constexpr int kStatsThreads = 512;  // statistics threads per CTA, upper bound
+constexpr int kMaxJobs = 64;             // tensors per launch
+constexpr int kStatsConsumers = 384;     // statistics consumer threads per CTA, upper bound
+constexpr int kStatsStages = 4;          // statistics ring stages
+constexpr int kStatsStageBytes = 24576;  // bytes per stage
 constexpr int NVFP4_DEV_NONFINITE_FLAG = 1;
 
 // One tensor of a launch: the caller's pointers plus its workspace slices.
@@ -31,14 +33,16 @@ struct KvBatch {
   int n;
 };
 
-// Statistics partition: CTA c of P owns rows [c T / P, (c + 1) T / P); its
-// tpr * rpp threads each own an 8-channel chunk (tpr per row) of every rpp-th row.
+// Statistics partition: CTA c of P owns rows [c T / P, (c + 1) T / P), streamed
+// in stages of rows_per_stage rows (a multiple of rpp); its tpr * rpp consumer
+// threads each own an 8-channel chunk (tpr per row) of every rpp-th row.
 struct KvGeom {
   int64_t T;
   int C;    // H * D
   int P;    // statistics CTAs (one per SM)
-  int tpr;  // threads per row: min(C / 8, kStatsThreads)
-  int rpp;  // rows in parallel: kStatsThreads / tpr
+  int tpr;  // threads per row: min(C / 8, kStatsConsumers)
+  int rpp;  // rows in parallel: kStatsConsumers / tpr
+  int rows_per_stage;
   unsigned* header;  // [0] quant CTAs finished, [1] status flags
   int* dev_status;
   int first_launch;  // 1: write *dev_status, 0: OR into it

@@ -9,14 +9,14 @@
 // that of the raw values.
 //
 // Work split.  The grid is cooperative, one CTA per SM.  CTA c owns the rows
-// [c T / P, (c + 1) T / P) of every job and streams them as whole rows -- each
-// row of C channels is contiguous in memory, which is the access pattern HBM
-// serves fastest.  Thread t owns the 8-channel chunk t % tpr of every rpp-th
-// row from t / tpr (a slab of 8 tpr channels; wider tensors take several
-// slabs), reads it with 16-byte non-caching loads, one batch of rows in flight
-// while the previous batch is folded, and keeps, per channel, (sum, low part) by
-// TwoSum -- so its partial sum is exact -- plus min and max (unsmoothed
-// tensors: the absolute maximum only).
+// [c T / P, (c + 1) T / P) of every job -- one contiguous byte range per job,
+// the access pattern HBM serves fastest.  A producer thread streams it into a
+// shared-memory ring with 1-D bulk copies (cp.async.bulk), stage by stage of R
+// rows; consumer thread t owns the 8-channel chunk t % tpr of every rpp-th row
+// of a stage from t / tpr (a slab of 8 tpr channels; wider tensors take several
+// slabs, and then each row of a stage is its own copy) and keeps, per channel,
+// (sum, low part) by TwoSum -- so its partial sum is exact -- plus min and max
+// (unsmoothed tensors: the absolute maximum only).
 //
 // A smoothed job's per-thread partials go to the workspace (one slice per job,
 // [P][rpp][C] {sum, low, min, max}) and the CTA arrives on the job's counter;
@@ -28,6 +28,7 @@
 // fp32 -- and folds max |x - mean| = max(max - mean, mean - min) (monotone
 // rounding) into the job's amax.  The quantization kernel, launched after this
 // grid, reads the finished amax and means.
+#include "bulk.cuh"
 #include "common.cuh"
 #include "kv_kernels.cuh"
 
@@ -35,17 +36,9 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kThreads = kStatsThreads;
+constexpr int kThreads = kStatsConsumers + 32;  // consumer warps + one producer warp
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowsBF16 = 4, kRowsF32 = 2;  // rows per load batch (two batches in flight)
 constexpr unsigned kStatusTimeout = 2u;
-constexpr uint64_t kWaitNs = 2000000000ull;
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
 
 // (s, n) pairs carry sum = s + n (n: the low part lost by s).
 __device__ __forceinline__ void comp_add(float& s, float& n, float s2, float n2) {
@@ -68,9 +61,11 @@ __device__ __forceinline__ void two_sum2(float2& sum, float2& low, float2 x) {
 }
 
 struct StatsSmem {
+  uint64_t full[kStatsStages], empty[kStatsStages];
   float4 runs[kThreads];  // slice reduction: one run per thread
   float red[kWarps];
   int ok;
+  volatile int abort;  // a ring wait gave up: stop waiting
 };
 
 // Max over the CTA's threads; valid in every thread.
@@ -81,6 +76,18 @@ __device__ __forceinline__ float block_max(float v, StatsSmem& sm) {
   __syncthreads();
   float r = 0.0f;
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = max_nan(r, sm.red[w]);
+  return r;
+}
+
+// Max over the first `n` threads (whole warps, synchronised by named barrier 1).
+__device__ __forceinline__ float consumer_max(float v, StatsSmem& sm, int n) {
+  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+  named_barrier(1, n);
+  if ((threadIdx.x & 31) == 0) sm.red[threadIdx.x >> 5] = v;
+  named_barrier(1, n);
+  float r = 0.0f;
+  for (int w = 0; w < n / 32; ++w) r = max_nan(r, sm.red[w]);
+  named_barrier(1, n);
   return r;
 }
 
@@ -141,38 +148,28 @@ __device__ __forceinline__ void fold_row(const uint4 v0, const uint4 v1, Acc8& a
   }
 }
 
-// Streams rows r, r + rpp, ... < r1 of one 8-channel chunk at `p` (row stride
-// `rs` bytes): a batch of rows is loaded while the previous one is folded.
+// Folds this thread's rows of one landed stage (`rows` valid rows of slab_bytes each).
 template <bool kBF16, bool kSmooth>
-__device__ __forceinline__ void stream_rows(const uint8_t* p, size_t rs, int64_t r, int64_t r1, int rpp, Acc8& a) {
-  constexpr int kRows = kBF16 ? kRowsBF16 : kRowsF32;
-  uint4 A[kRows][kBF16 ? 1 : 2], B[kRows][kBF16 ? 1 : 2];
-  auto load = [&](int64_t rb, uint4 (&v)[kRows][kBF16 ? 1 : 2]) {
+__device__ __forceinline__ void fold_stage(const uint8_t* stage, int slab_bytes, int rows, int rl, int rpp,
+                                           int chunk, Acc8& a) {
+  constexpr int es = kBF16 ? 2 : 4;
+  const uint8_t* p = stage + (size_t)rl * slab_bytes + 8 * chunk * es;
+  const size_t step = (size_t)rpp * slab_bytes;
+  int j = rl;
+  for (; j + 3 * rpp < rows; j += 4 * rpp, p += 4 * step) {  // four rows at a time
+    uint4 v[4][2];
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      const int64_t rr = rb + (int64_t)i * rpp;
-      if (rr < r1) {
-        const uint8_t* q = p + (size_t)rr * rs;
-        v[i][0] = ld_nc_v4(q);
-        if (!kBF16) v[i][kBF16 ? 0 : 1] = ld_nc_v4(q + 16);
-      }
+    for (int i = 0; i < 4; ++i) {
+      v[i][0] = *reinterpret_cast<const uint4*>(p + i * step);
+      v[i][1] = kBF16 ? v[i][0] : *reinterpret_cast<const uint4*>(p + i * step + 16);
     }
-  };
-  auto fold = [&](int64_t rb, const uint4 (&v)[kRows][kBF16 ? 1 : 2]) {
 #pragma unroll
-    for (int i = 0; i < kRows; ++i)
-      if (rb + (int64_t)i * rpp < r1) fold_row<kBF16, kSmooth>(v[i][0], v[i][kBF16 ? 0 : 1], a);
-  };
-  const int64_t step = (int64_t)kRows * rpp;
-  if (r < r1) load(r, A);
-  while (r < r1) {
-    if (r + step < r1) load(r + step, B);
-    fold(r, A);
-    r += step;
-    if (r >= r1) break;
-    if (r + step < r1) load(r + step, A);
-    fold(r, B);
-    r += step;
+    for (int i = 0; i < 4; ++i) fold_row<kBF16, kSmooth>(v[i][0], v[i][1], a);
+  }
+  for (; j < rows; j += rpp, p += step) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
+    const uint4 v1 = kBF16 ? v0 : *reinterpret_cast<const uint4*>(p + 16);
+    fold_row<kBF16, kSmooth>(v0, v1, a);
   }
 }
 
@@ -235,71 +232,130 @@ __device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm) {
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1) kv_stats_kernel(const __grid_constant__ KvBatch b, const KvGeom G) {
-  __shared__ StatsSmem sm;
+  extern __shared__ __align__(128) uint8_t ring[];
+  StatsSmem& sm = *reinterpret_cast<StatsSmem*>(ring + (size_t)kStatsStages * kStatsStageBytes);
   constexpr int es = kBF16 ? 2 : 4;
   const int c = blockIdx.x;
   const int64_t r0 = (int64_t)c * G.T / G.P, r1 = (int64_t)(c + 1) * G.T / G.P;
-  const int chunk = threadIdx.x % G.tpr, rl = threadIdx.x / G.tpr;
-  const bool lane_on = rl < G.rpp;  // threads beyond tpr * rpp idle
-  const size_t rs = (size_t)G.C * es;
+  const size_t rs = (size_t)G.C * es;                 // row stride in bytes
+  const int slab_ch = 8 * G.tpr;                      // channels per slab
+  const int nslab = (G.C + slab_ch - 1) / slab_ch;
+  const int consumers = (G.tpr * G.rpp + 31) / 32 * 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStatsStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], consumers / 32);
+    }
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
 
-  for (int job = 0; job < b.n; ++job) {
-    const KvJob& J = b.job[job];
-    const bool smooth = J.smooth != 0;
-    float amax = 0.0f;
-    for (int s0 = 0; s0 < G.C; s0 += 8 * G.tpr) {  // slabs of tpr chunks
-      const int ch = s0 + 8 * chunk;
-      const bool on = lane_on && ch < G.C;
-      Acc8 a;
-      acc_reset(a);
-      if (on) {
-        const uint8_t* p = static_cast<const uint8_t*>(J.x) + (size_t)ch * es;
-        if (smooth) stream_rows<kBF16, true>(p, rs, r0 + rl, r1, G.rpp, a);
-        else stream_rows<kBF16, false>(p, rs, r0 + rl, r1, G.rpp, a);
-      }
-      if (smooth) {
-        if (on) {
-          float4* dst = J.part + ((size_t)c * G.rpp + rl) * G.C + ch;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float mn0, mn1, mx0, mx1;
-            if (kBF16) {
-              mn0 = bf16lo(a.mnw[q]); mn1 = bf16hi(a.mnw[q]); mx0 = bf16lo(a.mxw[q]); mx1 = bf16hi(a.mxw[q]);
-            } else {
-              mn0 = a.mn[2 * q]; mn1 = a.mn[2 * q + 1]; mx0 = a.mx[2 * q]; mx1 = a.mx[2 * q + 1];
+  if (threadIdx.x >= consumers) {
+    // producer: one thread streams the CTA's rows of every job and slab, stage by stage
+    if (threadIdx.x == consumers) {
+      int f = 0;
+      for (int job = 0; job < b.n; ++job) {
+        const uint8_t* x = static_cast<const uint8_t*>(b.job[job].x);
+        for (int sl = 0; sl < nslab; ++sl) {
+          const int s0 = sl * slab_ch, sb = min(slab_ch, G.C - s0) * es;  // slab bytes of this slab
+          for (int64_t row = r0; row < r1; row += G.rows_per_stage, ++f) {
+            const int rows = (int)min((int64_t)G.rows_per_stage, r1 - row);
+            const int st = f % kStatsStages;
+            if (f >= kStatsStages && !sm.abort &&
+                !mbar_wait(&sm.empty[st], (unsigned)(f / kStatsStages - 1) & 1u)) {
+              sm.abort = 1;
+              atomicOr(G.header + 1, kStatusTimeout);
             }
-            dst[2 * q] = make_float4(a.s[q].x, a.l[q].x, mn0, mx0);
-            dst[2 * q + 1] = make_float4(a.s[q].y, a.l[q].y, mn1, mx1);
+            if (sm.abort) continue;
+            uint8_t* dst = ring + (size_t)st * kStatsStageBytes;
+            mbar_expect_tx(&sm.full[st], (unsigned)(rows * sb));
+            if (nslab == 1) {  // whole rows: the stage is one contiguous range
+              bulk_load(dst, x + (size_t)row * rs, (unsigned)(rows * sb), &sm.full[st]);
+            } else {
+              for (int i = 0; i < rows; ++i)
+                bulk_load(dst + (size_t)i * sb, x + (size_t)(row + i) * rs + (size_t)s0 * es, (unsigned)sb,
+                          &sm.full[st]);
+            }
           }
         }
-      } else {
-        float v = a.amax;
-        if (kBF16) {
-          const uint32_t w = bf16x2_max_nan(bf16x2_max_nan(a.mxw[0], a.mxw[1]), bf16x2_max_nan(a.mxw[2], a.mxw[3]));
-          v = max_nan(v, max_nan(bf16lo(w), bf16hi(w)));
-        }
-        amax = max_nan(amax, v);
       }
     }
-    if (smooth) {
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(J.ctr + 1, 1u);  // this CTA's partials are published
-    } else {
-      const float m = block_max(amax, sm);
-      if (threadIdx.x == 0) atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
+  } else {
+    // consumers
+    const int chunk = threadIdx.x % G.tpr, rl = threadIdx.x / G.tpr;
+    const bool lane_on = rl < G.rpp;  // threads beyond tpr * rpp idle
+    int f = 0;
+    for (int job = 0; job < b.n; ++job) {
+      const KvJob& J = b.job[job];
+      const bool smooth = J.smooth != 0;
+      float amax = 0.0f;
+      for (int sl = 0; sl < nslab; ++sl) {
+        const int s0 = sl * slab_ch, sb = min(slab_ch, G.C - s0) * es;
+        const int ch = s0 + 8 * chunk;
+        const bool on = lane_on && ch < G.C;
+        Acc8 a;
+        acc_reset(a);
+        for (int64_t row = r0; row < r1; row += G.rows_per_stage, ++f) {
+          const int rows = (int)min((int64_t)G.rows_per_stage, r1 - row);
+          const int st = f % kStatsStages;
+          if (!sm.abort && !mbar_wait(&sm.full[st], (unsigned)(f / kStatsStages) & 1u)) {
+            sm.abort = 1;
+            atomicOr(G.header + 1, kStatusTimeout);
+          }
+          const uint8_t* stage = ring + (size_t)st * kStatsStageBytes;
+          if (on) {
+            if (smooth) fold_stage<kBF16, true>(stage, sb, rows, rl, G.rpp, chunk, a);
+            else fold_stage<kBF16, false>(stage, sb, rows, rl, G.rpp, chunk, a);
+          }
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[st]);
+        }
+        if (smooth) {
+          if (on) {
+            float4* dst = J.part + ((size_t)c * G.rpp + rl) * G.C + ch;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float mn0, mn1, mx0, mx1;
+              if (kBF16) {
+                mn0 = bf16lo(a.mnw[q]); mn1 = bf16hi(a.mnw[q]); mx0 = bf16lo(a.mxw[q]); mx1 = bf16hi(a.mxw[q]);
+              } else {
+                mn0 = a.mn[2 * q]; mn1 = a.mn[2 * q + 1]; mx0 = a.mx[2 * q]; mx1 = a.mx[2 * q + 1];
+              }
+              dst[2 * q] = make_float4(a.s[q].x, a.l[q].x, mn0, mx0);
+              dst[2 * q + 1] = make_float4(a.s[q].y, a.l[q].y, mn1, mx1);
+            }
+          }
+        } else {
+          float v = a.amax;
+          if (kBF16) {
+            const uint32_t w = bf16x2_max_nan(bf16x2_max_nan(a.mxw[0], a.mxw[1]), bf16x2_max_nan(a.mxw[2], a.mxw[3]));
+            v = max_nan(v, max_nan(bf16lo(w), bf16hi(w)));
+          }
+          amax = max_nan(amax, v);
+        }
+      }
+      if (smooth) {
+        __threadfence();
+        named_barrier(1, consumers);
+        if (threadIdx.x == 0) atomicAdd(J.ctr + 1, 1u);  // this CTA's partials are published
+      } else {
+        const float m = consumer_max(amax, sm, consumers);
+        if (threadIdx.x == 0) atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
+      }
     }
   }
 
-  // every job streamed: reduce this CTA's channel slice of each smoothed job
+  // every job streamed: reduce this CTA's channel slice of each smoothed job (all threads)
+  __syncthreads();
   for (int job = 0; job < b.n; ++job) {
     const KvJob& J = b.job[job];
     if (!J.smooth) continue;
     if (threadIdx.x == 0) {
-      const uint64_t t0 = global_timer_ns();
+      const uint64_t t0 = bulk_timer_ns();
       int ok = 1;
       for (unsigned it = 0; ld_acquire_u32(J.ctr + 1) < (unsigned)G.P; ++it) {
-        if (global_timer_ns() - t0 > kWaitNs) {
+        if (bulk_timer_ns() - t0 > kBulkWaitNs) {
           ok = 0;
           atomicOr(G.header + 1, kStatusTimeout);
           break;
@@ -317,10 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1) kv_stats_kernel(const __grid_cons
 }
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s) {
+  const size_t smem = (size_t)kStatsStages * kStatsStageBytes + sizeof(StatsSmem);
+  cudaError_t e = bf16 ? cudaFuncSetAttribute(kv_stats_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                       : cudaFuncSetAttribute(kv_stats_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.P);
-  cfg.blockDim = dim3((g.tpr * g.rpp + 31) / 32 * 32);  // whole warps: the extra threads idle but join the collectives
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3((g.tpr * g.rpp + 31) / 32 * 32 + 32);  // consumer warps + the producer warp
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // CTAs wait for each other's partials: all must be resident

@@ -39,8 +39,14 @@ METRIC = "NVFP4 smooth+quantize GB/s and fraction of GB300 HBM peak per KV chunk
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of each kernel on this step's workload, from one ncu
-# capture of this script (profiles/); None until captured for the current kernel version.
-NCU_TRAFFIC = {}
+# capture of this script (profiles/kv_chunk_7040x24x128_launch_list.md); drop an entry when its
+# kernel changes.
+NCU_TRAFFIC = {"kv_stats": 114128256, "kv_quant": 20782848}
+# ALU-pipe warp instructions per launch of the quantization kernel on this step (same capture:
+# sm__inst_executed_pipe_alu at 57.45% of its peak of 2 per SM per cycle over 46,992 active
+# cycles x 152 SMs); the pass is bound by that pipe, not by HBM.
+NCU_ALU_INST = {"kv_quant": 8.207e6}
+ALU_PEAK_PER_SM_CLK = 2.0  # warp instructions: one per SM sub-partition every 2 cycles
 
 
 def parse():
@@ -357,8 +363,8 @@ def run_ours(args, ws, rank):
         ka.append(ea.elapsed_time(eb))
         kb.append(eb.elapsed_time(ec))
     stats_ms, quant_ms = statistics.mean(ka), statistics.mean(kb)
-    stats_bytes = 2 * n_el * 2.0       # K and V read once
-    quant_bytes = step_bytes           # K and V read again, codes and scales written
+    stats_bytes = 2 * n_el * 2.0       # K and V read once (the algorithmic read)
+    quant_bytes = 2 * n_el * 0.5625    # codes and scales written (its re-read of K and V is not algorithmic)
     kernels = {"kv_stats": {"ms_per_launch": stats_ms, "algorithmic_bytes": stats_bytes,
                             "GB/s": stats_bytes / (stats_ms * 1e-3) / 1e9},
                "kv_quant": {"ms_per_launch": quant_ms, "algorithmic_bytes": quant_bytes,
@@ -368,6 +374,21 @@ def run_ours(args, ws, rank):
 
     peak, peak_kind = measured_peaks()
     clocks = clk.summary()
+    if dom == "kv_quant":
+        sm_mhz = clocks.get("sm_mhz") or 2070.0
+        alu_peak = props.multi_processor_count * ALU_PEAK_PER_SM_CLK * sm_mhz * 1e6 / 1e9
+        alu_ach = NCU_ALU_INST["kv_quant"] / (quant_ms * 1e-3) / 1e9
+        roofline = {"bound": "alu", "achieved": alu_ach, "peak": alu_peak, "unit": "G warp-inst/s (ALU pipe)",
+                    "frac": alu_ach / alu_peak, "traffic": NCU_TRAFFIC.get(dom), "kernel": dom,
+                    "peak_source": "SMs x 2 ALU warp-instructions per SM per clock x sampled SM clock",
+                    "alu_inst_per_launch": NCU_ALU_INST["kv_quant"],
+                    "hbm_frac": kernels[dom]["GB/s"] / peak, "step_frac": per_gpu_gbs / peak}
+    else:
+        roofline = {"bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": peak, "unit": "GB/s",
+                    "frac": kernels[dom]["GB/s"] / peak, "traffic": NCU_TRAFFIC.get(dom),
+                    "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs",
+                    "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"],
+                    "step_frac": per_gpu_gbs / peak}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": rounds_w * rot,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -378,11 +399,7 @@ def run_ours(args, ws, rank):
                    "l2": f"rotating {rot} input/output sets ({rot * step_bytes / 1e6:.0f} MB > 2x L2 {l2 / 1e6:.0f} MB)",
                    "graph": "CUDA graph of one rotation round", "parallelism": f"replicas{ws}"},
         "elements_per_s": ws * steps * 2 * n_el / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": kernels[dom]["GB/s"], "peak": peak, "unit": "GB/s",
-                     "frac": kernels[dom]["GB/s"] / peak, "traffic": NCU_TRAFFIC.get(dom),
-                     "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"],
-                     "step_frac": per_gpu_gbs / peak},
+        "roofline": roofline,
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": e2e_ms / args.e2e_steps},
@@ -392,6 +409,7 @@ def run_ours(args, ws, rank):
 
     if not args.no_rows:
         line["rows"] = secondary_rows(nv, W, torch, dev, l2, peak)
+        line["size_ceiling"] = size_ceiling_rows(torch, dev, l2)
     if not args.no_cpu and rank == 0:
         gbs, secs, elems = cpu_oracle_run(T_CHUNK)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -423,6 +441,36 @@ def _time_graph(torch, fn, reps_in_graph, replays, warm=2):
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / (reps_in_graph * replays)  # ms per fn call
+
+
+def size_ceiling_rows(torch, dev, l2):
+    """What plain device kernels (torch's copy and sum, not this library) reach at this step's sizes.
+
+    HBM throughput depends strongly on transfer size here: a kernel moving tens of MB pays a
+    fixed launch/ramp/drain cost of several microseconds, so these rows bound what any one
+    kernel over one tensor or one K+V pair can reach.
+    """
+    flush = torch.empty(int(2.5 * l2), dtype=torch.uint8, device=dev)
+    out = {}
+    for label, n in (("one_tensor_43MB", T_CHUNK * HEADS * HEAD_DIM), ("k_and_v_86MB", 2 * T_CHUNK * HEADS * HEAD_DIM)):
+        a = torch.randn(n, device=dev).to(torch.bfloat16)
+        b = torch.empty_like(a)
+        for kind in ("copy", "sum"):
+            best = 1e9
+            for _ in range(6):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if kind == "copy":
+                    b.copy_(a)
+                else:
+                    a.sum(dtype=torch.float32)
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            nbytes = a.numel() * 2 * (2 if kind == "copy" else 1)
+            out[f"torch_{kind}_{label}"] = {"GB/s": nbytes / (best * 1e-3) / 1e9, "us": best * 1e3, "bytes": nbytes}
+    return out
 
 
 def secondary_rows(nv, W, torch, dev, l2, peak):

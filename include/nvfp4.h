@@ -200,6 +200,21 @@ nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, 
                                    uint8_t* scales, float* tensor_scale, int* dev_status, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/* nvfp4_weight_quant_2d without a workspace.  The pages have no counterpart:
+ * this call exists for callers that cannot allocate device memory or hand the
+ * library a scratch buffer -- e.g. a runtime that passes the library only the
+ * tensors it reads and writes, or code that must not call into an allocator
+ * at that point.  Its scratch (the per-CTA amax partials, 4 per SM) is a
+ * file-scope device array inside the library of 4096 entries: the call returns
+ * NVFP4_EWORKSPACE on a device with more than 1024 SMs.  The first call on a
+ * device looks up that array's address (once per device, with the device
+ * current); make that first call before capturing a stream.  All calls on a
+ * device share the one array, so calls that overlap in time (several streams
+ * or host threads) race: order them.  Results, arguments and other errors are
+ * those of nvfp4_weight_quant_2d. */
+nvfp4_status nvfp4_weight_quant_2d_static(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,
+                                          uint8_t* scales, float* tensor_scale, int* dev_status, void* stream);
+
 /* Dequantize 16x16-tiled NVFP4 weights to bf16 out[M][N]
  * (bf16_rne(fl(Q * fl(E * g)))).  tensor_scale is device [1]. */
 nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,

@@ -28,6 +28,7 @@ EXPORTS = (
     "nvfp4_kv_dequant",
     "nvfp4_w2d_workspace_bytes",
     "nvfp4_weight_quant_2d",
+    "nvfp4_weight_quant_2d_static",
     "nvfp4_weight_dequant_2d",
 )
 
@@ -87,6 +88,8 @@ def load(path: str | None = None):
     lib.nvfp4_w2d_workspace_bytes.restype = sz
     lib.nvfp4_weight_quant_2d.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
     lib.nvfp4_weight_quant_2d.restype = i32
+    lib.nvfp4_weight_quant_2d_static.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp]
+    lib.nvfp4_weight_quant_2d_static.restype = i32
     lib.nvfp4_weight_dequant_2d.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     lib.nvfp4_weight_dequant_2d.restype = i32
     _lib = lib
@@ -144,6 +147,10 @@ def nvfp4_w2d_workspace_bytes(M, N):
 def nvfp4_weight_quant_2d(w, dt, M, N, codes, scales, tensor_scale, dev_status, workspace, workspace_bytes, stream):
     return load().nvfp4_weight_quant_2d(w, dt, M, N, codes, scales, tensor_scale, dev_status, workspace,
                                         workspace_bytes, stream)
+
+
+def nvfp4_weight_quant_2d_static(w, dt, M, N, codes, scales, tensor_scale, dev_status, stream):
+    return load().nvfp4_weight_quant_2d_static(w, dt, M, N, codes, scales, tensor_scale, dev_status, stream)
 
 
 def nvfp4_weight_dequant_2d(codes, scales, tensor_scale, M, N, out_bf16, stream):

@@ -4,6 +4,7 @@
 // enqueued on an error), carves its workspace, and enqueues the kernels on the
 // caller's stream.  No allocation, no synchronization, no printing.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "nvfp4.h"
@@ -232,6 +233,63 @@ size_t nvfp4_w2d_workspace_bytes(int64_t M, int64_t N) {
   const int sms = device_sms();
   if (sms <= 0) return 0;
   return align_up((size_t)sms * 4 * sizeof(float), kWsAlign);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of nvfp4_weight_quant_2d_static: one amax partial per amax CTA (4 per SM).
+// A file-scope device array, so the call needs no workspace and allocates nothing.
+// Every slot is written by its CTA before the quantization kernel reads it, so
+// nothing in it has to start at zero.  All calls on one device share it.
+constexpr int kW2dStaticPartials = 4096;  // room for 1024 SMs
+static __device__ __align__(256) float g_w2d_static_scratch[kW2dStaticPartials];
+constexpr int kMaxDevices = 64;
+
+// Device address of the scratch on the current device, looked up once per device
+// (cudaGetSymbolAddress with that device current); nullptr if the lookup fails.
+float* w2d_static_scratch() {
+  static std::atomic<void*> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_w2d_static_scratch) != cudaSuccess || !q) return nullptr;
+    cache[dev].store(q, std::memory_order_release);
+    p = q;
+  }
+  return static_cast<float*>(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4_status nvfp4_weight_quant_2d_static(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,
+                                          uint8_t* scales, float* tensor_scale, int* dev_status, void* stream) {
+  if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
+  if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return NVFP4_ESHAPE;
+  if (M > 0 && N > ((int64_t)1 << 60) / M) return NVFP4_ESHAPE;
+  if (!tensor_scale) return NVFP4_EINVAL;
+  if (M > 0 && (!w || !codes || !scales)) return NVFP4_EINVAL;
+  if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVFP4_EALIGN;
+  if (!aligned(tensor_scale, 4) || !aligned(dev_status, 4)) return NVFP4_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ECUDA;
+  if (sms * 4 > kW2dStaticPartials) return NVFP4_EWORKSPACE;  // more amax CTAs than the scratch holds
+  float* scratch = w2d_static_scratch();
+  if (!scratch) return NVFP4_ECUDA;
+  W2dGeom geo;
+  geo.M = M;
+  geo.N = N;
+  geo.amax_ctas = sms * 4;
+  const int64_t ntiles = (M / 16) * (N / 16);
+  const int qctas = quant_grid(ntiles, sms);
+  cudaError_t e = launch_w2d_quant(w, dt == NVFP4_IN_BF16, geo, codes, scales, tensor_scale, dev_status, scratch,
+                                   qctas, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
 nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,

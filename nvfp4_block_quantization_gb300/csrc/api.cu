@@ -111,10 +111,10 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
     KvBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxJobs, n_jobs - first);
-    // smoothed tensors first: the statistics kernel streams the jobs in batch order and
-    // reduces the smoothed ones at the end, when their partials are long published
+    // unsmoothed tensors first: their statistics finish soonest (no reduction), so
+    // their quantization starts while the smoothed ones are still being streamed
     int order[kMaxJobs], no = 0;
-    for (int pass = 1; pass >= 0; --pass)
+    for (int pass = 0; pass <= 1; ++pass)
       for (int i = 0; i < b.n; ++i)
         if ((jobs[first + i].smooth != 0) == (pass == 1)) order[no++] = first + i;
     for (int i = 0; i < b.n; ++i) {

@@ -24,7 +24,7 @@ struct KvJob {
   float* tensor_scale;
   float4* part;   // [P][rpp][C] {sum, low part, min, max} per statistics thread (smoothed tensors)
   float* mean;    // [C] mean used for smoothing
-  unsigned* ctr;  // [0] amax bits, [1] statistics CTAs that published their partials
+  unsigned* ctr;  // [0] amax bits, [1] statistics CTAs that published their partials, [2] ... that finished the job
   int smooth;
 };
 

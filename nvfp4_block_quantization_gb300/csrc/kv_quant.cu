@@ -15,10 +15,12 @@
 // current one is quantized.  A warp reads 32 consecutive blocks of a row
 // (coalesced) and writes their codes and scale bytes contiguously.
 //
-// Each CTA waits for the statistics grid (programmatic dependent launch), reads
-// the job's amax, and builds the per-tensor table: g = fl(amax / 2688) and, per
-// E4M3 code E, fl(1 / fl(E * g)) and E * E.  The last CTA to finish resets the
-// jobs' counters in the workspace and publishes the status word.
+// The grid is a programmatic dependent of the statistics grid and may run beside
+// it: each CTA fetches its first rows, waits (bounded) until every statistics
+// CTA has counted itself ready for this CTA's job, reads the job's amax, and
+// builds the per-tensor table: g = fl(amax / 2688) and, per E4M3 code E,
+// fl(1 / fl(E * g)) and E * E.  The last CTA to finish resets the jobs'
+// counters in the workspace and publishes the status word.
 #include "common.cuh"
 #include "kv_kernels.cuh"
 
@@ -31,7 +33,17 @@ constexpr unsigned kStatusNonfinite = 1u;
 struct QuantConst {
   float2 tab[128];  // {fl(1 / fl(E * g)) or 0 when unusable, E * E} per E4M3 code
   int last;
+  int ok;  // this job's statistics are final
 };
+
+constexpr unsigned kStatusTimeout = 2u;
+constexpr uint64_t kReadyWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Four-Over-Six on one block z[16].  The two candidates' sequential error
 // chains run side by side in one packed f32x2 accumulator (lane x: scale 6,
@@ -136,9 +148,22 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
   if (active && r < G.T) load_block<kBF16>(px, a0);
   if (active && r + step < G.T) load_block<kBF16>(px + px_step, a1);
 
-  // the statistics grid must have finished (its amax and means are read below)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const unsigned amax_bits = *reinterpret_cast<volatile const unsigned*>(J.ctr);
+  // wait (bounded) until every statistics CTA has finished this job: its amax and means are read below
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = timer_ns();
+    int ok = 1;
+    for (unsigned it = 0; ld_acquire_u32(J.ctr + 2) < (unsigned)G.P; ++it) {
+      if (timer_ns() - t0 > kReadyWaitNs) {
+        ok = 0;
+        atomicOr(G.header + 1, kStatusTimeout);
+        break;
+      }
+      __nanosleep(it < 8 ? 128 : 512);
+    }
+    qc.ok = ok;
+  }
+  __syncthreads();
+  const unsigned amax_bits = qc.ok ? *reinterpret_cast<volatile const unsigned*>(J.ctr) : 0x7fc00000u;
   const float amax = __uint_as_float(amax_bits);
   const bool nonfinite = !finite_f(amax);
   const float g = nonfinite ? __int_as_float(0x7fc00000) : __fdiv_rn(amax, kTensorDenom);
@@ -212,6 +237,7 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
     for (int j = threadIdx.x; j < b.n; j += blockDim.x) {
       b.job[j].ctr[0] = 0u;
       b.job[j].ctr[1] = 0u;
+      b.job[j].ctr[2] = 0u;
     }
     if (threadIdx.x == 0) {
       const unsigned st = atomicAdd(G.header + 1, 0u);

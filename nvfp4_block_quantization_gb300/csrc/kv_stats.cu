@@ -20,14 +20,18 @@
 //
 // A smoothed job's per-thread partials go to the workspace (one slice per job,
 // [P][rpp][C] {sum, low, min, max}) and the CTA arrives on the job's counter;
-// an unsmoothed job's absolute maximum is folded into its amax directly.  When
-// a CTA has streamed every job it reduces, for each smoothed job, its slice of
-// channels [c C / P, (c + 1) C / P): it waits (bounded) until all CTAs have
-// arrived, combines each channel's P * rpp partials in a fixed order, writes
-// the mean -- the binary64 quotient of the compensated sum, rounded once to
-// fp32 -- and folds max |x - mean| = max(max - mean, mean - min) (monotone
-// rounding) into the job's amax.  The quantization kernel, launched after this
-// grid, reads the finished amax and means.
+// it then waits (bounded; all CTAs stream the same job at about the same time)
+// until every CTA has arrived, reduces its slice of channels [c C / P,
+// (c + 1) C / P) -- each channel's P * rpp partials combined in a fixed order,
+// the mean the binary64 quotient of the compensated sum rounded once to fp32 --
+// and folds max |x - mean| = max(max - mean, mean - min) (monotone rounding)
+// into the job's amax.  An unsmoothed job's absolute maximum is folded into its
+// amax directly.  Either way the CTA then counts itself on the job's ready
+// counter (release).  The host orders unsmoothed jobs first.
+//
+// The grid lets its dependent launch start at once: the quantization kernel's
+// CTAs wait for their own job's ready count (acquire), so one job's
+// quantization overlaps the statistics of the next.
 #include "bulk.cuh"
 #include "common.cuh"
 #include "kv_kernels.cuh"
@@ -178,12 +182,11 @@ __device__ __forceinline__ void fold_stage(const uint8_t* stage, int slab_bytes,
 // max |x - mean| into the job's amax.  The blockDim / nch threads of a channel
 // each fold a contiguous run of its partials (loads 8 at a time); thread j < nch
 // then folds channel j's runs in order.
-__device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm) {
+__device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm, int nt) {
   const int c = blockIdx.x;
   const int ch0 = (int)((int64_t)c * G.C / G.P), ch1 = (int)((int64_t)(c + 1) * G.C / G.P);
   const int np = G.P * G.rpp;  // partials per channel
   float cam = 0.0f;
-  const int nt = blockDim.x;
   for (int cb = ch0; cb < ch1; cb += nt) {
     const int nch = min(nt, ch1 - cb);
     const int runs = nt / nch;  // runs per channel
@@ -205,9 +208,9 @@ __device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm) {
         }
       }
     }
-    __syncthreads();  // the previous block's runs have been read
+    named_barrier(1, nt);  // the previous block's runs have been read
     sm.runs[threadIdx.x] = make_float4(s, l, mn, mx);
-    __syncthreads();
+    named_barrier(1, nt);
     if (threadIdx.x < nch) {
       s = 0.0f;
       l = 0.0f;
@@ -224,14 +227,20 @@ __device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm) {
       cam = max_nan(cam, max_nan(__fsub_rn(mx, mu), __fsub_rn(mu, mn)));
     }
   }
-  const float m = block_max(cam, sm);
-  if (threadIdx.x == 0) atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
+  __threadfence();  // the means are visible before the job is marked ready
+  const float m = consumer_max(cam, sm, nt);
+  if (threadIdx.x == 0) {
+    atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
+    __threadfence();
+    atomicAdd(J.ctr + 2, 1u);  // this CTA's share of the job is final
+  }
 }
 
 }  // namespace
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kThreads, 1) kv_stats_kernel(const __grid_constant__ KvBatch b, const KvGeom G) {
+// at most 80 registers, so that a quantization CTA fits on the SM beside this one
+__global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch b, const KvGeom G) {
   extern __shared__ __align__(128) uint8_t ring[];
   StatsSmem& sm = *reinterpret_cast<StatsSmem*>(ring + (size_t)kStatsStages * kStatsStageBytes);
   constexpr int es = kBF16 ? 2 : 4;
@@ -250,6 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1) kv_stats_kernel(const __grid_cons
     mbar_fence_init();
   }
   __syncthreads();
+  // the quantization grid may launch now: its CTAs wait for each job's ready count,
+  // not for this grid to end
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x >= consumers) {
     // producer: one thread streams the CTA's rows of every job and slab, stage by stage
@@ -338,38 +350,33 @@ __global__ void __launch_bounds__(kThreads, 1) kv_stats_kernel(const __grid_cons
       if (smooth) {
         __threadfence();
         named_barrier(1, consumers);
-        if (threadIdx.x == 0) atomicAdd(J.ctr + 1, 1u);  // this CTA's partials are published
+        if (threadIdx.x == 0) {
+          atomicAdd(J.ctr + 1, 1u);  // this CTA's partials are published
+          // every CTA streams the same job at about the same time: a short wait
+          const uint64_t t0 = bulk_timer_ns();
+          int ok = 1;
+          for (unsigned it = 0; ld_acquire_u32(J.ctr + 1) < (unsigned)G.P; ++it) {
+            if (bulk_timer_ns() - t0 > kBulkWaitNs) {
+              ok = 0;
+              atomicOr(G.header + 1, kStatusTimeout);
+              break;
+            }
+            __nanosleep(it < 16 ? 64 : 256);
+          }
+          sm.ok = ok;
+        }
+        named_barrier(1, consumers);
+        if (sm.ok) reduce_slice(J, G, sm, consumers);
       } else {
         const float m = consumer_max(amax, sm, consumers);
-        if (threadIdx.x == 0) atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
-      }
-    }
-  }
-
-  // every job streamed: reduce this CTA's channel slice of each smoothed job (all threads)
-  __syncthreads();
-  for (int job = 0; job < b.n; ++job) {
-    const KvJob& J = b.job[job];
-    if (!J.smooth) continue;
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = bulk_timer_ns();
-      int ok = 1;
-      for (unsigned it = 0; ld_acquire_u32(J.ctr + 1) < (unsigned)G.P; ++it) {
-        if (bulk_timer_ns() - t0 > kBulkWaitNs) {
-          ok = 0;
-          atomicOr(G.header + 1, kStatusTimeout);
-          break;
+        if (threadIdx.x == 0) {
+          atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
+          __threadfence();
+          atomicAdd(J.ctr + 2, 1u);  // this CTA's share of the job is final
         }
-        __nanosleep(it < 16 ? 64 : 512);
       }
-      sm.ok = ok;
     }
-    __syncthreads();
-    if (sm.ok) reduce_slice(J, G, sm);
-    __syncthreads();
   }
-  // the quantization kernel may start its prologue now; it waits for this grid to finish
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s) {

@@ -220,10 +220,7 @@ nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const
   if (!aligned(tensor_scale, 4) || !aligned(mean, 4)) return NVFP4_EALIGN;
   const int sms = device_sms();
   if (sms <= 0) return NVFP4_ECUDA;
-  const int C = H * D;
-  const int64_t nblocks = T * (int64_t)(C / 16);
-  const int ctas = quant_grid(nblocks, sms);
-  cudaError_t e = launch_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, C, out_bf16, ctas,
+  cudaError_t e = launch_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H * D, out_bf16, sms,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }

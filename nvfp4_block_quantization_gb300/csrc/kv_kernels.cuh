@@ -59,7 +59,7 @@ cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& g, const KvQuantShap
 KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms);
 cudaError_t launch_kv_empty(const KvBatch& b, int C, int* dev_status, int first_launch, cudaStream_t s);
 cudaError_t launch_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* g, const float* mean,
-                              int64_t tpg, int64_t T, int C, void* out, int ctas, cudaStream_t s);
+                              int64_t tpg, int64_t T, int C, void* out, int sms, cudaStream_t s);
 
 // 16x16-tile weight quantizer.
 struct W2dGeom {

@@ -283,7 +283,7 @@ nvfp4_status nvfp4_weight_quant_2d_static(const void* w, nvfp4_in_dtype dt, int6
   geo.N = N;
   geo.amax_ctas = sms * 4;
   const int64_t ntiles = (M / 16) * (N / 16);
-  const int qctas = quant_grid(ntiles, sms);
+  const int qctas = quant_grid(2 * ntiles, sms);  // two threads per tile
   cudaError_t e = launch_w2d_quant(w, dt == NVFP4_IN_BF16, geo, codes, scales, tensor_scale, dev_status, scratch,
                                    qctas, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
@@ -308,7 +308,7 @@ nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, 
   geo.N = N;
   geo.amax_ctas = sms * 4;
   const int64_t ntiles = (M / 16) * (N / 16);
-  const int qctas = quant_grid(ntiles, sms);
+  const int qctas = quant_grid(2 * ntiles, sms);  // two threads per tile
   cudaError_t e = launch_w2d_quant(w, dt == NVFP4_IN_BF16, geo, codes, scales, tensor_scale, dev_status,
                                    static_cast<float*>(workspace), qctas, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
@@ -323,8 +323,7 @@ nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales
     return NVFP4_EALIGN;
   const int sms = device_sms();
   if (sms <= 0) return NVFP4_ECUDA;
-  const int ctas = quant_grid(M * N / 16, sms);
-  cudaError_t e = launch_w2d_dequant(codes, scales, tensor_scale, M, N, out_bf16, ctas,
+  cudaError_t e = launch_w2d_dequant(codes, scales, tensor_scale, M, N, out_bf16, sms,
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }

@@ -64,6 +64,13 @@ __device__ __forceinline__ float min_nan(float a, float b) {
   return r;
 }
 
+// max(|a|, |b|, |c|) in one instruction (a NaN operand is ignored).
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float r;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ bool finite_f(float x) { return fabsf(x) <= 3.402823466e38f; }
 
 // Lane-wise min / max of two bf16 pairs; a NaN in either input makes that lane NaN.

@@ -70,6 +70,6 @@ cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8
                              float* tensor_scale, int* dev_status, float* amax_part, int quant_ctas,
                              cudaStream_t s);
 cudaError_t launch_w2d_dequant(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t M, int64_t N,
-                               void* out, int ctas, cudaStream_t s);
+                               void* out, int sms, cudaStream_t s);
 
 }  // namespace nvfp4

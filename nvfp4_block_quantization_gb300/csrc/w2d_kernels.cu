@@ -31,17 +31,36 @@ __device__ __forceinline__ void load_row16(const void* base, int64_t elem, float
   }
 }
 
+// Absolute maximum (NaN-propagating) of the matrix, per CTA: CTA c reads the
+// contiguous range of 16-byte chunks [c n / P, (c + 1) n / P) with 8 loads in
+// flight per thread; partial c goes to amax_part[c].
 template <bool kBF16>
 __global__ void __launch_bounds__(256) w2d_amax_kernel(const void* w, int64_t n16, float* amax_part, int* dev_status) {
   __shared__ float red[32];
   if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status) *dev_status = 0;
-  float m = 0.0f;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
-    float v[16];
-    load_row16<kBF16>(w, i * 16, v);
+  const uint4* p = static_cast<const uint4*>(w);
+  const int64_t nv = n16 * (kBF16 ? 2 : 4);  // 16-byte chunks
+  const int64_t a = (int64_t)blockIdx.x * nv / gridDim.x, b = (int64_t)(blockIdx.x + 1) * nv / gridDim.x;
+  constexpr int U = 8;
+  uint32_t mw = 0u;  // bf16: max of |x| pairs
+  float mf = 0.0f;   // fp32
+  for (int64_t i = a + threadIdx.x; i < b; i += (int64_t)U * blockDim.x) {
+    uint4 v[U];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m = max_nan(m, fabsf(v[j]));
+    for (int u = 0; u < U; ++u) v[u] = i + (int64_t)u * blockDim.x < b ? ld_nc_v4(p + i + (int64_t)u * blockDim.x)
+                                                                        : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (kBF16) {
+        mw = bf16x2_max_nan(mw, bf16x2_max_nan(v[u].x & 0x7fff7fffu, v[u].y & 0x7fff7fffu));
+        mw = bf16x2_max_nan(mw, bf16x2_max_nan(v[u].z & 0x7fff7fffu, v[u].w & 0x7fff7fffu));
+      } else {
+        mf = max_nan(mf, max_nan(max_nan(fabsf(__uint_as_float(v[u].x)), fabsf(__uint_as_float(v[u].y))),
+                                 max_nan(fabsf(__uint_as_float(v[u].z)), fabsf(__uint_as_float(v[u].w)))));
+      }
+    }
   }
+  float m = kBF16 ? max_nan(bf16lo(mw), bf16hi(mw)) : mf;
   for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
@@ -52,21 +71,14 @@ __global__ void __launch_bounds__(256) w2d_amax_kernel(const void* w, int64_t n1
   }
 }
 
-// Sum of fused squared errors of one 16-element tile row under `inv`.
-__device__ __forceinline__ float row_err(const float v[16], float inv, float acc) {
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    float y0 = __fmul_rn(v[2 * p], inv);
-    float y1 = __fmul_rn(v[2 * p + 1], inv);
-    uint32_t q = e2m1x2_to_f16x2(e2m1x2(y0, y1));
-    float d0 = __fsub_rn(y0, f16lo(q));
-    acc = __fmaf_rn(d0, d0, acc);
-    float d1 = __fsub_rn(y1, f16hi(q));
-    acc = __fmaf_rn(d1, d1, acc);
-  }
-  return acc;
-}
-
+// Quantization: two threads per 16x16 tile (lanes 2p and 2p + 1 of a warp), one
+// per candidate (even lane: scale mapping the tile amax to 6, odd lane: to 4).
+// Each finds the tile amax (rows 0-7 / 8-15, combined with its partner), picks
+// its candidate's E4M3 scale, and quantizes the whole tile under it, keeping
+// the 256 codes in registers and the error as one fused multiply-add per
+// element in row-major order.  The pair then compares errors (lower wins, ties
+// to 6) and the winner stores its codes and the scale byte.  A warp covers 16
+// adjacent tiles: 512 contiguous bytes of every tile row.
 template <bool kBF16>
 __global__ void __launch_bounds__(256) w2d_quant_kernel(const void* w, int64_t M, int64_t N,
                                                         const float* amax_part, int namax, uint8_t* codes,
@@ -87,8 +99,8 @@ __global__ void __launch_bounds__(256) w2d_quant_kernel(const void* w, int64_t M
   const float amax = red[0];
   const bool nonfinite = !finite_f(amax);
   const float g = nonfinite ? __int_as_float(0x7fc00000) : __fdiv_rn(amax, kTensorDenom);
-  const float k6 = __frcp_rn(__fmul_rn(6.0f, g));
-  const float k4 = __frcp_rn(__fmul_rn(4.0f, g));
+  const int half = threadIdx.x & 1;  // 0: candidate 6, 1: candidate 4
+  const float kM = __frcp_rn(__fmul_rn(half ? 4.0f : 6.0f, g));
   build_table(&tab, g);
   __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -96,83 +108,129 @@ __global__ void __launch_bounds__(256) w2d_quant_kernel(const void* w, int64_t M
     if (nonfinite && dev_status) atomicOr(dev_status, NVFP4_DEV_NONFINITE_FLAG);
   }
 
+  const unsigned pair_mask = 3u << (threadIdx.x & 30);
   const int64_t TN = N / 16;
   const int64_t ntiles = (M / 16) * TN;
-  for (int64_t tl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; tl < ntiles; tl += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t npairs = (int64_t)gridDim.x * (blockDim.x / 2);
+  for (int64_t tl = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 2; tl < ntiles; tl += npairs) {
     const int64_t ti = tl / TN, tj = tl - ti * TN;
     const int64_t base = ti * 16 * N + tj * 16;
-    uint32_t sc = 0u;
-    float inv = 0.0f;
-    if (nonfinite) {
-      sc = 0x7Fu;
-    } else {
-      float ab = 0.0f;
-      for (int r = 0; r < 16; ++r) {
-        float v[16];
-        load_row16<kBF16>(w, base + r * N, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[j]));
-      }
-      if (g > 0.0f && ab > 0.0f) {
-        const uint32_t ee = e4m3x2(__fmul_rn(ab, k6), __fmul_rn(ab, k4));
-        const uint32_t e6 = ee & 0xFFu, e4 = ee >> 8;
-        const float inv6 = tab.inv[e6], inv4 = tab.inv[e4];
-        float acc6 = 0.0f, acc4 = 0.0f;
-        for (int r = 0; r < 16; ++r) {
-          float v[16];
-          load_row16<kBF16>(w, base + r * N, v);
-          acc6 = row_err(v, inv6, acc6);
-          acc4 = row_err(v, inv4, acc4);
-        }
-        const float err6 = __fmul_rn(tab.e2[e6], acc6);
-        const float err4 = __fmul_rn(tab.e2[e4], acc4);
-        const bool ok6 = inv6 > 0.0f, ok4 = inv4 > 0.0f;
-        if (ok4 && (!ok6 || err4 < err6)) {
-          sc = e4;
-          inv = inv4;
-        } else if (ok6) {
-          sc = e6;
-          inv = inv6;
-        }
-      }
+    // tile amax: this lane's 8 rows, then the partner's
+    float ab = 0.0f;
+#pragma unroll 2
+    for (int r = 8 * half; r < 8 * half + 8; ++r) {
+      float v[16];
+      load_row16<kBF16>(w, base + r * N, v);
+      ab = max3_abs(ab, max3_abs(max3_abs(v[0], v[1], v[2]), max3_abs(v[3], v[4], v[5]), max3_abs(v[6], v[7], v[8])),
+                    max3_abs(max3_abs(v[9], v[10], v[11]), max3_abs(v[12], v[13], v[14]), v[15]));
     }
+    ab = fmaxf(ab, __shfl_xor_sync(pair_mask, ab, 1));
+    // this lane's candidate
+    const uint32_t e = e4m3x2(__fmul_rn(ab, kM), 0.0f) & 0x7Fu;
+    const float inv = tab.inv[e];
+    uint2 cw[16];
+    float acc = 0.0f;
+#pragma unroll
     for (int r = 0; r < 16; ++r) {
-      uint32_t wd[2] = {0u, 0u};
-      if (inv > 0.0f) {
-        float v[16];
-        load_row16<kBF16>(w, base + r * N, v);
+      float v[16];
+      load_row16<kBF16>(w, base + r * N, v);
 #pragma unroll
-        for (int p = 0; p < 8; ++p)
-          wd[p >> 2] |= e2m1x2(__fmul_rn(v[2 * p], inv), __fmul_rn(v[2 * p + 1], inv)) << (8 * (p & 3));
+      for (int h = 0; h < 2; ++h) {
+        float y[8];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 yy = __fmul2_rn(make_float2(v[8 * h + 2 * p], v[8 * h + 2 * p + 1]), make_float2(inv, inv));
+          y[2 * p] = yy.x;
+          y[2 * p + 1] = yy.y;
+        }
+        uint32_t q[4];
+        const uint32_t c = e2m1x8(y, q);
+        if (h == 0) cw[r].x = c; else cw[r].y = c;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          float d0, d1;
+          f16x2_minus(q[p], y[2 * p], y[2 * p + 1], d0, d1);
+          acc = __fmaf_rn(d0, d0, acc);
+          acc = __fmaf_rn(d1, d1, acc);
+        }
       }
-      reinterpret_cast<uint2*>(codes + (base + r * N) / 2)[0] = make_uint2(wd[0], wd[1]);
     }
-    scales[tl] = (uint8_t)sc;
+    const float err = __fmul_rn(tab.e2[e], acc);
+    const bool ok = inv > 0.0f && ab > 0.0f && !nonfinite;
+    const float err_o = __shfl_xor_sync(pair_mask, err, 1);
+    const bool ok_o = __shfl_xor_sync(pair_mask, ok ? 1 : 0, 1) != 0;
+    const bool ok6 = half ? ok_o : ok, ok4 = half ? ok : ok_o;
+    const float err6 = half ? err_o : err, err4 = half ? err : err_o;
+    const bool pick4 = ok4 && (!ok6 || err4 < err6);
+    // the winner writes; with no usable candidate the even lane writes zeros (or the NaN filler)
+    const bool writer = half ? pick4 : !pick4;
+    if (writer) {
+      const bool use = half ? true : ok6;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        reinterpret_cast<uint2*>(codes + (base + r * N) / 2)[0] = use ? cw[r] : make_uint2(0u, 0u);
+      scales[tl] = nonfinite ? 0x7Fu : (uint8_t)(use ? e : 0u);
+    }
   }
 }
 
+// Dequant: thread (c, r) owns 16-column block blockIdx.x * cw + c of the
+// contiguous row range [blockIdx.y * R, (blockIdx.y + 1) * R), rows r, r + rpp,
+// ...; codes and scale bytes of four rows are fetched ahead and each block's 16
+// bf16 values go out in one 32-byte streaming store (two 16-byte stores when the
+// output is only 16-byte aligned).
+template <bool kWide>
 __global__ void __launch_bounds__(256) w2d_dequant_kernel(const uint8_t* __restrict__ codes,
                                                           const uint8_t* __restrict__ scales,
                                                           const float* __restrict__ tensor_scale, int64_t M,
-                                                          int64_t N, __nv_bfloat16* __restrict__ out) {
-  const int64_t n16 = M * N / 16;
-  const int64_t TN = N / 16;
+                                                          int64_t N, int cw, int rpp, int64_t rows_per_cta,
+                                                          __nv_bfloat16* __restrict__ out) {
+  constexpr int kAhead = 4;
+  const int64_t nbr = N / 16;
+  const int c = threadIdx.x % cw, rl = threadIdx.x / cw;
+  const int64_t cb = (int64_t)blockIdx.x * cw + c;
+  if (cb >= nbr || rl >= rpp) return;
+  const int64_t ra = (int64_t)blockIdx.y * rows_per_cta;
+  const int64_t rb = ra + rows_per_cta < M ? ra + rows_per_cta : M;
+  const uint2* c8 = reinterpret_cast<const uint2*>(codes) + cb;
+  const uint8_t* s8 = scales + cb;
+  uint4* o = reinterpret_cast<uint4*>(out + cb * 16);
+  const size_t orow = (size_t)N / 8;  // uint4 per output row
   const float g = __ldg(tensor_scale);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = (i * 16) / N, c = (i * 16) - r * N;
-    const float S = __fmul_rn(e4m3_value(scales[(r / 16) * TN + c / 16]), g);
-    const uint2 cw = __ldg(reinterpret_cast<const uint2*>(codes) + i);
-    uint32_t o[8];
+  for (int64_t r = ra + rl; r < rb; r += (int64_t)kAhead * rpp) {
+    uint2 cwd[kAhead];
+    uint32_t sc[kAhead];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint32_t byte = ((p < 4 ? cw.x : cw.y) >> (8 * (p & 3))) & 0xFFu;
-      const uint32_t q = e2m1x2_to_f16x2(byte);
-      __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(f16lo(q), S), __fmul_rn(f16hi(q), S));
-      o[p] = *reinterpret_cast<uint32_t*>(&h);
+    for (int u = 0; u < kAhead; ++u) {
+      const int64_t row = r + (int64_t)u * rpp;
+      if (row < rb) {
+        cwd[u] = __ldg(c8 + (size_t)row * nbr);
+        sc[u] = __ldg(s8 + (size_t)(row / 16) * nbr);
+      }
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int64_t row = r + (int64_t)u * rpp;
+      if (row >= rb) break;
+      const float S = __fmul_rn(e4m3_value(sc[u]), g);
+      uint32_t wd[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const uint32_t byte = ((p < 4 ? cwd[u].x : cwd[u].y) >> (8 * (p & 3))) & 0xFFu;
+        const uint32_t q = e2m1x2_to_f16x2(byte);
+        __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(f16lo(q), S), __fmul_rn(f16hi(q), S));
+        wd[p] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      uint4* dst = o + (size_t)row * orow;
+      if (kWide) {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(wd[0]), "r"(wd[1]),
+                     "r"(wd[2]), "r"(wd[3]), "r"(wd[4]), "r"(wd[5]), "r"(wd[6]), "r"(wd[7])
+                     : "memory");
+      } else {
+        dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+      }
+    }
   }
 }
 
@@ -194,9 +252,25 @@ cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8
 }
 
 cudaError_t launch_w2d_dequant(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t M, int64_t N,
-                               void* out, int ctas, cudaStream_t s) {
+                               void* out, int sms, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  w2d_dequant_kernel<<<ctas, 256, 0, s>>>(codes, scales, g, M, N, static_cast<__nv_bfloat16*>(out));
+  const int64_t nbr = N / 16;
+  const int cw = nbr < 256 ? (int)nbr : 256;
+  const int rpp = 256 / cw;
+  const int64_t gx = (nbr + cw - 1) / cw;
+  int64_t gy = ((int64_t)32 * (sms > 0 ? sms : 1) + gx - 1) / gx;  // 32 CTAs per SM in total
+  const int64_t max_gy = (M + rpp - 1) / rpp;
+  if (gy > max_gy) gy = max_gy;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const int64_t rows_per_cta = (M + gy - 1) / gy;
+  gy = (M + rows_per_cta - 1) / rows_per_cta;
+  const dim3 grid((unsigned)gx, (unsigned)gy), block(cw * rpp);
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if ((reinterpret_cast<uintptr_t>(out) % 32) == 0)
+    w2d_dequant_kernel<true><<<grid, block, 0, s>>>(codes, scales, g, M, N, cw, rpp, rows_per_cta, o);
+  else
+    w2d_dequant_kernel<false><<<grid, block, 0, s>>>(codes, scales, g, M, N, cw, rpp, rows_per_cta, o);
   return cudaGetLastError();
 }
 

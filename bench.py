@@ -56,6 +56,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-rows", action="store_true", help="skip the secondary rows (dequant, weights, 30 layers)")
+    p.add_argument("--rows", nargs="+", default=None, metavar="ROW",
+                   help="run only these secondary rows: kv_write_30_layers kv_cache_read_dequant weight_quant_2d "
+                        "activation_quant_1d k_only_smooth_quant")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=30)
     return p.parse_args()
@@ -408,7 +411,7 @@ def run_ours(args, ws, rank):
     }
 
     if not args.no_rows:
-        line["rows"] = secondary_rows(nv, W, torch, dev, l2, peak)
+        line["rows"] = secondary_rows(nv, W, torch, dev, peak, args.rows)
         line["size_ceiling"] = size_ceiling_rows(torch, dev, l2)
     if not args.no_cpu and rank == 0:
         gbs, secs, elems = cpu_oracle_run(T_CHUNK)
@@ -444,83 +447,84 @@ def _time_graph(torch, fn, reps_in_graph, replays, warm=2):
 
 
 def size_ceiling_rows(torch, dev, l2):
-    """What plain device kernels (torch's copy and sum, not this library) reach at this step's sizes.
+    """What a plain device copy (torch's, not this library) reaches at this step's sizes.
 
-    HBM throughput depends strongly on transfer size here: a kernel moving tens of MB pays a
-    fixed launch/ramp/drain cost of several microseconds, so these rows bound what any one
-    kernel over one tensor or one K+V pair can reach.
+    Same method as the step: a CUDA graph replayed over rotating buffers whose
+    footprint exceeds 2x L2, so every read comes from HBM and no dirty lines are
+    left for the timed kernel to write back.  Bytes are read + written.
     """
-    flush = torch.empty(int(2.5 * l2), dtype=torch.uint8, device=dev)
     out = {}
     for label, n in (("one_tensor_43MB", T_CHUNK * HEADS * HEAD_DIM), ("k_and_v_86MB", 2 * T_CHUNK * HEADS * HEAD_DIM)):
-        a = torch.randn(n, device=dev).to(torch.bfloat16)
-        b = torch.empty_like(a)
-        for kind in ("copy", "sum"):
-            best = 1e9
-            for _ in range(6):
-                flush.fill_(1)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                if kind == "copy":
-                    b.copy_(a)
-                else:
-                    a.sum(dtype=torch.float32)
-                e1.record()
-                torch.cuda.synchronize()
-                best = min(best, e0.elapsed_time(e1))
-            nbytes = a.numel() * 2 * (2 if kind == "copy" else 1)
-            out[f"torch_{kind}_{label}"] = {"GB/s": nbytes / (best * 1e-3) / 1e9, "us": best * 1e3, "bytes": nbytes}
+        nbuf = max(4, int(2 * 2.5 * l2 // (n * 2)) + 1)
+        srcs = [torch.empty(n, dtype=torch.bfloat16, device=dev).fill_(1.0) for _ in range(nbuf)]
+        dsts = [torch.empty_like(srcs[0]) for _ in range(nbuf)]
+        ms = _time_graph(torch, lambda i: dsts[i % nbuf].copy_(srcs[i % nbuf]), nbuf, 10)
+        nbytes = n * 2 * 2
+        out[f"torch_copy_{label}"] = {"GB/s": nbytes / (ms * 1e-3) / 1e9, "us": ms * 1e3, "bytes": nbytes,
+                                      "method": f"graph over {nbuf} rotating buffer pairs"}
+        del srcs, dsts
     return out
 
 
-def secondary_rows(nv, W, torch, dev, l2, peak):
-    """The other hot-path rows, each on its own seeded synthetic workload (device-generated)."""
-    rows = {}
-    gen = torch.Generator(device=dev)
+def _chunk_k_device(torch, gen, dev):
+    """One layer's K chunk on the device: per-(head, channel) offsets N(0, 3^2) plus N(0, 1) noise,
+    15 whole channels (0.5%) scaled by 16, bf16 (the same law as the step's K)."""
+    off = torch.randn((HEADS, HEAD_DIM), generator=gen, device=dev) * 3.0
+    k = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev) + off
+    ch = torch.randperm(HEADS * HEAD_DIM, generator=gen, device=dev)[:15]
+    k.view(T_CHUNK, -1)[:, ch] *= 16.0
+    return k.to(torch.bfloat16)
 
-    # 30-layer full-model chunk write: K and V of every layer in one batched call
+
+def row_kv_write_30_layers(nv, W, torch, dev, peak):
+    """Full-model chunk write: K and V of all 30 layers in one batched call."""
+    gen = torch.Generator(device=dev)
     gen.manual_seed(3000)
     L = 30
     xs, flags = [], []
     for layer in range(L):
-        off = torch.randn((HEADS, HEAD_DIM), generator=gen, device=dev) * 3.0
-        k = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev) + off
-        ch = torch.randperm(HEADS * HEAD_DIM, generator=gen, device=dev)[:15]
-        k.view(T_CHUNK, -1)[:, ch] *= 16.0
-        v = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev)
-        xs += [k.to(torch.bfloat16), v.to(torch.bfloat16)]
+        xs.append(_chunk_k_device(torch, gen, dev))
+        xs.append(torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev).to(torch.bfloat16))
         flags += [True, False]
-        del k, v
     outs, status = nv.kv_smooth_quant_batched(xs, flags)
     wsb = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 2 * L, dev)
     ms = _time_graph(torch, lambda i: nv.kv_smooth_quant_batched(xs, flags, workspace=wsb, outs=outs, status=status),
                      1, 20)
     b = 2 * L * T_CHUNK * HEADS * HEAD_DIM * QUANT_BYTES_PER_ELEM
-    rows["kv_write_30_layers"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
 
-    # cache read: 21 frames (3 global-sink frames of chunk 0 + the 18 most recent frames of chunks
-    # 0..2) x 880 tokens, K and V of layers 0 and 1, packed by the quantizer; per-frame groups carry
-    # each frame's chunk tensor scale and mean.
+
+def row_kv_cache_read_dequant(nv, W, torch, dev, peak):
+    """Cache read: 21 frames (3 global-sink frames of chunk 0 + the 18 most recent frames of
+    chunks 0..2) x 880 tokens, quantized by this library from seeded chunks (four caches: K and
+    V of two layers); per-frame groups carry each frame's chunk tensor scale and mean."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
     Tc, F = 21 * 880, 880
     frame_src = [(0, f) for f in range(3)] + [(0, 6), (0, 7)] + [(1, f) for f in range(8)] + [(2, f) for f in range(8)]
     caches = []
-    for t in range(4):  # (layer, K/V) pairs
+    for t in range(4):
         chunk_q = []
         for c in range(3):
-            x = xs[(c * 2 + t) % len(xs)]  # seeded chunk tensors reused as the cache's source chunks
+            x = _chunk_k_device(torch, gen, dev)
             chunk_q.append(nv.kv_smooth_quant(x, True))
+            del x
         codes = torch.cat([chunk_q[c].codes[f * F:(f + 1) * F] for c, f in frame_src])
         scales = torch.cat([chunk_q[c].scales[f * F:(f + 1) * F] for c, f in frame_src])
         gs = torch.cat([chunk_q[c].tensor_scale for c, f in frame_src])
         means = torch.stack([chunk_q[c].mean for c, f in frame_src])
         out = torch.empty((Tc, HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev)
         caches.append((codes, scales, gs, means, out))
+        del chunk_q
     ms = _time_graph(torch, lambda i: nv.kv_dequant(*caches[i % 4][:3], mean=caches[i % 4][3],
                                                     tokens_per_group=F, out=caches[i % 4][4]), 8, 20)
     b = Tc * HEADS * HEAD_DIM * DEQUANT_BYTES_PER_ELEM
-    rows["kv_cache_read_dequant"] = {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
 
-    # weights: 4 x 3072x3072 and 2 x 3072x14336 with 16x16 tiles
+
+def row_weight_quant_2d(nv, W, torch, dev, peak):
+    """Weights: 4 x 3072x3072 and 2 x 3072x14336 bf16, N(0, 0.02^2), 16x16 tiles."""
+    gen = torch.Generator(device=dev)
     ws_ = []
     for i, (M, N) in enumerate(W.WEIGHT_SHAPES):
         gen.manual_seed(5000 + i)
@@ -528,25 +532,45 @@ def secondary_rows(nv, W, torch, dev, l2, peak):
         ws_.append((w, nv.weight_quant_2d(w), nv.w2d_workspace(M, N, dev)))
     ms = _time_graph(torch, lambda i: [nv.weight_quant_2d(w, workspace=wk, out=o) for (w, o, wk) in ws_], 1, 10)
     b = sum(M * N for (M, N) in W.WEIGHT_SHAPES) * W2D_BYTES_PER_ELEM
-    rows["weight_quant_2d"] = {"GB/s": b / ms / 1e6, "ms_all_six": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms_all_six": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
 
-    # activations 7040 x 3072, 1-D blocks
+
+def row_activation_quant_1d(nv, W, torch, dev, peak):
+    """Activations 7040 x 3072 bf16 ~ N(0, 1), 1-D 16-element blocks (four rotating matrices)."""
+    gen = torch.Generator(device=dev)
     gen.manual_seed(5100)
     acts = [torch.randn((T_CHUNK, 1, 3072), generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
     aouts = [nv.kv_smooth_quant(a, False) for a in acts]
     aws = nv.kv_workspace(T_CHUNK, 1, 3072, 1, dev)
     ms = _time_graph(torch, lambda i: nv.kv_smooth_quant(acts[i % 4], False, workspace=aws, out=aouts[i % 4]), 8, 20)
     b = T_CHUNK * 3072 * QUANT_BYTES_PER_ELEM
-    rows["activation_quant_1d"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
 
-    # single K tensor (smooth+quant alone, no V to overlap with)
-    kx = [xs[2 * i] for i in range(4)]
+
+def row_k_only_smooth_quant(nv, W, torch, dev, peak):
+    """A single K tensor smoothed and quantized alone (no V to overlap with); four rotating K."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
+    kx = [_chunk_k_device(torch, gen, dev) for _ in range(4)]
     kouts = [nv.kv_smooth_quant(k, True) for k in kx]
     kws = nv.kv_workspace(T_CHUNK, HEADS, HEAD_DIM, 1, dev)
     ms = _time_graph(torch, lambda i: nv.kv_smooth_quant(kx[i % 4], True, workspace=kws, out=kouts[i % 4]), 8, 20)
     b = T_CHUNK * HEADS * HEAD_DIM * QUANT_BYTES_PER_ELEM
-    rows["k_only_smooth_quant"] = {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
-    torch.cuda.synchronize()
+    return {"GB/s": b / ms / 1e6, "ms": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+
+
+ROWS = {"kv_write_30_layers": row_kv_write_30_layers, "kv_cache_read_dequant": row_kv_cache_read_dequant,
+        "weight_quant_2d": row_weight_quant_2d, "activation_quant_1d": row_activation_quant_1d,
+        "k_only_smooth_quant": row_k_only_smooth_quant}
+
+
+def secondary_rows(nv, W, torch, dev, peak, names=None):
+    """The other hot-path rows, each on its own seeded synthetic workload (device-generated)."""
+    rows = {}
+    for name in (names or list(ROWS)):
+        rows[name] = ROWS[name](nv, W, torch, dev, peak)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     return rows
 
 

@@ -54,6 +54,7 @@ KvPlan kv_plan(int64_t T, int H, int D, int ctas) {
   g.tpr = std::min(g.C / 8, kStatsConsumers);
   g.rpp = kStatsConsumers / g.tpr;
   g.rows_per_stage = g.rpp;  // set per element size at launch (stats_stage_rows)
+  g.inv_T = T > 0 ? 1.0 / (double)T : 0.0;
   p.header_bytes = kWsAlign;
   p.ctr_bytes = kWsAlign;
   p.mean_bytes = align_up((size_t)g.C * sizeof(float), kWsAlign);

@@ -43,15 +43,19 @@ struct KvGeom {
   int tpr;  // threads per row: min(C / 8, kStatsConsumers)
   int rpp;  // rows in parallel: kStatsConsumers / tpr
   int rows_per_stage;
+  double inv_T;  // binary64 reciprocal of T: mean = fl32(sum * inv_T)
   unsigned* header;  // [0] quant CTAs finished, [1] status flags
   int* dev_status;
   int first_launch;  // 1: write *dev_status, 0: OR into it
 };
 
 // Quantization launch shape: CTAs of cw * rpp threads cover cw block columns of
-// rpp rows; gx CTAs across the columns, gy down the rows, one z slice per job.
+// rpp rows.  A 1-D grid: first gx * gy_early CTAs for each job but the last (they
+// run beside the statistics grid, one per SM in total), then gx * gy_last CTAs
+// for the last job (two per SM once the statistics grid has finished).
 struct KvQuantShape {
-  int cw, rpp, gx, gy;
+  int cw, rpp, gx, gy_early, gy_last;
+  int ctas;  // total CTAs
 };
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s);

@@ -8,11 +8,13 @@
 // the block's absolute maximum to 6 and to 4; the block is quantized to E2M1
 // under both and the candidate with the lower squared error is kept, ties to 6.
 //
-// Launch: grid (gx, gy, jobs), CTAs of cw * rpp threads.  Thread (c, r) of a CTA
-// owns block column blockIdx.x * cw + c (16 channels) and the rows
-// blockIdx.y * rpp + r + i * gy * rpp, so the column's 16 channel means stay in
-// registers for the whole loop; the next row's block is loaded before the
-// current one is quantized.  A warp reads 32 consecutive blocks of a row
+// Launch: a 1-D grid of CTAs of cw * rpp threads; CTA (job, y, x) owns block
+// columns x * cw + c (16 channels each) of the rows y * rpp + r + i * gy * rpp, so
+// a column's 16 channel means stay in registers for the whole loop; the next
+// row's block is loaded before the current one is quantized.  All jobs but the
+// last come first with gy_early row slots each (they run beside the statistics
+// grid); the last job follows with gy_last slots (two CTAs per SM once the
+// statistics grid has finished).  A warp reads 32 consecutive blocks of a row
 // (coalesced) and writes their codes and scale bytes contiguously.
 //
 // The grid is a programmatic dependent of the statistics grid and may run beside
@@ -131,15 +133,31 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
                                                           const KvQuantShape S) {
   __shared__ QuantConst qc;
   constexpr int es = kBF16 ? 2 : 4;
-  const KvJob& J = b.job[blockIdx.z];
+  // this CTA's job, row slot y of gy, and column group x
+  const int n_early = S.gx * S.gy_early * (b.n - 1);
+  int job, y, x, gy;
+  if ((int)blockIdx.x < n_early) {
+    job = blockIdx.x / (S.gx * S.gy_early);
+    const int rem = blockIdx.x - job * (S.gx * S.gy_early);
+    y = rem / S.gx;
+    x = rem - y * S.gx;
+    gy = S.gy_early;
+  } else {
+    job = b.n - 1;
+    const int rem = blockIdx.x - n_early;
+    y = rem / S.gx;
+    x = rem - y * S.gx;
+    gy = S.gy_last;
+  }
+  const KvJob& J = b.job[job];
   const int nbr = G.C / 16;  // blocks per row
   const int c = threadIdx.x % S.cw, rl = threadIdx.x / S.cw;
-  const int cb = blockIdx.x * S.cw + c;
+  const int cb = x * S.cw + c;
   const bool active = cb < nbr;
   // rows r, r + step, r + 2 step, ... in pairs (r, r + step)
-  const int64_t step = (int64_t)S.gy * S.rpp;
+  const int64_t step = (int64_t)gy * S.rpp;
   const size_t row_bytes = (size_t)G.C * es;
-  int64_t r = (int64_t)blockIdx.y * S.rpp + rl;
+  int64_t r = (int64_t)y * S.rpp + rl;
   const uint8_t* px = static_cast<const uint8_t*>(J.x) + (size_t)16 * cb * es + (size_t)r * row_bytes;
   const size_t px_step = (size_t)step * row_bytes;
 
@@ -174,7 +192,7 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
     const bool ok = (E > 0.0f) && (Sc > 0.0f) && finite_f(inv);
     qc.tab[e] = make_float2(ok ? inv : 0.0f, ok ? __fmul_rn(E, E) : 0.0f);
   }
-  if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+  if (threadIdx.x == 0 && x == 0 && y == 0) {
     *J.tensor_scale = g;
     if (nonfinite) atomicOr(G.header + 1, kStatusNonfinite);
   }
@@ -228,7 +246,7 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned total = gridDim.x;
     qc.last = (atomicAdd(G.header + 0, 1u) + 1u == total);
   }
   __syncthreads();
@@ -257,21 +275,27 @@ KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms) {
   q.cw = nbr < 256 ? nbr : 256;
   q.rpp = 256 / q.cw;
   q.gx = (nbr + q.cw - 1) / q.cw;
-  // one wave: 2 CTAs per SM over all jobs
-  const int64_t want = (int64_t)2 * (sms > 0 ? sms : 1);
-  int64_t per_job = (want + n_jobs - 1) / n_jobs;
-  int64_t gy = (per_job + q.gx - 1) / q.gx;
   const int64_t max_gy = (T + q.rpp - 1) / q.rpp;
-  if (gy > max_gy) gy = max_gy;
-  if (gy < 1) gy = 1;
-  if (gy > 65535) gy = 65535;
-  q.gy = (int)gy;
+  auto clamp_gy = [&](int64_t want_ctas) {
+    int64_t gy = (want_ctas + q.gx - 1) / q.gx;
+    if (gy > max_gy) gy = max_gy;
+    if (gy < 1) gy = 1;
+    if (gy > 65535) gy = 65535;
+    return (int)gy;
+  };
+  const int64_t s = sms > 0 ? sms : 1;
+  // jobs but the last share two CTAs per SM (one of which fits beside the statistics
+  // grid); the last job, which starts when the statistics grid has finished, gets two
+  // CTAs per SM of its own
+  q.gy_early = n_jobs > 1 ? clamp_gy((2 * s + n_jobs - 1) / n_jobs) : 1;
+  q.gy_last = clamp_gy(2 * s);
+  q.ctas = q.gx * q.gy_early * (n_jobs - 1) + q.gx * q.gy_last;
   return q;
 }
 
 cudaError_t launch_kv_quant(const KvBatch& b, const KvGeom& g, const KvQuantShape& q, bool bf16, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(q.gx, q.gy, b.n);
+  cfg.gridDim = dim3(q.ctas);
   cfg.blockDim = dim3(q.cw * q.rpp);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

@@ -44,6 +44,13 @@ constexpr int kThreads = kStatsConsumers + 32;  // consumer warps + one producer
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kStatusTimeout = 2u;
 
+// Atomic add with release semantics at GPU scope: the calling thread's earlier
+// writes and atomics, and those it has observed through a CTA barrier, are
+// visible before the counter moves.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // (s, n) pairs carry sum = s + n (n: the low part lost by s).
 __device__ __forceinline__ void comp_add(float& s, float& n, float s2, float n2) {
   float t, e;
@@ -221,18 +228,17 @@ __device__ void reduce_slice(const KvJob& J, const KvGeom& G, StatsSmem& sm, int
         mx = max_nan(mx, v.w);
       }
       const int ch = cb + threadIdx.x;
-      const float mu = J.mean_in ? J.mean_in[ch] : (float)(((double)s + (double)l) / (double)G.T);
+      const float mu = J.mean_in ? J.mean_in[ch] : (float)(((double)s + (double)l) * G.inv_T);
       J.mean[ch] = mu;
       if (J.mean_out) J.mean_out[ch] = mu;
       cam = max_nan(cam, max_nan(__fsub_rn(mx, mu), __fsub_rn(mu, mn)));
     }
   }
-  __threadfence();  // the means are visible before the job is marked ready
+  // consumer_max's barriers order every thread's mean stores before thread 0's release
   const float m = consumer_max(cam, sm, nt);
   if (threadIdx.x == 0) {
     atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
-    __threadfence();
-    atomicAdd(J.ctr + 2, 1u);  // this CTA's share of the job is final
+    red_release_add(J.ctr + 2, 1u);  // this CTA's share of the job is final
   }
 }
 
@@ -348,10 +354,9 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         }
       }
       if (smooth) {
-        __threadfence();
-        named_barrier(1, consumers);
+        named_barrier(1, consumers);  // every consumer's partials are written
         if (threadIdx.x == 0) {
-          atomicAdd(J.ctr + 1, 1u);  // this CTA's partials are published
+          red_release_add(J.ctr + 1, 1u);  // this CTA's partials are published
           // every CTA streams the same job at about the same time: a short wait
           const uint64_t t0 = bulk_timer_ns();
           int ok = 1;
@@ -371,8 +376,7 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         const float m = consumer_max(amax, sm, consumers);
         if (threadIdx.x == 0) {
           atomicMax(J.ctr + 0, __float_as_uint(m) & 0x7fffffffu);
-          __threadfence();
-          atomicAdd(J.ctr + 2, 1u);  // this CTA's share of the job is final
+          red_release_add(J.ctr + 2, 1u);  // this CTA's share of the job is final
         }
       }
     }

@@ -54,10 +54,8 @@ __device__ __forceinline__ uint64_t timer_ns() {
 // within a factor of two of each other), err = fl(E^2 * acc).
 __device__ __forceinline__ void quant_block(const float z[16], const float2* tab, float k6, float k4, bool nonfinite,
                                             uint2& code, uint32_t& sc) {
-  float a[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = fmaxf(fabsf(z[2 * i]), fabsf(z[2 * i + 1]));
-  const float ma = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+  const float ma = max3_abs(max3_abs(max3_abs(z[0], z[1], z[2]), max3_abs(z[3], z[4], z[5]), max3_abs(z[6], z[7], z[8])),
+                            max3_abs(z[9], z[10], z[11]), max3_abs(max3_abs(z[12], z[13], z[14]), z[15], 0.0f));
   const float2 s2 = __fmul2_rn(make_float2(ma, ma), make_float2(k6, k4));
   const uint32_t e = e4m3x2(s2.x, s2.y);
   const uint32_t e6 = e & 0x7Fu, e4 = (e >> 8) & 0x7Fu;
@@ -124,6 +122,19 @@ __device__ __forceinline__ void smooth_block(const RawBlock<kBF16>& r, const flo
       z[4 * q + 3] = __fsub_rn(__uint_as_float(r.v[q].w), mu[4 * q + 3]);
     }
   }
+}
+
+// Smooths, quantizes and stores one loaded block.
+template <bool kBF16>
+__device__ __forceinline__ void quant_store(const RawBlock<kBF16>& r, const float mu[16], const float2* tab, float k6,
+                                            float k4, bool nonfinite, uint2* pc, uint8_t* ps) {
+  float z[16];
+  smooth_block<kBF16>(r, mu, z);
+  uint2 code;
+  uint32_t sc;
+  quant_block(z, tab, k6, k4, nonfinite, code, sc);
+  *pc = code;
+  *ps = (uint8_t)sc;
 }
 
 }  // namespace
@@ -215,30 +226,24 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
     uint2* pc = reinterpret_cast<uint2*>(J.codes) + (size_t)r * nbr + cb;
     uint8_t* ps = J.scales + (size_t)r * nbr + cb;
     const size_t pq_step = (size_t)step * nbr;
-    for (; r < G.T; r += 2 * step) {
-      // next pair in flight while this pair is quantized
-      RawBlock<kBF16> n0 = {}, n1 = {};
-      if (r + 2 * step < G.T) load_block<kBF16>(px + 2 * px_step, n0);
-      if (r + 3 * step < G.T) load_block<kBF16>(px + 3 * px_step, n1);
-      const bool second = r + step < G.T;
-      float z0[16], z1[16];
-      smooth_block<kBF16>(a0, mu, z0);
-      smooth_block<kBF16>(a1, mu, z1);
-      uint2 c0, c1;
-      uint32_t s0, s1;
-      quant_block(z0, qc.tab, k6, k4, nonfinite, c0, s0);
-      quant_block(z1, qc.tab, k6, k4, nonfinite, c1, s1);
-      *pc = c0;
-      *ps = (uint8_t)s0;
-      if (second) {
-        pc[pq_step] = c1;
-        ps[pq_step] = (uint8_t)s1;
-      }
-      a0 = n0;
-      a1 = n1;
-      px += 2 * px_step;
-      pc += 2 * pq_step;
-      ps += 2 * pq_step;
+    // rows k = 0 .. n-1 of this thread (row r + k * step), two per half-iteration: the
+    // pair in (a0, a1) is quantized while the next pair loads into (b0, b1), then
+    // the roles swap, so no buffer is copied
+    const int n = r < G.T ? (int)((G.T - r + step - 1) / step) : 0;
+    RawBlock<kBF16> b0, b1;
+    for (int k = 0; k < n; k += 4) {
+      if (k + 2 < n) load_block<kBF16>(px + 2 * px_step, b0);
+      if (k + 3 < n) load_block<kBF16>(px + 3 * px_step, b1);
+      quant_store<kBF16>(a0, mu, qc.tab, k6, k4, nonfinite, pc, ps);
+      if (k + 1 < n) quant_store<kBF16>(a1, mu, qc.tab, k6, k4, nonfinite, pc + pq_step, ps + pq_step);
+      if (k + 2 >= n) break;
+      if (k + 4 < n) load_block<kBF16>(px + 4 * px_step, a0);
+      if (k + 5 < n) load_block<kBF16>(px + 5 * px_step, a1);
+      quant_store<kBF16>(b0, mu, qc.tab, k6, k4, nonfinite, pc + 2 * pq_step, ps + 2 * pq_step);
+      if (k + 3 < n) quant_store<kBF16>(b1, mu, qc.tab, k6, k4, nonfinite, pc + 3 * pq_step, ps + 3 * pq_step);
+      px += 4 * px_step;
+      pc += 4 * pq_step;
+      ps += 4 * pq_step;
     }
   }
 

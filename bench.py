@@ -523,16 +523,24 @@ def row_kv_cache_read_dequant(nv, W, torch, dev, peak):
 
 
 def row_weight_quant_2d(nv, W, torch, dev, peak):
-    """Weights: 4 x 3072x3072 and 2 x 3072x14336 bf16, N(0, 0.02^2), 16x16 tiles."""
+    """Weights: 4 x 3072x3072 and 2 x 3072x14336 bf16, N(0, 0.02^2), 16x16 tiles, in one batched call
+    (and, for comparison, as six single calls)."""
     gen = torch.Generator(device=dev)
     ws_ = []
     for i, (M, N) in enumerate(W.WEIGHT_SHAPES):
         gen.manual_seed(5000 + i)
         w = (torch.randn((M, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
         ws_.append((w, nv.weight_quant_2d(w), nv.w2d_workspace(M, N, dev)))
-    ms = _time_graph(torch, lambda i: [nv.weight_quant_2d(w, workspace=wk, out=o) for (w, o, wk) in ws_], 1, 10)
+    mats = [w for (w, _, _) in ws_]
+    bouts, bstatus = nv.weight_quant_2d_batched(mats)
+    bws = nv.w2d_batched_workspace(len(mats), dev)
+    ms = _time_graph(torch, lambda i: nv.weight_quant_2d_batched(mats, workspace=bws, outs=bouts, status=bstatus),
+                     1, 10)
+    ms_single = _time_graph(torch, lambda i: [nv.weight_quant_2d(w, workspace=wk, out=o) for (w, o, wk) in ws_],
+                            1, 10)
     b = sum(M * N for (M, N) in W.WEIGHT_SHAPES) * W2D_BYTES_PER_ELEM
-    return {"GB/s": b / ms / 1e6, "ms_all_six": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms_all_six": ms, "ms_six_single_calls": ms_single, "bytes": b,
+            "frac": b / ms / 1e6 / peak}
 
 
 def row_activation_quant_1d(nv, W, torch, dev, peak):

@@ -200,6 +200,32 @@ nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, 
                                    uint8_t* scales, float* tensor_scale, int* dev_status, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/* One matrix of a batched weight call (the matrices may differ in shape). */
+typedef struct nvfp4_w2d_job {
+  const void* w;        /* device [M][N] input */
+  int64_t M, N;         /* multiples of 16; M may be 0 */
+  uint8_t* codes;       /* device [M][N/2] */
+  uint8_t* scales;      /* device [M/16][N/16] */
+  float* tensor_scale;  /* device [1], this matrix's g */
+} nvfp4_w2d_job;
+
+/* Workspace for nvfp4_weight_quant_2d_batched with n_jobs matrices (current
+ * device); 0 for n_jobs < 1. */
+size_t nvfp4_w2d_batched_workspace_bytes(int n_jobs);
+
+/* Quantize n_jobs independent weight matrices (e.g. all linear layers of a
+ * block) in one amax launch and one quantization launch: each matrix gets
+ * exactly the result nvfp4_weight_quant_2d would give it, with its own tensor
+ * scale.  `jobs` is a HOST array read before the call returns; matrices
+ * beyond 64 go into further launch pairs on the same stream.  *dev_status is
+ * the OR over matrices.  The workspace (at least
+ * nvfp4_w2d_batched_workspace_bytes(n_jobs) bytes, 256-byte aligned) needs no
+ * initialisation; calls that share it must not overlap.
+ * Errors: NVFP4_EINVAL (NULL jobs, n_jobs < 1, bad dt or a NULL pointer in a
+ * job), NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA. */
+nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs, nvfp4_in_dtype dt,
+                                           int* dev_status, void* workspace, size_t workspace_bytes, void* stream);
+
 /* nvfp4_weight_quant_2d without a workspace.  The pages have no counterpart:
  * this call exists for callers that cannot allocate device memory or hand the
  * library a scratch buffer -- e.g. a runtime that passes the library only the

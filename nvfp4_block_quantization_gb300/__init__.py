@@ -16,12 +16,13 @@ import ctypes
 from typing import NamedTuple, Optional, Sequence
 
 from . import _lib
-from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job
+from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_w2d_job
 
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "w2d_workspace", "weight_quant_2d", "weight_dequant_2d", "load_library",
+    "kv_dequant", "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
+    "weight_dequant_2d", "load_library",
 ]
 
 
@@ -231,6 +232,52 @@ def weight_quant_2d(w, workspace=None, out: Optional[W2dQuantized] = None, strea
                                     _ptr(workspace), workspace.numel(), _stream(stream))
     _lib.check(st, "nvfp4_weight_quant_2d")
     return W2dQuantized(codes, scales, g, status)
+
+
+def w2d_batched_workspace(n_jobs: int, device=None):
+    torch = _torch()
+    nbytes = _lib.nvfp4_w2d_batched_workspace_bytes(n_jobs)
+    if nbytes == 0:
+        raise NVFP4Error(_lib.NVFP4_EINVAL, "w2d_batched_workspace")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def weight_quant_2d_batched(ws: Sequence, workspace=None, outs=None, status=None, stream=None):
+    """Quantize several weight matrices (shapes may differ, dtype shared) in one amax and one quantizer launch.
+
+    Returns (list of W2dQuantized, status) with one shared device status word (OR over matrices).
+    """
+    torch = _torch()
+    n = len(ws)
+    if n == 0:
+        raise ValueError("need at least one matrix")
+    w0 = ws[0]
+    for w in ws:
+        _check_cuda(w)
+        if w.dim() != 2 or w.dtype != w0.dtype:
+            raise ValueError("all matrices of a batch are 2-D and share a dtype")
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=w0.device)
+    if outs is None:
+        outs = []
+        for w in ws:
+            M, N = w.shape
+            outs.append(W2dQuantized(torch.empty((M, N // 2), dtype=torch.uint8, device=w.device),
+                                     torch.empty((M // 16, N // 16), dtype=torch.uint8, device=w.device),
+                                     torch.empty(1, dtype=torch.float32, device=w.device), status))
+    if workspace is None:
+        workspace = w2d_batched_workspace(n, w0.device)
+    jobs = (nvfp4_w2d_job * n)()
+    for i, (w, o) in enumerate(zip(ws, outs)):
+        jobs[i].w = w.data_ptr()
+        jobs[i].M, jobs[i].N = w.shape
+        jobs[i].codes = o.codes.data_ptr()
+        jobs[i].scales = o.scales.data_ptr()
+        jobs[i].tensor_scale = o.tensor_scale.data_ptr()
+    st = _lib.nvfp4_weight_quant_2d_batched(jobs, n, _dt(w0), _ptr(status), _ptr(workspace), workspace.numel(),
+                                            _stream(stream))
+    _lib.check(st, "nvfp4_weight_quant_2d_batched")
+    return outs, status
 
 
 def weight_dequant_2d(codes, scales, tensor_scale, out=None, stream=None):

@@ -28,6 +28,8 @@ EXPORTS = (
     "nvfp4_kv_dequant",
     "nvfp4_w2d_workspace_bytes",
     "nvfp4_weight_quant_2d",
+    "nvfp4_w2d_batched_workspace_bytes",
+    "nvfp4_weight_quant_2d_batched",
     "nvfp4_weight_quant_2d_static",
     "nvfp4_weight_dequant_2d",
 )
@@ -39,6 +41,17 @@ class nvfp4_kv_job(ctypes.Structure):
         ("smooth", ctypes.c_int),
         ("mean_in", ctypes.c_void_p),
         ("mean_out", ctypes.c_void_p),
+        ("codes", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+    ]
+
+
+class nvfp4_w2d_job(ctypes.Structure):
+    _fields_ = [
+        ("w", ctypes.c_void_p),
+        ("M", ctypes.c_int64),
+        ("N", ctypes.c_int64),
         ("codes", ctypes.c_void_p),
         ("scales", ctypes.c_void_p),
         ("tensor_scale", ctypes.c_void_p),
@@ -88,6 +101,10 @@ def load(path: str | None = None):
     lib.nvfp4_w2d_workspace_bytes.restype = sz
     lib.nvfp4_weight_quant_2d.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
     lib.nvfp4_weight_quant_2d.restype = i32
+    lib.nvfp4_w2d_batched_workspace_bytes.argtypes = [i32]
+    lib.nvfp4_w2d_batched_workspace_bytes.restype = sz
+    lib.nvfp4_weight_quant_2d_batched.argtypes = [ctypes.POINTER(nvfp4_w2d_job), i32, i32, vp, vp, sz, vp]
+    lib.nvfp4_weight_quant_2d_batched.restype = i32
     lib.nvfp4_weight_quant_2d_static.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp]
     lib.nvfp4_weight_quant_2d_static.restype = i32
     lib.nvfp4_weight_dequant_2d.argtypes = [vp, vp, vp, i64, i64, vp, vp]
@@ -155,3 +172,11 @@ def nvfp4_weight_quant_2d_static(w, dt, M, N, codes, scales, tensor_scale, dev_s
 
 def nvfp4_weight_dequant_2d(codes, scales, tensor_scale, M, N, out_bf16, stream):
     return load().nvfp4_weight_dequant_2d(codes, scales, tensor_scale, M, N, out_bf16, stream)
+
+
+def nvfp4_w2d_batched_workspace_bytes(n_jobs):
+    return load().nvfp4_w2d_batched_workspace_bytes(n_jobs)
+
+
+def nvfp4_weight_quant_2d_batched(jobs, n_jobs, dt, dev_status, workspace, workspace_bytes, stream):
+    return load().nvfp4_weight_quant_2d_batched(jobs, n_jobs, dt, dev_status, workspace, workspace_bytes, stream)

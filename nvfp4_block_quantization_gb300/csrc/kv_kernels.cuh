@@ -70,6 +70,26 @@ struct W2dGeom {
   int64_t M, N;
   int amax_ctas;
 };
+
+// One matrix of a weight launch: its CTAs are [amax_begin, amax_begin + amax_ctas) of
+// the amax grid (its partials sit at those indices of the workspace) and
+// [quant_begin, quant_begin + quant_ctas) of the quantization grid.
+constexpr int kMaxW2dJobs = 64;
+struct W2dJob {
+  const void* w;
+  int64_t M, N;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;
+  int amax_begin, amax_ctas, quant_begin, quant_ctas;
+};
+struct W2dBatch {
+  W2dJob job[kMaxW2dJobs];
+  int n;
+  int reset_status;  // 1: the launch starts *dev_status at 0 (first launch of a call)
+};
+cudaError_t launch_w2d_batch(const W2dBatch& b, bool bf16, int amax_ctas, int quant_ctas, float* amax_part,
+                             int* dev_status, cudaStream_t s);
 cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8_t* codes, uint8_t* scales,
                              float* tensor_scale, int* dev_status, float* amax_part, int quant_ctas,
                              cudaStream_t s);

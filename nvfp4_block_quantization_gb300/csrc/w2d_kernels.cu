@@ -31,16 +31,27 @@ __device__ __forceinline__ void load_row16(const void* base, int64_t elem, float
   }
 }
 
-// Absolute maximum (NaN-propagating) of the matrix, per CTA: CTA c reads the
-// contiguous range of 16-byte chunks [c n / P, (c + 1) n / P) with 8 loads in
-// flight per thread; partial c goes to amax_part[c].
+// The job of CTA `bx` in a launch that gives job j the CTAs [begin_j, begin_j + n_j).
+__device__ __forceinline__ int w2d_job_of(const W2dBatch& b, int bx, bool quant) {
+  int j = 0;
+  while (j + 1 < b.n && bx >= (quant ? b.job[j + 1].quant_begin : b.job[j + 1].amax_begin)) ++j;
+  return j;
+}
+
+// Absolute maximum (NaN-propagating) of each matrix, per CTA: CTA c of job j
+// reads the contiguous range of 16-byte chunks [c n / k, (c + 1) n / k) of the
+// job's k CTAs with 8 loads in flight per thread; the partial goes to
+// amax_part[blockIdx.x] (a job's partials are contiguous).
 template <bool kBF16>
-__global__ void __launch_bounds__(256) w2d_amax_kernel(const void* w, int64_t n16, float* amax_part, int* dev_status) {
+__global__ void __launch_bounds__(256) w2d_amax_kernel(const __grid_constant__ W2dBatch bt, float* amax_part,
+                                                       int* dev_status) {
   __shared__ float red[32];
-  if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status) *dev_status = 0;
-  const uint4* p = static_cast<const uint4*>(w);
-  const int64_t nv = n16 * (kBF16 ? 2 : 4);  // 16-byte chunks
-  const int64_t a = (int64_t)blockIdx.x * nv / gridDim.x, b = (int64_t)(blockIdx.x + 1) * nv / gridDim.x;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status && bt.reset_status) *dev_status = 0;
+  const W2dJob& J = bt.job[w2d_job_of(bt, blockIdx.x, false)];
+  const int lc = blockIdx.x - J.amax_begin;
+  const uint4* p = static_cast<const uint4*>(J.w);
+  const int64_t nv = J.M * J.N / 16 * (kBF16 ? 2 : 4);  // 16-byte chunks
+  const int64_t a = (int64_t)lc * nv / J.amax_ctas, b = (int64_t)(lc + 1) * nv / J.amax_ctas;
   constexpr int U = 8;
   uint32_t mw = 0u;  // bf16: max of |x| pairs
   float mf = 0.0f;   // fp32
@@ -80,13 +91,18 @@ __global__ void __launch_bounds__(256) w2d_amax_kernel(const void* w, int64_t n1
 // to 6) and the winner stores its codes and the scale byte.  A warp covers 16
 // adjacent tiles: 512 contiguous bytes of every tile row.
 template <bool kBF16>
-__global__ void __launch_bounds__(256) w2d_quant_kernel(const void* w, int64_t M, int64_t N,
-                                                        const float* amax_part, int namax, uint8_t* codes,
-                                                        uint8_t* scales, float* tensor_scale, int* dev_status) {
+__global__ void __launch_bounds__(256) w2d_quant_kernel(const __grid_constant__ W2dBatch bt, const float* amax_part,
+                                                        int* dev_status) {
   __shared__ QuantTable tab;
   __shared__ float red[32];
+  const W2dJob& J = bt.job[w2d_job_of(bt, blockIdx.x, true)];
+  const void* w = J.w;
+  const int64_t M = J.M, N = J.N;
+  uint8_t* codes = J.codes;
+  uint8_t* scales = J.scales;
+  const int lq = blockIdx.x - J.quant_begin;  // this CTA within the job's CTAs
   float m = 0.0f;
-  for (int i = threadIdx.x; i < namax; i += blockDim.x) m = max_nan(m, amax_part[i]);
+  for (int i = threadIdx.x; i < J.amax_ctas; i += blockDim.x) m = max_nan(m, amax_part[J.amax_begin + i]);
   for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
@@ -103,16 +119,16 @@ __global__ void __launch_bounds__(256) w2d_quant_kernel(const void* w, int64_t M
   const float kM = __frcp_rn(__fmul_rn(half ? 4.0f : 6.0f, g));
   build_table(&tab, g);
   __syncthreads();
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *tensor_scale = g;
+  if (lq == 0 && threadIdx.x == 0) {
+    *J.tensor_scale = g;
     if (nonfinite && dev_status) atomicOr(dev_status, NVFP4_DEV_NONFINITE_FLAG);
   }
 
   const unsigned pair_mask = 3u << (threadIdx.x & 30);
   const int64_t TN = N / 16;
   const int64_t ntiles = (M / 16) * TN;
-  const int64_t npairs = (int64_t)gridDim.x * (blockDim.x / 2);
-  for (int64_t tl = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 2; tl < ntiles; tl += npairs) {
+  const int64_t npairs = (int64_t)J.quant_ctas * (blockDim.x / 2);
+  for (int64_t tl = ((int64_t)lq * blockDim.x + threadIdx.x) / 2; tl < ntiles; tl += npairs) {
     const int64_t ti = tl / TN, tj = tl - ti * TN;
     const int64_t base = ti * 16 * N + tj * 16;
     // tile amax: this lane's 8 rows, then the partner's
@@ -234,21 +250,35 @@ __global__ void __launch_bounds__(256) w2d_dequant_kernel(const uint8_t* __restr
   }
 }
 
+cudaError_t launch_w2d_batch(const W2dBatch& b, bool bf16, int amax_ctas, int quant_ctas, float* amax_part,
+                             int* dev_status, cudaStream_t s) {
+  if (bf16) w2d_amax_kernel<true><<<amax_ctas, 256, 0, s>>>(b, amax_part, dev_status);
+  else w2d_amax_kernel<false><<<amax_ctas, 256, 0, s>>>(b, amax_part, dev_status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (bf16) w2d_quant_kernel<true><<<quant_ctas, 256, 0, s>>>(b, amax_part, dev_status);
+  else w2d_quant_kernel<false><<<quant_ctas, 256, 0, s>>>(b, amax_part, dev_status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8_t* codes, uint8_t* scales,
                              float* tensor_scale, int* dev_status, float* amax_part, int quant_ctas,
                              cudaStream_t s) {
-  const int64_t n16 = geo.M * geo.N / 16;
-  if (bf16) w2d_amax_kernel<true><<<geo.amax_ctas, 256, 0, s>>>(w, n16, amax_part, dev_status);
-  else w2d_amax_kernel<false><<<geo.amax_ctas, 256, 0, s>>>(w, n16, amax_part, dev_status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (bf16)
-    w2d_quant_kernel<true><<<quant_ctas, 256, 0, s>>>(w, geo.M, geo.N, amax_part, geo.amax_ctas, codes, scales,
-                                                      tensor_scale, dev_status);
-  else
-    w2d_quant_kernel<false><<<quant_ctas, 256, 0, s>>>(w, geo.M, geo.N, amax_part, geo.amax_ctas, codes, scales,
-                                                       tensor_scale, dev_status);
-  return cudaGetLastError();
+  W2dBatch b;
+  b.n = 1;
+  b.reset_status = 1;
+  W2dJob& j = b.job[0];
+  j.w = w;
+  j.M = geo.M;
+  j.N = geo.N;
+  j.codes = codes;
+  j.scales = scales;
+  j.tensor_scale = tensor_scale;
+  j.amax_begin = 0;
+  j.amax_ctas = geo.amax_ctas;
+  j.quant_begin = 0;
+  j.quant_ctas = quant_ctas;
+  return launch_w2d_batch(b, bf16, geo.amax_ctas, quant_ctas, amax_part, dev_status, s);
 }
 
 cudaError_t launch_w2d_dequant(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t M, int64_t N,

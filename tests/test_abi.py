@@ -113,6 +113,31 @@ def test_weight_argument_errors(lib):
     assert L.nvfp4_weight_dequant_2d(g, g, None, 32, 32, g, None) == L.NVFP4_EINVAL
 
 
+def test_weight_batched_argument_errors(lib):
+    from nvfp4_block_quantization_gb300 import _lib as L
+
+    g = P(4096)
+
+    def jobs(*specs):
+        arr = (L.nvfp4_w2d_job * len(specs))()
+        for k, (w, M, N, c, s, t) in enumerate(specs):
+            arr[k].w, arr[k].M, arr[k].N, arr[k].codes, arr[k].scales, arr[k].tensor_scale = w, M, N, c, s, t
+        return arr
+
+    b = L.nvfp4_weight_quant_2d_batched
+    ok = (g, 32, 32, g, g, g)
+    assert b(None, 1, 0, None, g, 1 << 20, None) == L.NVFP4_EINVAL
+    assert b(jobs(ok), 0, 0, None, g, 1 << 20, None) == L.NVFP4_EINVAL
+    assert b(jobs(ok), 1, 2, None, g, 1 << 20, None) == L.NVFP4_EINVAL
+    assert b(jobs(ok, (g, 20, 32, g, g, g)), 2, 0, None, g, 1 << 20, None) == L.NVFP4_ESHAPE
+    assert b(jobs(ok, (g, 32, 8, g, g, g)), 2, 0, None, g, 1 << 20, None) == L.NVFP4_ESHAPE
+    assert b(jobs(ok, (None, 32, 32, g, g, g)), 2, 0, None, g, 1 << 20, None) == L.NVFP4_EINVAL
+    assert b(jobs(ok, (g, 32, 32, g, g, None)), 2, 0, None, g, 1 << 20, None) == L.NVFP4_EINVAL
+    assert b(jobs((g, 32, 32, P(4097), g, g)), 1, 0, None, g, 1 << 20, None) == L.NVFP4_EALIGN
+    assert b(jobs(ok), 1, 0, P(4098), g, 1 << 20, None) == L.NVFP4_EALIGN
+    assert L.nvfp4_w2d_batched_workspace_bytes(0) == 0
+
+
 def test_product_path_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "nvfp4_block_quantization_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -309,6 +309,53 @@ def test_weight_2d_full_size_sampled_tiles(nv, oracle):
         assert np.array_equal(got, d["codes"].astype(np.int64))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_weight_2d_batched_bit_exact(nv, oracle, dtype):
+    """Mixed shapes (one empty) in one batched call: every matrix matches the oracle on its own."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    shapes = [(256, 512), (0, 64), (48, 80), (160, 3072), (16, 16), (512, 256)]
+    ws_np = [W.weight(20 + i, M, N) for i, (M, N) in enumerate(shapes)]
+    if dtype == "bf16":
+        ws_np = [W.to_bf16_bits(w) for w in ws_np]
+    outs, status = nv.weight_quant_2d_batched([dev(w) for w in ws_np])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for w, o in zip(ws_np, outs):
+        if w.shape[0] == 0:
+            assert float(o.tensor_scale.item()) == 0.0
+            continue
+        ref = oracle.weight_quant_2d(w)
+        assert_same_bits_f32(float(o.tensor_scale.item()), ref["g"])
+        assert np.array_equal(host(o.scales), ref["scales"])
+        assert np.array_equal(host(o.codes), ref["codes"])
+
+
+def test_weight_2d_batched_many_and_nonfinite(nv):
+    """70 matrices (two launch pairs of at most 64) equal the single calls; a NaN in the first sets the shared status."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    shapes = [(16 * (1 + i % 5), 16 * (1 + (3 * i) % 7)) for i in range(70)]
+    ws = [dev(W.to_bf16_bits(W.weight(100 + i, M, N))) for i, (M, N) in enumerate(shapes)]
+    ws[0][3, 5] = float("nan")
+    outs, status = nv.weight_quant_2d_batched(ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+    assert torch.isnan(outs[0].tensor_scale).all()
+    assert bool((outs[0].scales == 0x7F).all()) and bool((outs[0].codes == 0).all())
+    for w, o in zip(ws[1:], outs[1:]):
+        s = nv.weight_quant_2d(w)
+        torch.cuda.synchronize()
+        assert int(s.status.item()) == 0
+        assert torch.equal(o.codes, s.codes) and torch.equal(o.scales, s.scales)
+        assert torch.equal(o.tensor_scale.view(torch.int32), s.tensor_scale.view(torch.int32))
+    # a clean batch after the NaN one on the same workspace and status word reports no error
+    ws2 = ws[1:]
+    outs2, status2 = nv.weight_quant_2d_batched(ws2, status=status)
+    torch.cuda.synchronize()
+    assert int(status2.item()) == 0
+
+
 def test_activations_1d_bit_exact(nv, oracle):
     from nvfp4_block_quantization_gb300 import workloads as W
 

@@ -21,8 +21,9 @@
 // it: each CTA fetches its first rows, waits (bounded) until every statistics
 // CTA has counted itself ready for this CTA's job, reads the job's amax, and
 // builds the per-tensor table: g = fl(amax / 2688) and, per E4M3 code E,
-// fl(1 / fl(E * g)) and E * E.  The last CTA to finish resets the jobs'
-// counters in the workspace and publishes the status word.
+// fl(1 / fl(E * g)) and E * E.  Once every CTA has read the counters it needs
+// (before its rows), the last of them resets the jobs' counters in the
+// workspace and publishes the status word.
 #include "common.cuh"
 #include "kv_kernels.cuh"
 
@@ -34,7 +35,6 @@ constexpr unsigned kStatusNonfinite = 1u;
 
 struct QuantConst {
   float2 tab[128];  // {fl(1 / fl(E * g)) or 0 when unusable, E * E} per E4M3 code
-  int last;
   int ok;  // this job's statistics are final
 };
 
@@ -209,6 +209,27 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
   }
   const float k6 = __frcp_rn(__fmul_rn(6.0f, g)), k4 = __frcp_rn(__fmul_rn(4.0f, g));
   __syncthreads();
+  // Every thread of this CTA has read the counters it needs, so the CTA counts
+  // itself done with the workspace now (not after its rows): the last CTA to
+  // arrive returns the workspace to its idle state while the others still work.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(G.header + 0, 1u) + 1u == gridDim.x) {
+      __threadfence();
+      for (int j = 0; j < b.n; ++j) {
+        b.job[j].ctr[0] = 0u;
+        b.job[j].ctr[1] = 0u;
+        b.job[j].ctr[2] = 0u;
+      }
+      const unsigned st = atomicAdd(G.header + 1, 0u);
+      if (G.dev_status) {
+        if (G.first_launch) *G.dev_status = (int)st;
+        else atomicOr(G.dev_status, (int)st);
+      }
+      G.header[1] = 0u;
+      G.header[0] = 0u;
+    }
+  }
 
   if (active) {
     float mu[16];
@@ -247,31 +268,6 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
     }
   }
 
-  // the last CTA of the launch returns the workspace to its idle state
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned total = gridDim.x;
-    qc.last = (atomicAdd(G.header + 0, 1u) + 1u == total);
-  }
-  __syncthreads();
-  if (qc.last) {
-    __threadfence();
-    for (int j = threadIdx.x; j < b.n; j += blockDim.x) {
-      b.job[j].ctr[0] = 0u;
-      b.job[j].ctr[1] = 0u;
-      b.job[j].ctr[2] = 0u;
-    }
-    if (threadIdx.x == 0) {
-      const unsigned st = atomicAdd(G.header + 1, 0u);
-      if (G.dev_status) {
-        if (G.first_launch) *G.dev_status = (int)st;
-        else atomicOr(G.dev_status, (int)st);
-      }
-      G.header[1] = 0u;
-      G.header[0] = 0u;
-    }
-  }
 }
 
 KvQuantShape kv_quant_shape(int64_t T, int C, int n_jobs, int sms) {

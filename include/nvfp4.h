@@ -209,18 +209,25 @@ typedef struct nvfp4_w2d_job {
   float* tensor_scale;  /* device [1], this matrix's g */
 } nvfp4_w2d_job;
 
-/* Workspace for nvfp4_weight_quant_2d_batched with n_jobs matrices (current
- * device); 0 for n_jobs < 1. */
+/* Workspace for nvfp4_weight_quant_2d_batched (a few hundred bytes, the same
+ * for every n_jobs >= 1); 0 for n_jobs < 1. */
 size_t nvfp4_w2d_batched_workspace_bytes(int n_jobs);
 
 /* Quantize n_jobs independent weight matrices (e.g. all linear layers of a
- * block) in one amax launch and one quantization launch: each matrix gets
- * exactly the result nvfp4_weight_quant_2d would give it, with its own tensor
- * scale.  `jobs` is a HOST array read before the call returns; matrices
- * beyond 64 go into further launch pairs on the same stream.  *dev_status is
- * the OR over matrices.  The workspace (at least
- * nvfp4_w2d_batched_workspace_bytes(n_jobs) bytes, 256-byte aligned) needs no
- * initialisation; calls that share it must not overlap.
+ * block) in one enqueue: each matrix gets exactly the result
+ * nvfp4_weight_quant_2d would give it, with its own tensor scale.  `jobs` is a
+ * HOST array read before the call returns; matrices beyond 64 go into further
+ * launch pairs on the same stream.  *dev_status is the OR over matrices.
+ * Implementation: an amax grid takes the matrices one after another (smallest
+ * first) and publishes each one's amax when complete; the quantization grid
+ * runs beside it and starts on a matrix as soon as its amax is published
+ * (bounded waits of about 2 s; if one runs out, *dev_status gets
+ * NVFP4_DEV_TIMEOUT, that matrix is written as for a non-finite amax and the
+ * workspace must be zero-filled again).
+ * The workspace (at least nvfp4_w2d_batched_workspace_bytes(n_jobs) bytes,
+ * 256-byte aligned) must be ZERO-FILLED before its first use; every completed
+ * call leaves it zero, so later calls on one stream reuse it without clearing.
+ * Calls that share it must not overlap.
  * Errors: NVFP4_EINVAL (NULL jobs, n_jobs < 1, bad dt or a NULL pointer in a
  * job), NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA. */
 nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs, nvfp4_in_dtype dt,

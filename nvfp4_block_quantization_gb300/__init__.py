@@ -239,7 +239,7 @@ def w2d_batched_workspace(n_jobs: int, device=None):
     nbytes = _lib.nvfp4_w2d_batched_workspace_bytes(n_jobs)
     if nbytes == 0:
         raise NVFP4Error(_lib.NVFP4_EINVAL, "w2d_batched_workspace")
-    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")  # must start zero-filled
 
 
 def weight_quant_2d_batched(ws: Sequence, workspace=None, outs=None, status=None, stream=None):

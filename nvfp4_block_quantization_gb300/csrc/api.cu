@@ -317,9 +317,7 @@ nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, 
 
 size_t nvfp4_w2d_batched_workspace_bytes(int n_jobs) {
   if (n_jobs < 1) return 0;
-  const int sms = device_sms();
-  if (sms <= 0) return 0;
-  return align_up((size_t)(sms * 4 + std::min(n_jobs, kMaxW2dJobs)) * sizeof(float), kWsAlign);
+  return align_up((size_t)(1 + 2 * kMaxW2dJobs) * sizeof(unsigned), kWsAlign);
 }
 
 nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs, nvfp4_in_dtype dt, int* dev_status,
@@ -336,23 +334,25 @@ nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs
     if (!aligned(j.tensor_scale, 4)) return NVFP4_EALIGN;
   }
   if (!aligned(dev_status, 4)) return NVFP4_EALIGN;
+  const size_t need = align_up((size_t)(1 + 2 * kMaxW2dJobs) * sizeof(unsigned), kWsAlign);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)) return NVFP4_EWORKSPACE;
   const int sms = device_sms();
   if (sms <= 0) return NVFP4_ECUDA;
-  const size_t need = align_up((size_t)(sms * 4 + std::min(n_jobs, kMaxW2dJobs)) * sizeof(float), kWsAlign);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)) return NVFP4_EWORKSPACE;
   const bool bf16 = dt == NVFP4_IN_BF16;
   for (int first = 0; first < n_jobs; first += kMaxW2dJobs) {
     W2dBatch b;
     std::memset(&b, 0, sizeof(b));
     b.n = std::min(kMaxW2dJobs, n_jobs - first);
     b.reset_status = first == 0 ? 1 : 0;
-    double total = 0.0;
-    for (int i = 0; i < b.n; ++i) total += (double)jobs[first + i].M * (double)jobs[first + i].N;
-    // amax CTAs in proportion to each matrix's size (at least one each), 4 per SM in total;
-    // quantization CTAs as for a single matrix
-    int a = 0, q = 0;
+    b.amax_grid = sms * 4;
+    // smallest matrices first: their amax is complete soonest, so their
+    // quantization starts while the amax pass reads the larger ones
+    int order[kMaxW2dJobs];
+    for (int i = 0; i < b.n; ++i) order[i] = first + i;
+    std::stable_sort(order, order + b.n, [&](int x, int y) { return jobs[x].M * jobs[x].N < jobs[y].M * jobs[y].N; });
+    int q = 0;
     for (int i = 0; i < b.n; ++i) {
-      const nvfp4_w2d_job& src = jobs[first + i];
+      const nvfp4_w2d_job& src = jobs[order[i]];
       W2dJob& j = b.job[i];
       j.w = src.w;
       j.M = src.M;
@@ -360,16 +360,12 @@ nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs
       j.codes = src.codes;
       j.scales = src.scales;
       j.tensor_scale = src.tensor_scale;
-      const double share = total > 0.0 ? (double)src.M * (double)src.N / total : 0.0;
-      j.amax_ctas = std::max(1, (int)(share * sms * 4));
-      j.amax_begin = a;
-      a += j.amax_ctas;
       j.quant_ctas = quant_grid(2 * (src.M / 16) * (src.N / 16), sms);  // two threads per tile
       j.quant_begin = q;
       q += j.quant_ctas;
     }
-    if (launch_w2d_batch(b, bf16, a, q, static_cast<float*>(workspace), dev_status,
-                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_w2d_batch_overlapped(b, bf16, q, static_cast<unsigned*>(workspace), dev_status,
+                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return NVFP4_ECUDA;
   }
   return NVFP4_OK;

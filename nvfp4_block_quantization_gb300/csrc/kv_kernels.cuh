@@ -13,6 +13,7 @@ constexpr int kStatsConsumers = 384;     // statistics consumer threads per CTA,
 constexpr int kStatsStages = 4;          // statistics ring stages
 constexpr int kStatsStageBytes = 24576;  // bytes per stage
 constexpr int NVFP4_DEV_NONFINITE_FLAG = 1;
+constexpr int NVFP4_DEV_TIMEOUT_FLAG = 2;
 
 // One tensor of a launch: the caller's pointers plus its workspace slices.
 struct KvJob {
@@ -87,9 +88,16 @@ struct W2dBatch {
   W2dJob job[kMaxW2dJobs];
   int n;
   int reset_status;  // 1: the launch starts *dev_status at 0 (first launch of a call)
+  int amax_grid;     // overlapped launch: CTAs of the amax grid (each covers a slice of every job)
 };
 cudaError_t launch_w2d_batch(const W2dBatch& b, bool bf16, int amax_ctas, int quant_ctas, float* amax_part,
                              int* dev_status, cudaStream_t s);
+// Overlapped launch pair: the amax grid takes the jobs one after another and
+// publishes each job's amax as soon as it is complete; the quantization grid
+// (a programmatic dependent) starts on a job as soon as its amax is.  ctr holds
+// 1 + 2 * kMaxW2dJobs words, zero before the launch and zero again after it.
+cudaError_t launch_w2d_batch_overlapped(const W2dBatch& b, bool bf16, int quant_ctas, unsigned* ctr, int* dev_status,
+                                        cudaStream_t s);
 cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8_t* codes, uint8_t* scales,
                              float* tensor_scale, int* dev_status, float* amax_part, int quant_ctas,
                              cudaStream_t s);

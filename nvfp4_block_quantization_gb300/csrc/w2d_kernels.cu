@@ -5,9 +5,14 @@
 // Each 16x16 tile gets one E4M3 scale chosen by Four-Over-Six; the tile's error
 // accumulates its 256 squared errors in row-major order.
 //
-//   w2d_amax   per-CTA absolute maximum (NaN-propagating) over the matrix.
-//   w2d_quant  one thread per tile: tile amax, both candidates' errors, the
-//              choice, then the chosen codes (the tile is re-read from L1/L2).
+//   w2d_amax       per-CTA absolute maximum (NaN-propagating) over each matrix.
+//   w2d_amax_seq   (batched calls) every CTA takes its slice of each matrix in
+//                  turn and publishes that matrix's amax once all CTAs have
+//                  folded theirs in, so quantization of the first matrices
+//                  overlaps the amax pass over the later ones.
+//   w2d_quant      two threads per tile: tile amax, both candidates' errors,
+//                  the choice, then the chosen codes.
+#include "bulk.cuh"
 #include "common.cuh"
 #include "kv_kernels.cuh"
 
@@ -38,20 +43,23 @@ __device__ __forceinline__ int w2d_job_of(const W2dBatch& b, int bx, bool quant)
   return j;
 }
 
-// Absolute maximum (NaN-propagating) of each matrix, per CTA: CTA c of job j
-// reads the contiguous range of 16-byte chunks [c n / k, (c + 1) n / k) of the
-// job's k CTAs with 8 loads in flight per thread; the partial goes to
-// amax_part[blockIdx.x] (a job's partials are contiguous).
+// NaN-propagating maximum over the block's threads; the result is valid in
+// thread 0.  `red` holds one value per warp.
+__device__ __forceinline__ float block_max_nan(float m, float* red) {
+  for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  return m;
+}
+
+// Absolute maximum (NaN-propagating) of the 16-byte chunks [a, b) of one matrix,
+// eight loads in flight per thread; the result is valid in thread 0.
 template <bool kBF16>
-__global__ void __launch_bounds__(256) w2d_amax_kernel(const __grid_constant__ W2dBatch bt, float* amax_part,
-                                                       int* dev_status) {
-  __shared__ float red[32];
-  if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status && bt.reset_status) *dev_status = 0;
-  const W2dJob& J = bt.job[w2d_job_of(bt, blockIdx.x, false)];
-  const int lc = blockIdx.x - J.amax_begin;
-  const uint4* p = static_cast<const uint4*>(J.w);
-  const int64_t nv = J.M * J.N / 16 * (kBF16 ? 2 : 4);  // 16-byte chunks
-  const int64_t a = (int64_t)lc * nv / J.amax_ctas, b = (int64_t)(lc + 1) * nv / J.amax_ctas;
+__device__ __forceinline__ float range_amax(const uint4* p, int64_t a, int64_t b, float* red) {
   constexpr int U = 8;
   uint32_t mw = 0u;  // bf16: max of |x| pairs
   float mf = 0.0f;   // fp32
@@ -71,14 +79,47 @@ __global__ void __launch_bounds__(256) w2d_amax_kernel(const __grid_constant__ W
       }
     }
   }
-  float m = kBF16 ? max_nan(bf16lo(mw), bf16hi(mw)) : mf;
-  for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-    for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (threadIdx.x == 0) amax_part[blockIdx.x] = m;
+  return block_max_nan(kBF16 ? max_nan(bf16lo(mw), bf16hi(mw)) : mf, red);
+}
+
+// Absolute maximum (NaN-propagating) of each matrix, per CTA: CTA c of job j
+// reads the contiguous range of 16-byte chunks [c n / k, (c + 1) n / k) of the
+// job's k CTAs with 8 loads in flight per thread; the partial goes to
+// amax_part[blockIdx.x] (a job's partials are contiguous).
+template <bool kBF16>
+__global__ void __launch_bounds__(256) w2d_amax_kernel(const __grid_constant__ W2dBatch bt, float* amax_part,
+                                                       int* dev_status) {
+  __shared__ float red[32];
+  if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status && bt.reset_status) *dev_status = 0;
+  const W2dJob& J = bt.job[w2d_job_of(bt, blockIdx.x, false)];
+  const int lc = blockIdx.x - J.amax_begin;
+  const int64_t nv = J.M * J.N / 16 * (kBF16 ? 2 : 4);  // 16-byte chunks
+  const int64_t a = (int64_t)lc * nv / J.amax_ctas, b = (int64_t)(lc + 1) * nv / J.amax_ctas;
+  const float m = range_amax<kBF16>(static_cast<const uint4*>(J.w), a, b, red);
+  if (threadIdx.x == 0) amax_part[blockIdx.x] = m;
+}
+
+// Batched amax, one matrix after another: CTA c of the grid folds the chunks
+// [c n / P, (c + 1) n / P) of each matrix into the matrix's amax word
+// (ctr[1 + 2 j], the bits of |x|: as unsigned integers they order like the
+// values, NaN above every number) and then counts itself on the matrix's ready
+// word (ctr[2 + 2 j], release).  The quantization grid may start at once.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) w2d_amax_seq_kernel(const __grid_constant__ W2dBatch bt, unsigned* ctr,
+                                                           int* dev_status) {
+  __shared__ float red[32];
+  if (blockIdx.x == 0 && threadIdx.x == 0 && dev_status && bt.reset_status) *dev_status = 0;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int j = 0; j < bt.n; ++j) {
+    const W2dJob& J = bt.job[j];
+    const int64_t nv = J.M * J.N / 16 * (kBF16 ? 2 : 4);  // 16-byte chunks
+    const int64_t a = (int64_t)blockIdx.x * nv / gridDim.x, b = (int64_t)(blockIdx.x + 1) * nv / gridDim.x;
+    const float m = range_amax<kBF16>(static_cast<const uint4*>(J.w), a, b, red);
+    if (threadIdx.x == 0) {
+      atomicMax(ctr + 1 + 2 * j, __float_as_uint(m) & 0x7fffffffu);
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr + 2 + 2 * j) : "memory");
+    }
+    __syncthreads();  // red is reused by the next matrix
   }
 }
 
@@ -90,26 +131,42 @@ __global__ void __launch_bounds__(256) w2d_amax_kernel(const __grid_constant__ W
 // element in row-major order.  The pair then compares errors (lower wins, ties
 // to 6) and the winner stores its codes and the scale byte.  A warp covers 16
 // adjacent tiles: 512 contiguous bytes of every tile row.
-template <bool kBF16>
+// kSeq (overlapped batched launch): thread 0 waits (bounded) until the job's
+// ready word counts every amax CTA, and the amax is the job's amax word; once
+// every CTA has read what it needs, the last of them returns ctr to zero.
+template <bool kBF16, bool kSeq>
 __global__ void __launch_bounds__(256) w2d_quant_kernel(const __grid_constant__ W2dBatch bt, const float* amax_part,
-                                                        int* dev_status) {
+                                                        unsigned* ctr, int* dev_status) {
   __shared__ QuantTable tab;
   __shared__ float red[32];
-  const W2dJob& J = bt.job[w2d_job_of(bt, blockIdx.x, true)];
+  const int jb = w2d_job_of(bt, blockIdx.x, true);
+  const W2dJob& J = bt.job[jb];
   const void* w = J.w;
   const int64_t M = J.M, N = J.N;
   uint8_t* codes = J.codes;
   uint8_t* scales = J.scales;
   const int lq = blockIdx.x - J.quant_begin;  // this CTA within the job's CTAs
-  float m = 0.0f;
-  for (int i = threadIdx.x; i < J.amax_ctas; i += blockDim.x) m = max_nan(m, amax_part[J.amax_begin + i]);
-  for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (threadIdx.x == 0) red[0] = v;
+  if (kSeq) {
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = bulk_timer_ns();
+      bool ok = true;
+      for (unsigned it = 0; ld_acquire_u32(ctr + 2 + 2 * jb) < (unsigned)bt.amax_grid; ++it) {
+        if (bulk_timer_ns() - t0 > kBulkWaitNs) {
+          ok = false;
+          if (dev_status) atomicOr(dev_status, NVFP4_DEV_TIMEOUT_FLAG);
+          break;
+        }
+        __nanosleep(it < 8 ? 128 : 512);
+      }
+      red[0] = ok ? __uint_as_float(*reinterpret_cast<volatile const unsigned*>(ctr + 1 + 2 * jb))
+                  : __int_as_float(0x7fc00000);
+    }
+  } else {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < J.amax_ctas; i += blockDim.x) m = max_nan(m, amax_part[J.amax_begin + i]);
+    m = block_max_nan(m, red);
+    __syncthreads();
+    if (threadIdx.x == 0) red[0] = m;
   }
   __syncthreads();
   const float amax = red[0];
@@ -122,6 +179,17 @@ __global__ void __launch_bounds__(256) w2d_quant_kernel(const __grid_constant__ 
   if (lq == 0 && threadIdx.x == 0) {
     *J.tensor_scale = g;
     if (nonfinite && dev_status) atomicOr(dev_status, NVFP4_DEV_NONFINITE_FLAG);
+  }
+  if (kSeq && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ctr, 1u) + 1u == gridDim.x) {  // every CTA has read its amax word
+      __threadfence();
+      for (int j = 0; j < bt.n; ++j) {
+        ctr[1 + 2 * j] = 0u;
+        ctr[2 + 2 * j] = 0u;
+      }
+      ctr[0] = 0u;
+    }
   }
 
   const unsigned pair_mask = 3u << (threadIdx.x & 30);
@@ -256,9 +324,30 @@ cudaError_t launch_w2d_batch(const W2dBatch& b, bool bf16, int amax_ctas, int qu
   else w2d_amax_kernel<false><<<amax_ctas, 256, 0, s>>>(b, amax_part, dev_status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (bf16) w2d_quant_kernel<true><<<quant_ctas, 256, 0, s>>>(b, amax_part, dev_status);
-  else w2d_quant_kernel<false><<<quant_ctas, 256, 0, s>>>(b, amax_part, dev_status);
+  if (bf16) w2d_quant_kernel<true, false><<<quant_ctas, 256, 0, s>>>(b, amax_part, nullptr, dev_status);
+  else w2d_quant_kernel<false, false><<<quant_ctas, 256, 0, s>>>(b, amax_part, nullptr, dev_status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_w2d_batch_overlapped(const W2dBatch& b, bool bf16, int quant_ctas, unsigned* ctr, int* dev_status,
+                                        cudaStream_t s) {
+  if (bf16) w2d_amax_seq_kernel<true><<<b.amax_grid, 256, 0, s>>>(b, ctr, dev_status);
+  else w2d_amax_seq_kernel<false><<<b.amax_grid, 256, 0, s>>>(b, ctr, dev_status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(quant_ctas);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start beside the amax grid
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* no_part = nullptr;
+  if (bf16) return cudaLaunchKernelEx(&cfg, w2d_quant_kernel<true, true>, b, no_part, ctr, dev_status);
+  return cudaLaunchKernelEx(&cfg, w2d_quant_kernel<false, true>, b, no_part, ctr, dev_status);
 }
 
 cudaError_t launch_w2d_quant(const void* w, bool bf16, const W2dGeom& geo, uint8_t* codes, uint8_t* scales,

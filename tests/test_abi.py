@@ -136,6 +136,9 @@ def test_weight_batched_argument_errors(lib):
     assert b(jobs((g, 32, 32, P(4097), g, g)), 1, 0, None, g, 1 << 20, None) == L.NVFP4_EALIGN
     assert b(jobs(ok), 1, 0, P(4098), g, 1 << 20, None) == L.NVFP4_EALIGN
     assert L.nvfp4_w2d_batched_workspace_bytes(0) == 0
+    assert L.nvfp4_w2d_batched_workspace_bytes(1) == L.nvfp4_w2d_batched_workspace_bytes(64) > 0
+    assert b(jobs(ok), 1, 0, None, g, 16, None) == L.NVFP4_EWORKSPACE
+    assert b(jobs(ok), 1, 0, None, P(4096 + 128), 1 << 20, None) == L.NVFP4_EWORKSPACE
 
 
 def test_product_path_never_imports_the_oracle():

@@ -349,11 +349,18 @@ def test_weight_2d_batched_many_and_nonfinite(nv):
         assert int(s.status.item()) == 0
         assert torch.equal(o.codes, s.codes) and torch.equal(o.scales, s.scales)
         assert torch.equal(o.tensor_scale.view(torch.int32), s.tensor_scale.view(torch.int32))
-    # a clean batch after the NaN one on the same workspace and status word reports no error
+    # clean batches after the NaN one, twice on one workspace and the same status word: no
+    # error, and the same bits (the workspace returns to zero after every call)
     ws2 = ws[1:]
-    outs2, status2 = nv.weight_quant_2d_batched(ws2, status=status)
-    torch.cuda.synchronize()
-    assert int(status2.item()) == 0
+    wsp = nv.w2d_batched_workspace(len(ws2))
+    for _ in range(2):
+        outs2, status2 = nv.weight_quant_2d_batched(ws2, workspace=wsp, status=status)
+        torch.cuda.synchronize()
+        assert int(status2.item()) == 0
+        for o2, o in zip(outs2, outs[1:]):
+            assert torch.equal(o2.codes, o.codes) and torch.equal(o2.scales, o.scales)
+            assert torch.equal(o2.tensor_scale.view(torch.int32), o.tensor_scale.view(torch.int32))
+    assert not bool(wsp.any())
 
 
 def test_activations_1d_bit_exact(nv, oracle):

@@ -41,11 +41,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of each kernel on this step's workload, from one ncu
 # capture of this script (profiles/kv_chunk_7040x24x128_launch_list.md); drop an entry when its
 # kernel changes.
-NCU_TRAFFIC = {"kv_stats": 114416998, "kv_quant": 20503629}
+NCU_TRAFFIC = {"kv_stats": 114594892, "kv_quant": 20179993}
 # ALU-pipe warp instructions per launch of the quantization kernel on this step (same capture,
 # sm__inst_executed_pipe_alu.sum); the pass is bound by instruction issue (half of it on the
 # half-rate ALU pipe), not by HBM.
-NCU_ALU_INST = {"kv_quant": 8.524e6}
+NCU_ALU_INST = {"kv_quant": 7.524e6}
 ALU_PEAK_PER_SM_CLK = 2.0  # warp instructions: one per SM sub-partition every 2 cycles
 
 

@@ -159,27 +159,35 @@ __device__ __forceinline__ void fold_row(const uint4 v0, const uint4 v1, Acc8& a
   }
 }
 
-// Folds this thread's rows of one landed stage (`rows` valid rows of slab_bytes each).
+// 16-byte shared-memory load at a 32-bit shared address.
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+// Folds this thread's rows of one landed stage (`rows` valid rows of slab_bytes
+// each, starting at shared address stage_s).
 template <bool kBF16, bool kSmooth>
-__device__ __forceinline__ void fold_stage(const uint8_t* stage, int slab_bytes, int rows, int rl, int rpp,
-                                           int chunk, Acc8& a) {
+__device__ __forceinline__ void fold_stage(uint32_t stage_s, int slab_bytes, int rows, int rl, int rpp, int chunk,
+                                           Acc8& a) {
   constexpr int es = kBF16 ? 2 : 4;
-  const uint8_t* p = stage + (size_t)rl * slab_bytes + 8 * chunk * es;
-  const size_t step = (size_t)rpp * slab_bytes;
+  uint32_t p = stage_s + (uint32_t)(rl * slab_bytes + 8 * chunk * es);
+  const uint32_t step = (uint32_t)(rpp * slab_bytes);
   int j = rl;
   for (; j + 3 * rpp < rows; j += 4 * rpp, p += 4 * step) {  // four rows at a time
     uint4 v[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      v[i][0] = *reinterpret_cast<const uint4*>(p + i * step);
-      v[i][1] = kBF16 ? v[i][0] : *reinterpret_cast<const uint4*>(p + i * step + 16);
+      v[i][0] = lds_v4(p + i * step);
+      v[i][1] = kBF16 ? v[i][0] : lds_v4(p + i * step + 16);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) fold_row<kBF16, kSmooth>(v[i][0], v[i][1], a);
   }
   for (; j < rows; j += rpp, p += step) {
-    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
-    const uint4 v1 = kBF16 ? v0 : *reinterpret_cast<const uint4*>(p + 16);
+    const uint4 v0 = lds_v4(p);
+    const uint4 v1 = kBF16 ? v0 : lds_v4(p + 16);
     fold_row<kBF16, kSmooth>(v0, v1, a);
   }
 }
@@ -314,14 +322,15 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         const bool on = lane_on && ch < G.C;
         Acc8 a;
         acc_reset(a);
-        for (int64_t row = r0; row < r1; row += G.rows_per_stage, ++f) {
-          const int rows = (int)min((int64_t)G.rows_per_stage, r1 - row);
+        const int nrows = (int)(r1 - r0);
+        for (int row = 0; row < nrows; row += G.rows_per_stage, ++f) {
+          const int rows = min(G.rows_per_stage, nrows - row);
           const int st = f % kStatsStages;
           if (!sm.abort && !mbar_wait(&sm.full[st], (unsigned)(f / kStatsStages) & 1u)) {
             sm.abort = 1;
             atomicOr(G.header + 1, kStatusTimeout);
           }
-          const uint8_t* stage = ring + (size_t)st * kStatsStageBytes;
+          const uint32_t stage = smem_u32(ring) + (uint32_t)(st * kStatsStageBytes);
           if (on) {
             if (smooth) fold_stage<kBF16, true>(stage, sb, rows, rl, G.rpp, chunk, a);
             else fold_stage<kBF16, false>(stage, sb, rows, rl, G.rpp, chunk, a);

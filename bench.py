@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of each kernel on this step's workload, from one ncu
 # capture of this script (profiles/kv_chunk_7040x24x128_launch_list.md); drop an entry when its
 # kernel changes.
-NCU_TRAFFIC = {"kv_stats": 114594892, "kv_quant": 20179993}
+NCU_TRAFFIC = {"kv_stats": 114290918, "kv_quant": 20523417}
 # ALU-pipe warp instructions per launch of the quantization kernel on this step (same capture,
 # sm__inst_executed_pipe_alu.sum); the pass is bound by instruction issue (half of it on the
 # half-rate ALU pipe), not by HBM.

@@ -523,30 +523,36 @@ def row_kv_write_30_layers(nv, W, torch, dev, peak):
 
 def row_kv_cache_read_dequant(nv, W, torch, dev, peak):
     """Cache read: 21 frames (3 global-sink frames of chunk 0 + the 18 most recent frames of
-    chunks 0..2) x 880 tokens, quantized by this library from seeded chunks (four caches: K and
-    V of two layers); per-frame groups carry each frame's chunk tensor scale and mean."""
+    chunks 0..2) x 880 tokens, quantized by this library from seeded chunks; four caches, K and V
+    of two layers.  K's per-frame groups carry each frame's chunk tensor scale and mean (re-added
+    on the way out), V's only the tensor scale."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000)
     Tc, F = 21 * 880, 880
     frame_src = [(0, f) for f in range(3)] + [(0, 6), (0, 7)] + [(1, f) for f in range(8)] + [(2, f) for f in range(8)]
     caches = []
     for t in range(4):
+        is_k = t % 2 == 0
         chunk_q = []
         for c in range(3):
-            x = _chunk_k_device(torch, gen, dev)
-            chunk_q.append(nv.kv_smooth_quant(x, True))
+            x = _chunk_k_device(torch, gen, dev) if is_k else \
+                torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev).to(torch.bfloat16)
+            chunk_q.append(nv.kv_smooth_quant(x, is_k))
             del x
         codes = torch.cat([chunk_q[c].codes[f * F:(f + 1) * F] for c, f in frame_src])
         scales = torch.cat([chunk_q[c].scales[f * F:(f + 1) * F] for c, f in frame_src])
         gs = torch.cat([chunk_q[c].tensor_scale for c, f in frame_src])
-        means = torch.stack([chunk_q[c].mean for c, f in frame_src])
+        means = torch.stack([chunk_q[c].mean for c, f in frame_src]) if is_k else None
         out = torch.empty((Tc, HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev)
         caches.append((codes, scales, gs, means, out))
         del chunk_q
     ms = _time_graph(torch, lambda i: nv.kv_dequant(*caches[i % 4][:3], mean=caches[i % 4][3],
                                                     tokens_per_group=F, out=caches[i % 4][4]), 8, 20)
+    ms_k = _time_graph(torch, lambda i: nv.kv_dequant(*caches[2 * (i % 2)][:3], mean=caches[2 * (i % 2)][3],
+                                                      tokens_per_group=F, out=caches[2 * (i % 2)][4]), 8, 20)
     b = Tc * HEADS * HEAD_DIM * DEQUANT_BYTES_PER_ELEM
-    return {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "bytes": b, "frac": b / ms / 1e6 / peak}
+    return {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "ms_per_k_tensor": ms_k, "bytes": b,
+            "frac": b / ms / 1e6 / peak}
 
 
 def row_weight_quant_2d(nv, W, torch, dev, peak):

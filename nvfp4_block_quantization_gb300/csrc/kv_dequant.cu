@@ -87,10 +87,18 @@ __global__ void __launch_bounds__(256) kv_dequant_kernel(const uint8_t* __restri
         const int64_t grp = row / tpg;
         gend = (grp + 1) * tpg;
         g = __ldg(tensor_scale + grp);
-        if (kMean) {  // scalar loads: the mean pointer need only be 4-byte aligned
+        if (kMean) {  // four 16-byte loads when aligned (the API requires only 4 bytes)
           const float* m = mean + (size_t)grp * C + (size_t)cb * 16;
+          if ((reinterpret_cast<uintptr_t>(m) & 15) == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) mu[i] = __ldg(m + i);
+            for (int i = 0; i < 4; ++i) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(m) + i);
+              mu[4 * i] = v.x; mu[4 * i + 1] = v.y; mu[4 * i + 2] = v.z; mu[4 * i + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mu[i] = __ldg(m + i);
+          }
         }
       }
       const float S = __fmul_rn(e4m3_value(sc[u]), g);

@@ -256,6 +256,14 @@ def test_dequant_groups_bit_exact(nv, oracle):
         gd = nv.kv_dequant(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), torch.from_numpy(g).cuda(),
                            mean=None if m is None else torch.from_numpy(m).cuda(), tokens_per_group=tpg)
         assert np.array_equal(bf16_bits(gd), rd)
+    # a mean array that is only 4-byte aligned (the kernel's scalar-load path)
+    buf = torch.zeros(mean.size + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = torch.from_numpy(mean.ravel()).cuda()
+    m4 = buf[1:].view(mean.shape)
+    assert m4.data_ptr() % 16 != 0
+    gd = nv.kv_dequant(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), torch.from_numpy(g).cuda(),
+                       mean=m4, tokens_per_group=tpg)
+    assert np.array_equal(bf16_bits(gd), oracle.kv_dequant(codes, scales, g, mean=mean, tokens_per_group=tpg))
 
 
 def test_dequant_nan_filler(nv, oracle):

@@ -195,7 +195,7 @@ size_t nvfp4_w2d_workspace_bytes(int64_t M, int64_t N);
  *   codes        device [M][N/2], same nibble packing as the KV codes
  *   scales       device [M/16][N/16] E4M3 bytes
  *   tensor_scale device [1]
- * Errors as nvfp4_kv_smooth_quant. */
+ * Errors as nvfp4_kv_smooth_quant (NVFP4_ESHAPE also for M * N > 2^46). */
 nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, int64_t N, uint8_t* codes,
                                    uint8_t* scales, float* tensor_scale, int* dev_status, void* workspace,
                                    size_t workspace_bytes, void* stream);

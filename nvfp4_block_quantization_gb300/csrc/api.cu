@@ -228,6 +228,7 @@ nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const
 
 size_t nvfp4_w2d_workspace_bytes(int64_t M, int64_t N) {
   if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return 0;
+  if (M > 0 && N > ((int64_t)1 << 46) / M) return 0;
   const int sms = device_sms();
   if (sms <= 0) return 0;
   return align_up((size_t)sms * 4 * sizeof(float), kWsAlign);
@@ -269,7 +270,7 @@ nvfp4_status nvfp4_weight_quant_2d_static(const void* w, nvfp4_in_dtype dt, int6
                                           uint8_t* scales, float* tensor_scale, int* dev_status, void* stream) {
   if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
   if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return NVFP4_ESHAPE;
-  if (M > 0 && N > ((int64_t)1 << 60) / M) return NVFP4_ESHAPE;
+  if (M > 0 && N > ((int64_t)1 << 46) / M) return NVFP4_ESHAPE;  // (chunk index) * (CTAs) fits in int64
   if (!tensor_scale) return NVFP4_EINVAL;
   if (M > 0 && (!w || !codes || !scales)) return NVFP4_EINVAL;
   if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVFP4_EALIGN;
@@ -295,7 +296,7 @@ nvfp4_status nvfp4_weight_quant_2d(const void* w, nvfp4_in_dtype dt, int64_t M, 
                                    size_t workspace_bytes, void* stream) {
   if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
   if (M < 0 || N < 16 || (M % 16) != 0 || (N % 16) != 0) return NVFP4_ESHAPE;
-  if (M > 0 && N > ((int64_t)1 << 60) / M) return NVFP4_ESHAPE;
+  if (M > 0 && N > ((int64_t)1 << 46) / M) return NVFP4_ESHAPE;  // (chunk index) * (CTAs) fits in int64
   if (!tensor_scale) return NVFP4_EINVAL;
   if (M > 0 && (!w || !codes || !scales)) return NVFP4_EINVAL;
   if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVFP4_EALIGN;
@@ -327,7 +328,7 @@ nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs
   for (int i = 0; i < n_jobs; ++i) {
     const nvfp4_w2d_job& j = jobs[i];
     if (j.M < 0 || j.N < 16 || (j.M % 16) != 0 || (j.N % 16) != 0) return NVFP4_ESHAPE;
-    if (j.M > 0 && j.N > ((int64_t)1 << 60) / j.M) return NVFP4_ESHAPE;
+    if (j.M > 0 && j.N > ((int64_t)1 << 46) / j.M) return NVFP4_ESHAPE;
     if (!j.tensor_scale) return NVFP4_EINVAL;
     if (j.M > 0 && (!j.w || !j.codes || !j.scales)) return NVFP4_EINVAL;
     if (!aligned(j.w, 16) || !aligned(j.codes, 16) || !aligned(j.scales, 16)) return NVFP4_EALIGN;

@@ -107,6 +107,7 @@ def test_weight_argument_errors(lib):
     w = L.nvfp4_weight_quant_2d
     assert w(g, 0, 20, 32, g, g, g, None, g, 1 << 20, None) == L.NVFP4_ESHAPE
     assert w(g, 0, 32, 8, g, g, g, None, g, 1 << 20, None) == L.NVFP4_ESHAPE
+    assert w(g, 0, 1 << 24, 1 << 24, g, g, g, None, g, 1 << 20, None) == L.NVFP4_ESHAPE  # M * N > 2^46
     assert w(g, 3, 32, 32, g, g, g, None, g, 1 << 20, None) == L.NVFP4_EINVAL
     assert w(None, 0, 32, 32, g, g, g, None, g, 1 << 20, None) == L.NVFP4_EINVAL
     assert w(g, 0, 32, 32, P(4097), g, g, None, g, 1 << 20, None) == L.NVFP4_EALIGN

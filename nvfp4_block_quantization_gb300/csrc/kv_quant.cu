@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
         atomicOr(G.header + 1, kStatusTimeout);
         break;
       }
-      __nanosleep(it < 8 ? 128 : 512);
+      __nanosleep(64);
     }
     qc.ok = ok;
   }

@@ -339,6 +339,15 @@ def test_weight_2d_batched_bit_exact(nv, oracle, dtype):
         assert np.array_equal(host(o.codes), ref["codes"])
 
 
+def test_weight_2d_batched_all_empty(nv):
+    """A batch of empty matrices writes tensor scale 0 and status 0."""
+    ws = [torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), torch.empty((0, 32), dtype=torch.bfloat16, device="cuda")]
+    outs, status = nv.weight_quant_2d_batched(ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert all(float(o.tensor_scale.item()) == 0.0 for o in outs)
+
+
 def test_weight_2d_batched_many_and_nonfinite(nv):
     """70 matrices (two launch pairs of at most 64) equal the single calls; a NaN in the first sets the shared status."""
     from nvfp4_block_quantization_gb300 import workloads as W

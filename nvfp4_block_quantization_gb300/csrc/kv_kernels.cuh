@@ -34,9 +34,10 @@ struct KvBatch {
   int n;
 };
 
-// Statistics partition: CTA c of P owns rows [c T / P, (c + 1) T / P), streamed
-// in stages of rows_per_stage rows (a multiple of rpp); its tpr * rpp consumer
-// threads each own an 8-channel chunk (tpr per row) of every rpp-th row.
+// Statistics partition: the rows are cut into stages of rows_per_stage rows (a
+// multiple of rpp) and CTA c of P takes stages c, c + P, c + 2 P, ...; its
+// tpr * rpp consumer threads each own an 8-channel chunk (tpr per row) of every
+// rpp-th row.
 struct KvGeom {
   int64_t T;
   int C;    // H * D

@@ -8,13 +8,14 @@
 // the absolute maximum of the smoothed tensor.  V is not smoothed; its amax is
 // that of the raw values.
 //
-// Work split.  The grid is cooperative, one CTA per SM.  CTA c owns the rows
-// [c T / P, (c + 1) T / P) of every job -- one contiguous byte range per job,
-// the access pattern HBM serves fastest.  A producer thread streams it into a
-// shared-memory ring with 1-D bulk copies (cp.async.bulk), stage by stage of R
-// rows; consumer thread t owns the 8-channel chunk t % tpr of every rpp-th row
-// of a stage from t / tpr (a slab of 8 tpr channels; wider tensors take several
-// slabs, and then each row of a stage is its own copy) and keeps, per channel,
+// Work split.  The grid is cooperative, one CTA per SM.  The rows of every job
+// are cut into stages of R rows and CTA c takes stages c, c + P, c + 2 P, ...
+// (neighbouring CTAs read neighbouring stages at the same time).  A producer
+// thread streams them into a shared-memory ring with 1-D bulk copies
+// (cp.async.bulk), stage by stage; consumer thread t owns the 8-channel chunk
+// t % tpr of every rpp-th row of a stage from t / tpr (a slab of 8 tpr
+// channels; wider tensors take several slabs, and then each row of a stage is
+// its own copy) and keeps, per channel,
 // (sum, low part) by TwoSum -- so its partial sum is exact -- plus min and max
 // (unsmoothed tensors: the absolute maximum only).
 //
@@ -259,7 +260,6 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
   StatsSmem& sm = *reinterpret_cast<StatsSmem*>(ring + (size_t)kStatsStages * kStatsStageBytes);
   constexpr int es = kBF16 ? 2 : 4;
   const int c = blockIdx.x;
-  const int64_t r0 = (int64_t)c * G.T / G.P, r1 = (int64_t)(c + 1) * G.T / G.P;
   const size_t rs = (size_t)G.C * es;                 // row stride in bytes
   const int slab_ch = 8 * G.tpr;                      // channels per slab
   const int nslab = (G.C + slab_ch - 1) / slab_ch;
@@ -285,8 +285,8 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         const uint8_t* x = static_cast<const uint8_t*>(b.job[job].x);
         for (int sl = 0; sl < nslab; ++sl) {
           const int s0 = sl * slab_ch, sb = min(slab_ch, G.C - s0) * es;  // slab bytes of this slab
-          for (int64_t row = r0; row < r1; row += G.rows_per_stage, ++f) {
-            const int rows = (int)min((int64_t)G.rows_per_stage, r1 - row);
+          for (int64_t row = (int64_t)c * G.rows_per_stage; row < G.T; row += (int64_t)G.P * G.rows_per_stage, ++f) {
+            const int rows = (int)min((int64_t)G.rows_per_stage, G.T - row);
             const int st = f % kStatsStages;
             if (f >= kStatsStages && !sm.abort &&
                 !mbar_wait(&sm.empty[st], (unsigned)(f / kStatsStages - 1) & 1u)) {
@@ -322,9 +322,8 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         const bool on = lane_on && ch < G.C;
         Acc8 a;
         acc_reset(a);
-        const int nrows = (int)(r1 - r0);
-        for (int row = 0; row < nrows; row += G.rows_per_stage, ++f) {
-          const int rows = min(G.rows_per_stage, nrows - row);
+        for (int64_t row = (int64_t)c * G.rows_per_stage; row < G.T; row += (int64_t)G.P * G.rows_per_stage, ++f) {
+          const int rows = (int)min((int64_t)G.rows_per_stage, G.T - row);
           const int st = f % kStatsStages;
           if (!sm.abort && !mbar_wait(&sm.full[st], (unsigned)(f / kStatsStages) & 1u)) {
             sm.abort = 1;

@@ -555,6 +555,45 @@ def row_kv_cache_read_dequant(nv, W, torch, dev, peak):
             "frac": b / ms / 1e6 / peak}
 
 
+def row_kv_cache_view_gather(nv, W, torch, dev, peak):
+    """Cache read through the multi-shot cache manager: five 8-frame chunks written straight into
+    pool slots, then the next chunk's view (3 global-sink frames + the 18 most recent frames = 21
+    frames x 880 tokens) expanded by the gathered read from its slots; K (mean re-added) and V of
+    two layers, four pools in rotation."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3100)
+    F, Lf = 8, 880
+    pools, views = [], []
+    for layer in range(2):
+        cache = nv.KvCache(F, Lf, 3, 3, 18)
+        pk = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=True, device=dev)
+        pv = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=False, device=dev)
+        for c in range(5):
+            slot = cache.append()
+            k = _chunk_k_device(torch, gen, dev)
+            v = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev).to(torch.bfloat16)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            nv.kv_smooth_quant_batched([k, v], [True, False],
+                                       outs=[pk.slot_outputs(cache, slot, st), pv.slot_outputs(cache, slot, st)],
+                                       status=st)
+            del k, v
+        fi, fr, fs = cache.view()
+        assert len(fi) == 21
+        for pool, is_k in ((pk, True), (pv, False)):
+            out = torch.empty((len(fi) * Lf, HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+            pools.append((pool, fr, fs, is_k, out))
+    torch.cuda.synchronize()
+
+    def call(i):
+        pool, fr, fs, is_k, out = pools[i % 4]
+        nv.kv_gather_dequant(pool, fr, fs, Lf, with_mean=is_k, out=out)
+
+    ms = _time_graph(torch, call, 8, 20)
+    b = 21 * Lf * HEADS * HEAD_DIM * DEQUANT_BYTES_PER_ELEM
+    return {"GB/s": b / ms / 1e6, "ms_per_tensor": ms, "bytes": b, "frac": b / ms / 1e6 / peak,
+            "view_frames": 21, "slots_per_pool": 5}
+
+
 def row_weight_quant_2d(nv, W, torch, dev, peak):
     """Weights: 4 x 3072x3072 and 2 x 3072x14336 bf16, N(0, 0.02^2), 16x16 tiles, in one batched call
     (and, for comparison, as six single calls)."""
@@ -601,6 +640,7 @@ def row_k_only_smooth_quant(nv, W, torch, dev, peak):
 
 
 ROWS = {"kv_write_30_layers": row_kv_write_30_layers, "kv_cache_read_dequant": row_kv_cache_read_dequant,
+        "kv_cache_view_gather": row_kv_cache_view_gather,
         "weight_quant_2d": row_weight_quant_2d, "activation_quant_1d": row_activation_quant_1d,
         "k_only_smooth_quant": row_k_only_smooth_quant}
 

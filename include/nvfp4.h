@@ -65,7 +65,8 @@ typedef enum nvfp4_status {
   NVFP4_ESHAPE = 2,     /* a size is out of range (D % 16, H <= 0, T < 0, M/N % 16, ...) */
   NVFP4_EALIGN = 3,     /* a pointer is not aligned as required */
   NVFP4_EWORKSPACE = 4, /* workspace NULL, too small, or not 256-byte aligned */
-  NVFP4_ECUDA = 5       /* a CUDA runtime call or kernel launch failed */
+  NVFP4_ECUDA = 5,      /* a CUDA runtime call or kernel launch failed */
+  NVFP4_ECAPACITY = 6   /* the KV-cache pool has no free chunk slot */
 } nvfp4_status;
 
 typedef enum nvfp4_in_dtype {
@@ -180,6 +181,94 @@ nvfp4_status nvfp4_kv_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_
 nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
                               const float* mean, int64_t tokens_per_group, int64_t T, int H, int D,
                               void* out_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Multi-shot NVFP4 KV cache (LongLive-2.0 summary page, inference step 9:  */
+/* attention over a Global Sink, the first S_g frames of the video, plus a  */
+/* Shot-Level Sink, the first S_s frames of the current shot, held as       */
+/* START/LEN pointers into frames already cached; a prompt switch rebinds   */
+/* the shot sink.  Step 7: the cache is written one chunk of F_c frames at  */
+/* a time).                                                                 */
+/* ------------------------------------------------------------------------ */
+/* The local part of the attention is read as a rolling window of the W
+ * frames right before the chunk being generated.  The view of chunk n (first
+ * frame cur = n * F_c) is the union, in ascending frame order and without
+ * repeats, of [0, S_g), [START, START + S_s) and [cur - W, cur), each clipped
+ * to the cached frames [0, cur).
+ *
+ * Storage, per cached tensor (each layer's K, each layer's V), is a pool of
+ * chunk slots that the caller allocates on the device:
+ *   codes   [n_slots * F_c * L_f][H][D/2]    scales [n_slots * F_c * L_f][H][D/16]
+ *   g       [n_slots] fp32                   mean   [n_slots][H][D] fp32 (K only)
+ * Slot s holds one chunk; its frame i is pool rows [(s F_c + i) L_f, (s F_c + i + 1) L_f).
+ * The quantizer writes a chunk straight into its slot: x of F_c * L_f tokens,
+ * codes and scales at pool row s * F_c * L_f, tensor_scale = g + s,
+ * mean_out = mean + s * H * D.  Nothing is copied.
+ *
+ * The manager is host bookkeeping in a caller-owned struct: it makes no CUDA
+ * call and touches no device memory.  Release rule: when chunk n is written,
+ * a slot is freed if none of its chunk's frames can be in the view of chunk
+ * n + 1 or a later one (windows only move forward; a new shot sink covers only
+ * frames not yet written).  So a view stays valid until the next append. */
+#define NVFP4_KVCACHE_MAX_SLOTS 64
+typedef struct nvfp4_kvcache {
+  int frames_per_chunk;     /* F_c */
+  int global_sink;          /* S_g frames */
+  int shot_sink;            /* S_s frames */
+  int window;               /* W frames */
+  int n_slots;              /* chunk slots in the pool, <= NVFP4_KVCACHE_MAX_SLOTS */
+  int64_t tokens_per_frame; /* L_f */
+  int64_t n_chunks;         /* chunks written so far; the next one is chunk n_chunks */
+  int64_t shot_start;       /* START: first frame of the current shot */
+  int64_t slot_chunk[NVFP4_KVCACHE_MAX_SLOTS]; /* chunk held by each slot, -1 = free */
+} nvfp4_kvcache;
+
+/* Chunk slots that always suffice: ceil(S_g/F_c) + ceil(S_s/F_c) +
+ * max(1, ceil(W/F_c)); -1 for invalid sizes or more than the maximum. */
+int nvfp4_kvcache_slots_needed(int frames_per_chunk, int global_sink, int shot_sink, int window);
+
+/* An empty cache (one shot starting at frame 0).  NVFP4_ESHAPE for sizes out
+ * of range (F_c < 1, L_f < 1, negative sinks or window, n_slots outside
+ * [1, NVFP4_KVCACHE_MAX_SLOTS]); NVFP4_EINVAL for a NULL struct. */
+nvfp4_status nvfp4_kvcache_init(nvfp4_kvcache* c, int frames_per_chunk, int64_t tokens_per_frame, int global_sink,
+                                int shot_sink, int window, int n_slots);
+
+/* Chunk n_chunks is about to be written: frees the slots the release rule
+ * allows, stores the new chunk in the lowest free slot (*slot) and counts it.
+ * NVFP4_ECAPACITY (nothing changed but the releases) when every slot is live. */
+nvfp4_status nvfp4_kvcache_append(nvfp4_kvcache* c, int* slot);
+
+/* Prompt switch: the next chunk is the first of a new shot (START = its first
+ * frame); the old shot's sink frames become releasable. */
+nvfp4_status nvfp4_kvcache_new_shot(nvfp4_kvcache* c);
+
+/* The view of chunk n_chunks: per frame, in order, its video frame index, its
+ * first pool row and its slot (each output array optional, host memory).
+ * Returns the frame count (at most S_g + S_s + W), or -1 when max_frames is
+ * too small (nothing written) or the struct is inconsistent. */
+int nvfp4_kvcache_view(const nvfp4_kvcache* c, int64_t* frame_index, int64_t* frame_row, int* frame_slot,
+                       int max_frames);
+
+/* Frames one gathered read can take (its frame table is a kernel parameter). */
+#define NVFP4_MAX_VIEW_FRAMES 512
+
+/* Gathered cache read: expands n_frames view frames of tokens_per_frame (L_f)
+ * tokens each from a chunk-slot pool into out_bf16 [n_frames * L_f][H][D],
+ * frame i's tokens from pool rows [frame_row[i], frame_row[i] + L_f) with the
+ * tensor scale g_pool[frame_meta[i]] and, when mean_pool is set, the mean
+ * mean_pool[frame_meta[i]][H][D] added back: bf16_rne(fl(fl(Q * fl(E * g)) + mean))
+ * per element, as nvfp4_kv_dequant.
+ *   codes_pool, scales_pool  device, pool_rows rows (layouts above)
+ *   g_pool, mean_pool        device, n_meta entries (mean_pool may be NULL)
+ *   frame_row, frame_meta    HOST arrays of n_frames entries (the view of
+ *                            nvfp4_kvcache_view: frame_meta = frame_slot)
+ * Every frame must lie inside the pool and every frame_meta inside [0, n_meta):
+ * NVFP4_ESHAPE otherwise, checked before anything is enqueued.  n_frames = 0
+ * enqueues nothing.  Alignment and other errors as nvfp4_kv_dequant. */
+nvfp4_status nvfp4_kv_gather_dequant(const uint8_t* codes_pool, const uint8_t* scales_pool, const float* g_pool,
+                                     const float* mean_pool, int64_t pool_rows, int n_meta, const int64_t* frame_row,
+                                     const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
+                                     void* out_bf16, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Weights with 16x16 2-D blocks (LongLive-2.0 summary page, training        */

@@ -21,7 +21,7 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
+    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
     "weight_dequant_2d", "load_library",
 ]
 
@@ -203,6 +203,102 @@ def kv_dequant(codes, scales, tensor_scale, mean=None, tokens_per_group: Optiona
     st = _lib.nvfp4_kv_dequant(_ptr(codes), _ptr(scales), _ptr(tensor_scale), _ptr(mean), tpg, T, H, D, _ptr(out),
                                _stream(stream))
     _lib.check(st, "nvfp4_kv_dequant")
+    return out
+
+
+class KvCache:
+    """Host bookkeeping of a multi-shot NVFP4 KV cache (``nvfp4_kvcache_*``): which chunk
+    slot holds which chunk, the global sink, the shot sink (START/LEN) and the rolling
+    window.  No device memory: pair it with one ``KvCachePool`` per cached tensor."""
+
+    def __init__(self, frames_per_chunk: int, tokens_per_frame: int, global_sink: int, shot_sink: int, window: int,
+                 n_slots: Optional[int] = None):
+        if n_slots is None:
+            n_slots = _lib.nvfp4_kvcache_slots_needed(frames_per_chunk, global_sink, shot_sink, window)
+        self.state = _lib.nvfp4_kvcache()
+        _lib.check(_lib.nvfp4_kvcache_init(self.state, frames_per_chunk, tokens_per_frame, global_sink, shot_sink,
+                                           window, n_slots), "nvfp4_kvcache_init")
+
+    @property
+    def n_slots(self) -> int:
+        return self.state.n_slots
+
+    @property
+    def n_chunks(self) -> int:
+        return self.state.n_chunks
+
+    def append(self) -> int:
+        """Slot for the next chunk (releases dead slots first)."""
+        slot = ctypes.c_int(-1)
+        _lib.check(_lib.nvfp4_kvcache_append(self.state, slot), "nvfp4_kvcache_append")
+        return slot.value
+
+    def new_shot(self) -> None:
+        _lib.check(_lib.nvfp4_kvcache_new_shot(self.state), "nvfp4_kvcache_new_shot")
+
+    def view(self):
+        """(frame_index, frame_row, frame_slot) numpy arrays of the next chunk's view."""
+        import numpy as np
+
+        cap = self.state.global_sink + self.state.shot_sink + self.state.window
+        fi, fr = np.zeros(cap, np.int64), np.zeros(cap, np.int64)
+        fs = np.zeros(cap, np.int32)
+        n = _lib.nvfp4_kvcache_view(self.state, fi.ctypes.data, fr.ctypes.data, fs.ctypes.data, cap)
+        if n < 0:
+            raise NVFP4Error(_lib.NVFP4_EINVAL, "nvfp4_kvcache_view")
+        return fi[:n], fr[:n], fs[:n]
+
+
+class KvCachePool(NamedTuple):
+    """Device storage of one cached tensor: ``n_slots`` chunk slots of F_c * L_f tokens."""
+    codes: "torch.Tensor"   # uint8 [n_slots * F_c * L_f, H, D/2]
+    scales: "torch.Tensor"  # uint8 [n_slots * F_c * L_f, H, D/16]
+    g: "torch.Tensor"       # float32 [n_slots]
+    mean: Optional["torch.Tensor"]  # float32 [n_slots, H, D] (smoothed tensors) or None
+
+    @staticmethod
+    def allocate(cache: KvCache, H: int, D: int, smooth: bool, device=None) -> "KvCachePool":
+        torch = _torch()
+        st = cache.state
+        rows = st.n_slots * st.frames_per_chunk * st.tokens_per_frame
+        dev = device or "cuda"
+        return KvCachePool(torch.zeros((rows, H, D // 2), dtype=torch.uint8, device=dev),
+                           torch.zeros((rows, H, D // 16), dtype=torch.uint8, device=dev),
+                           torch.zeros(st.n_slots, dtype=torch.float32, device=dev),
+                           torch.zeros((st.n_slots, H, D), dtype=torch.float32, device=dev) if smooth else None)
+
+    def slot_outputs(self, cache: KvCache, slot: int, status=None) -> "KvQuantized":
+        """The quantizer's outputs for a chunk written straight into ``slot`` (views, no copy)."""
+        torch = _torch()
+        rows = cache.state.frames_per_chunk * cache.state.tokens_per_frame
+        r0 = slot * rows
+        if status is None:
+            status = torch.zeros(1, dtype=torch.int32, device=self.codes.device)
+        return KvQuantized(self.codes[r0:r0 + rows], self.scales[r0:r0 + rows], self.g[slot:slot + 1],
+                           None if self.mean is None else self.mean[slot], status)
+
+
+def kv_gather_dequant(pool: KvCachePool, frame_row, frame_slot, tokens_per_frame: int, with_mean: bool = True,
+                      out=None, stream=None):
+    """Expand a view (frame_row, frame_slot: host int arrays from ``KvCache.view``) to bf16
+    [n_frames * L_f, H, D], each frame with its slot's tensor scale (and mean when
+    ``with_mean`` and the pool has means)."""
+    import numpy as np
+
+    torch = _torch()
+    _check_cuda(pool.codes, pool.scales, pool.g, pool.mean)
+    rows, H, D2 = pool.codes.shape
+    D = 2 * D2
+    fr = np.ascontiguousarray(frame_row, dtype=np.int64)
+    fs = np.ascontiguousarray(frame_slot, dtype=np.int32)
+    n = int(fr.shape[0])
+    if out is None:
+        out = torch.empty((n * tokens_per_frame, H, D), dtype=torch.bfloat16, device=pool.codes.device)
+    mean = pool.mean if with_mean else None
+    st = _lib.nvfp4_kv_gather_dequant(_ptr(pool.codes), _ptr(pool.scales), _ptr(pool.g), _ptr(mean), rows,
+                                      int(pool.g.numel()), fr.ctypes.data, fs.ctypes.data, n, tokens_per_frame, H, D,
+                                      _ptr(out), _stream(stream))
+    _lib.check(st, "nvfp4_kv_gather_dequant")
     return out
 
 

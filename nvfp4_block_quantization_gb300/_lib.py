@@ -11,7 +11,9 @@ import os
 
 from .build import LIB_PATH
 
-NVFP4_OK, NVFP4_EINVAL, NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA = range(6)
+NVFP4_OK, NVFP4_EINVAL, NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA, NVFP4_ECAPACITY = range(7)
+NVFP4_KVCACHE_MAX_SLOTS = 64
+NVFP4_MAX_VIEW_FRAMES = 512
 NVFP4_IN_BF16, NVFP4_IN_FP32 = 0, 1
 NVFP4_DEV_OK, NVFP4_DEV_NONFINITE = 0, 1
 
@@ -26,6 +28,12 @@ EXPORTS = (
     "nvfp4_kv_stats_batched",
     "nvfp4_kv_quant_batched",
     "nvfp4_kv_dequant",
+    "nvfp4_kvcache_slots_needed",
+    "nvfp4_kvcache_init",
+    "nvfp4_kvcache_append",
+    "nvfp4_kvcache_new_shot",
+    "nvfp4_kvcache_view",
+    "nvfp4_kv_gather_dequant",
     "nvfp4_w2d_workspace_bytes",
     "nvfp4_weight_quant_2d",
     "nvfp4_w2d_batched_workspace_bytes",
@@ -55,6 +63,20 @@ class nvfp4_w2d_job(ctypes.Structure):
         ("codes", ctypes.c_void_p),
         ("scales", ctypes.c_void_p),
         ("tensor_scale", ctypes.c_void_p),
+    ]
+
+
+class nvfp4_kvcache(ctypes.Structure):
+    _fields_ = [
+        ("frames_per_chunk", ctypes.c_int),
+        ("global_sink", ctypes.c_int),
+        ("shot_sink", ctypes.c_int),
+        ("window", ctypes.c_int),
+        ("n_slots", ctypes.c_int),
+        ("tokens_per_frame", ctypes.c_int64),
+        ("n_chunks", ctypes.c_int64),
+        ("shot_start", ctypes.c_int64),
+        ("slot_chunk", ctypes.c_int64 * NVFP4_KVCACHE_MAX_SLOTS),
     ]
 
 
@@ -97,6 +119,19 @@ def load(path: str | None = None):
     lib.nvfp4_kv_quant_batched.restype = i32
     lib.nvfp4_kv_dequant.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.nvfp4_kv_dequant.restype = i32
+    P = ctypes.POINTER
+    lib.nvfp4_kvcache_slots_needed.argtypes = [i32, i32, i32, i32]
+    lib.nvfp4_kvcache_slots_needed.restype = i32
+    lib.nvfp4_kvcache_init.argtypes = [P(nvfp4_kvcache), i32, i64, i32, i32, i32, i32]
+    lib.nvfp4_kvcache_init.restype = i32
+    lib.nvfp4_kvcache_append.argtypes = [P(nvfp4_kvcache), P(i32)]
+    lib.nvfp4_kvcache_append.restype = i32
+    lib.nvfp4_kvcache_new_shot.argtypes = [P(nvfp4_kvcache)]
+    lib.nvfp4_kvcache_new_shot.restype = i32
+    lib.nvfp4_kvcache_view.argtypes = [P(nvfp4_kvcache), vp, vp, vp, i32]
+    lib.nvfp4_kvcache_view.restype = i32
+    lib.nvfp4_kv_gather_dequant.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32, i32, vp, vp]
+    lib.nvfp4_kv_gather_dequant.restype = i32
     lib.nvfp4_w2d_workspace_bytes.argtypes = [i64, i64]
     lib.nvfp4_w2d_workspace_bytes.restype = sz
     lib.nvfp4_weight_quant_2d.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
@@ -155,6 +190,33 @@ def nvfp4_kv_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, wor
 
 def nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream):
     return load().nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream)
+
+
+def nvfp4_kvcache_slots_needed(frames_per_chunk, global_sink, shot_sink, window):
+    return load().nvfp4_kvcache_slots_needed(frames_per_chunk, global_sink, shot_sink, window)
+
+
+def nvfp4_kvcache_init(c, frames_per_chunk, tokens_per_frame, global_sink, shot_sink, window, n_slots):
+    return load().nvfp4_kvcache_init(ctypes.byref(c), frames_per_chunk, tokens_per_frame, global_sink, shot_sink,
+                                     window, n_slots)
+
+
+def nvfp4_kvcache_append(c, slot):
+    return load().nvfp4_kvcache_append(ctypes.byref(c), ctypes.byref(slot))
+
+
+def nvfp4_kvcache_new_shot(c):
+    return load().nvfp4_kvcache_new_shot(ctypes.byref(c))
+
+
+def nvfp4_kvcache_view(c, frame_index, frame_row, frame_slot, max_frames):
+    return load().nvfp4_kvcache_view(ctypes.byref(c), frame_index, frame_row, frame_slot, max_frames)
+
+
+def nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_rows, n_meta, frame_row, frame_meta,
+                            n_frames, tokens_per_frame, H, D, out_bf16, stream):
+    return load().nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_rows, n_meta, frame_row,
+                                          frame_meta, n_frames, tokens_per_frame, H, D, out_bf16, stream)
 
 
 def nvfp4_w2d_workspace_bytes(M, N):

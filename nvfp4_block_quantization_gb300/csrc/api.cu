@@ -164,6 +164,7 @@ const char* nvfp4_status_string(nvfp4_status s) {
     case NVFP4_EALIGN: return "NVFP4_EALIGN: misaligned pointer";
     case NVFP4_EWORKSPACE: return "NVFP4_EWORKSPACE: workspace missing, too small or misaligned";
     case NVFP4_ECUDA: return "NVFP4_ECUDA: CUDA error";
+    case NVFP4_ECAPACITY: return "NVFP4_ECAPACITY: no free chunk slot in the KV-cache pool";
   }
   return "NVFP4_UNKNOWN";
 }

@@ -57,8 +57,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-rows", action="store_true", help="skip the secondary rows (dequant, weights, 30 layers)")
     p.add_argument("--rows", nargs="+", default=None, metavar="ROW",
-                   help="run only these secondary rows: kv_write_30_layers kv_cache_read_dequant weight_quant_2d "
-                        "activation_quant_1d k_only_smooth_quant")
+                   help="run only these secondary rows: kv_write_30_layers kv_cache_read_dequant kv_cache_view_gather "
+                        "gemm_w4a4 weight_quant_2d activation_quant_1d k_only_smooth_quant")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=30)
     return p.parse_args()
@@ -594,6 +594,60 @@ def row_kv_cache_view_gather(nv, W, torch, dev, peak):
             "view_frames": 21, "slots_per_pool": 5}
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates of the part
+
+
+def fp4_peak_tflops():
+    """Dense FP4 peak: the measured cuBLAS bf16 burst rate times the nominal FP4/BF16 ratio."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]) * FP4_OVER_BF16, "measured bf16 x nominal fp4/bf16 ratio 6"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, "fallback bf16 x nominal fp4/bf16 ratio 6"
+
+
+def row_gemm_w4a4(nv, W, torch, dev, peak):
+    """W4A4 linear layer: activations 7040 x 3072 ~ N(0, 1) quantized with 1-D blocks, four 3072 x 3072
+    weights ~ N(0, 0.02^2) quantized with 16x16 tiles (weights and their tensor-core scales prepared
+    once), Y = X W^T in bf16.  Times the GEMM alone (four weights in rotation) and the whole linear
+    step: quantize X, rearrange its scales, GEMM."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5200)
+    M, N, K = T_CHUNK, 3072, 3072
+    x = torch.randn((M, 1, K), generator=gen, device=dev).to(torch.bfloat16)
+    xq = nv.kv_smooth_quant(x, False)
+    xs = nv.mma_scales(xq.scales.view(M, K // 16), K)
+    wts = []
+    for i in range(4):
+        w = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        wq = nv.weight_quant_2d(w)
+        wts.append((wq, nv.mma_scales(wq.scales, K, tile2d=True)))
+        del w
+    plan = nv.GemmPlan(M, N, K)
+    ws = nv.gemm_workspace(dev)
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    xc = xq.codes.view(M, K // 2)
+
+    def gemm(i):
+        wq, wsc = wts[i % 4]
+        nv.gemm_w4a4(plan, xc, xs, xq.tensor_scale, wq.codes, wsc, wq.tensor_scale, ws, out=ys[i % 4])
+
+    ms = _time_graph(torch, gemm, 8, 20)
+    aws = nv.kv_workspace(M, 1, K, 1, dev)
+
+    def linear(i):
+        nv.kv_smooth_quant(x, False, workspace=aws, out=xq)
+        nv.mma_scales(xq.scales.view(M, K // 16), K, out=xs)
+        gemm(i)
+
+    ms_lin = _time_graph(torch, linear, 8, 20)
+    fl = 2.0 * M * N * K
+    pk, src = fp4_peak_tflops()
+    return {"TFLOP/s": fl / ms / 1e9, "ms_gemm": ms, "ms_linear_step": ms_lin, "flops": fl,
+            "peak_tflops": pk, "peak_source": src, "frac": fl / ms / 1e9 / pk}
+
+
 def row_weight_quant_2d(nv, W, torch, dev, peak):
     """Weights: 4 x 3072x3072 and 2 x 3072x14336 bf16, N(0, 0.02^2), 16x16 tiles, in one batched call
     (and, for comparison, as six single calls)."""
@@ -640,7 +694,7 @@ def row_k_only_smooth_quant(nv, W, torch, dev, peak):
 
 
 ROWS = {"kv_write_30_layers": row_kv_write_30_layers, "kv_cache_read_dequant": row_kv_cache_read_dequant,
-        "kv_cache_view_gather": row_kv_cache_view_gather,
+        "kv_cache_view_gather": row_kv_cache_view_gather, "gemm_w4a4": row_gemm_w4a4,
         "weight_quant_2d": row_weight_quant_2d, "activation_quant_1d": row_activation_quant_1d,
         "k_only_smooth_quant": row_k_only_smooth_quant}
 

@@ -342,6 +342,58 @@ nvfp4_status nvfp4_weight_quant_2d_static(const void* w, nvfp4_in_dtype dt, int6
 nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
                                      int64_t M, int64_t N, void* out_bf16, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* W4A4 NVFP4 GEMM (LongLive-2.0 summary page, training step 4: NVFP4 GEMMs  */
+/* with 2-D block scales for weights and 1-D for activations; inference     */
+/* step 6: a W4A4 model).                                                   */
+/* ------------------------------------------------------------------------ */
+/* Y[M][N] = bf16_rne(fl(gX * gW) * sum_k (QX * EX)[m][k] * (QW * EW)[n][k]), the
+ * sum accumulated in fp32 by the tensor cores (cuBLASLt, E2M1 operands with
+ * VEC16 UE4M3 block scales).  X is an activation quantized by the 1-D
+ * quantizer (nvfp4_kv_smooth_quant with H = 1, D = K, no smoothing): codes
+ * [M][K/2], scales [M][K/16].  W is a weight quantized by
+ * nvfp4_weight_quant_2d: codes [N][K/2], scales [N/16][K/16].
+ *
+ * The tensor cores read block scales in their own layout: per operand, tiles
+ * of 128 rows x 4 blocks (64 elements of K), 512 bytes each, K tiles fastest;
+ * inside a tile, block c of row r sits at byte (r % 32) * 16 + (r / 32) * 4 + c.
+ * Rows past the operand and blocks past K/16 are zero. */
+
+/* Bytes of an operand's scales in that layout: roundup(rows, 128) *
+ * roundup(K / 16, 4); 0 for invalid sizes. */
+int64_t nvfp4_mma_scales_bytes(int64_t rows, int64_t K);
+
+/* Row-major 1-D block scales [rows][K/16] (device) -> the tensor-core layout
+ * (device, nvfp4_mma_scales_bytes(rows, K) bytes, padding zeroed). */
+nvfp4_status nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* out, void* stream);
+
+/* 16x16-tile weight scales [N/16][K/16] (device) -> per-row block scales in the
+ * tensor-core layout for N rows (each tile's scale repeated for its 16 rows). */
+nvfp4_status nvfp4_w2d_scales_to_mma(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out, void* stream);
+
+/* Device workspace of nvfp4_gemm_w4a4 (256-byte aligned; no zero-fill needed). */
+size_t nvfp4_gemm_workspace_bytes(void);
+
+/* A GEMM plan for one shape: the cuBLASLt handle, descriptors and algorithm.
+ * It is the one object the library allocates, in host memory; the caller owns
+ * it and frees it with nvfp4_gemm_plan_destroy.  A plan serves one host thread
+ * at a time.  M >= 1, N a multiple of 16, K a multiple of 32 (NVFP4_ESHAPE
+ * otherwise); NVFP4_ECUDA when cuBLASLt has no algorithm for the shape. */
+typedef struct nvfp4_gemm_plan nvfp4_gemm_plan;
+nvfp4_status nvfp4_gemm_plan_create(int64_t M, int64_t N, int64_t K, nvfp4_gemm_plan** plan);
+void nvfp4_gemm_plan_destroy(nvfp4_gemm_plan* plan);
+
+/* Y = X W^T as above, enqueued on `stream`.
+ *   x_codes, w_codes          device, 16-byte aligned
+ *   x_scales_mma, w_scales_mma device, the tensor-core layout, 16-byte aligned
+ *   x_tensor_scale, w_tensor_scale  device fp32 [1] (gX, gW)
+ *   y_bf16                    device [M][N] bf16, 16-byte aligned
+ *   workspace                 device, nvfp4_gemm_workspace_bytes() */
+nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, const uint8_t* x_scales_mma,
+                             const float* x_tensor_scale, const uint8_t* w_codes, const uint8_t* w_scales_mma,
+                             const float* w_tensor_scale, void* y_bf16, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 #ifdef __cplusplus
 }
 #endif

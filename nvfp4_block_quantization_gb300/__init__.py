@@ -21,7 +21,8 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
+    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "GemmPlan", "gemm_w4a4",
+    "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
     "weight_dequant_2d", "load_library",
 ]
 
@@ -299,6 +300,56 @@ def kv_gather_dequant(pool: KvCachePool, frame_row, frame_slot, tokens_per_frame
                                       int(pool.g.numel()), fr.ctypes.data, fs.ctypes.data, n, tokens_per_frame, H, D,
                                       _ptr(out), _stream(stream))
     _lib.check(st, "nvfp4_kv_gather_dequant")
+    return out
+
+
+def mma_scales(scales, K: int, tile2d: bool = False, out=None, stream=None):
+    """Block scales in the tensor cores' layout (``nvfp4_scales_to_mma`` / ``nvfp4_w2d_scales_to_mma``).
+
+    ``scales``: uint8 [rows, K/16] (1-D activation scales) or, with ``tile2d``, the
+    16x16-tile weight scales [N/16, K/16]; returns a flat uint8 tensor."""
+    torch = _torch()
+    _check_cuda(scales)
+    rows = scales.shape[0] * (16 if tile2d else 1)
+    n = _lib.nvfp4_mma_scales_bytes(rows, K)
+    if out is None:
+        out = torch.empty(max(n, 16), dtype=torch.uint8, device=scales.device)
+    fn = _lib.nvfp4_w2d_scales_to_mma if tile2d else _lib.nvfp4_scales_to_mma
+    _lib.check(fn(_ptr(scales), rows, K, _ptr(out), _stream(stream)), fn.__name__)
+    return out
+
+
+class GemmPlan:
+    """Caller-owned W4A4 GEMM plan for one (M, N, K) (``nvfp4_gemm_plan_create``)."""
+
+    def __init__(self, M: int, N: int, K: int):
+        self.M, self.N, self.K = M, N, K
+        self._p = ctypes.c_void_p()
+        _lib.check(_lib.nvfp4_gemm_plan_create(M, N, K, self._p), "nvfp4_gemm_plan_create")
+
+    def __del__(self):
+        if getattr(self, "_p", None) is not None and self._p.value:
+            _lib.nvfp4_gemm_plan_destroy(self._p)
+            self._p = None
+
+
+def gemm_workspace(device=None):
+    torch = _torch()
+    return torch.empty(_lib.nvfp4_gemm_workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
+
+
+def gemm_w4a4(plan: GemmPlan, x_codes, x_scales_mma, x_tensor_scale, w_codes, w_scales_mma, w_tensor_scale,
+              workspace, out=None, stream=None):
+    """Y [M, N] bf16 = X W^T from NVFP4 operands (``nvfp4_gemm_w4a4``): X codes [M, K/2], W codes
+    [N, K/2], scales already in the tensor-core layout (``mma_scales``)."""
+    torch = _torch()
+    _check_cuda(x_codes, x_scales_mma, x_tensor_scale, w_codes, w_scales_mma, w_tensor_scale, workspace)
+    if out is None:
+        out = torch.empty((plan.M, plan.N), dtype=torch.bfloat16, device=x_codes.device)
+    st = _lib.nvfp4_gemm_w4a4(plan._p, _ptr(x_codes), _ptr(x_scales_mma), _ptr(x_tensor_scale), _ptr(w_codes),
+                              _ptr(w_scales_mma), _ptr(w_tensor_scale), _ptr(out), _ptr(workspace),
+                              workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_gemm_w4a4")
     return out
 
 

@@ -34,6 +34,13 @@ EXPORTS = (
     "nvfp4_kvcache_new_shot",
     "nvfp4_kvcache_view",
     "nvfp4_kv_gather_dequant",
+    "nvfp4_mma_scales_bytes",
+    "nvfp4_scales_to_mma",
+    "nvfp4_w2d_scales_to_mma",
+    "nvfp4_gemm_workspace_bytes",
+    "nvfp4_gemm_plan_create",
+    "nvfp4_gemm_plan_destroy",
+    "nvfp4_gemm_w4a4",
     "nvfp4_w2d_workspace_bytes",
     "nvfp4_weight_quant_2d",
     "nvfp4_w2d_batched_workspace_bytes",
@@ -132,6 +139,20 @@ def load(path: str | None = None):
     lib.nvfp4_kvcache_view.restype = i32
     lib.nvfp4_kv_gather_dequant.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.nvfp4_kv_gather_dequant.restype = i32
+    lib.nvfp4_mma_scales_bytes.argtypes = [i64, i64]
+    lib.nvfp4_mma_scales_bytes.restype = i64
+    lib.nvfp4_scales_to_mma.argtypes = [vp, i64, i64, vp, vp]
+    lib.nvfp4_scales_to_mma.restype = i32
+    lib.nvfp4_w2d_scales_to_mma.argtypes = [vp, i64, i64, vp, vp]
+    lib.nvfp4_w2d_scales_to_mma.restype = i32
+    lib.nvfp4_gemm_workspace_bytes.argtypes = []
+    lib.nvfp4_gemm_workspace_bytes.restype = sz
+    lib.nvfp4_gemm_plan_create.argtypes = [i64, i64, i64, P(vp)]
+    lib.nvfp4_gemm_plan_create.restype = i32
+    lib.nvfp4_gemm_plan_destroy.argtypes = [vp]
+    lib.nvfp4_gemm_plan_destroy.restype = None
+    lib.nvfp4_gemm_w4a4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.nvfp4_gemm_w4a4.restype = i32
     lib.nvfp4_w2d_workspace_bytes.argtypes = [i64, i64]
     lib.nvfp4_w2d_workspace_bytes.restype = sz
     lib.nvfp4_weight_quant_2d.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
@@ -217,6 +238,36 @@ def nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_row
                             n_frames, tokens_per_frame, H, D, out_bf16, stream):
     return load().nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_rows, n_meta, frame_row,
                                           frame_meta, n_frames, tokens_per_frame, H, D, out_bf16, stream)
+
+
+def nvfp4_mma_scales_bytes(rows, K):
+    return load().nvfp4_mma_scales_bytes(rows, K)
+
+
+def nvfp4_scales_to_mma(scales, rows, K, out, stream):
+    return load().nvfp4_scales_to_mma(scales, rows, K, out, stream)
+
+
+def nvfp4_w2d_scales_to_mma(scales, N, K, out, stream):
+    return load().nvfp4_w2d_scales_to_mma(scales, N, K, out, stream)
+
+
+def nvfp4_gemm_workspace_bytes():
+    return load().nvfp4_gemm_workspace_bytes()
+
+
+def nvfp4_gemm_plan_create(M, N, K, plan):
+    return load().nvfp4_gemm_plan_create(M, N, K, ctypes.byref(plan))
+
+
+def nvfp4_gemm_plan_destroy(plan):
+    load().nvfp4_gemm_plan_destroy(plan)
+
+
+def nvfp4_gemm_w4a4(plan, x_codes, x_scales_mma, x_tensor_scale, w_codes, w_scales_mma, w_tensor_scale, y_bf16,
+                    workspace, workspace_bytes, stream):
+    return load().nvfp4_gemm_w4a4(plan, x_codes, x_scales_mma, x_tensor_scale, w_codes, w_scales_mma, w_tensor_scale,
+                                  y_bf16, workspace, workspace_bytes, stream)
 
 
 def nvfp4_w2d_workspace_bytes(M, N):

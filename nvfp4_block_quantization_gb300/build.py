@@ -67,7 +67,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    r = subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"], capture_output=True, text=True)
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
+    r = subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib],
+                       capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)

@@ -1,0 +1,69 @@
+"""W4A4 NVFP4 GEMM without a GPU: the oracle reference against closed forms, and the
+C entry points' argument checks (which return before any CUDA or cuBLASLt call)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from oracle import gemm as og
+
+
+def test_reference_closed_form_scales():
+    """Every element 1.0; activation block scales 1 (even blocks) and 0.5 (odd blocks) times
+    (1 + m % 3); weight tile scales 2^(tile row % 4).  Each output is then a closed form."""
+    M, N, K = 5, 64, 128
+    KB = K // 16
+    xc = np.full((M, K // 2), 0x22, np.uint8)       # E2M1 code 2 = 1.0 in both nibbles
+    wc = np.full((N, K // 2), 0x22, np.uint8)
+    one_two_three = [0x38, 0x40, 0x44]               # E4M3 1, 2, 3
+    xs = np.array([[one_two_three[m % 3] if kb % 2 == 0 else 0x30 for kb in range(KB)] for m in range(M)], np.uint8)
+    pow2 = [0x38, 0x40, 0x48, 0x50]                  # E4M3 1, 2, 4, 8
+    ws = np.array([[pow2[t % 4]] * KB for t in range(N // 16)], np.uint8)
+    y, s = og.gemm_w4a4(xc, xs, 0.25, wc, ws, 3.0)
+    for m in range(M):
+        for n in range(N):
+            want = 0.75 * 16 * (2 ** ((n // 16) % 4)) * (KB // 2) * ((1 + m % 3) + 0.5)
+            assert y[m, n] == want and s[m, n] == want
+
+
+def test_reference_nibble_order_and_sign():
+    """Byte j holds element 2j in its low nibble: X bytes 0x42 (1, 2), W bytes 0x0A (-1, 0)
+    pair 1 with -1 and 2 with 0, so each byte contributes -1 (a swap in one operand would give 0
+    or -2)."""
+    K = 64
+    xc = np.full((1, K // 2), 0x42, np.uint8)
+    wc = np.full((16, K // 2), 0x0A, np.uint8)
+    xs = np.full((1, K // 16), 0x38, np.uint8)
+    ws = np.full((1, K // 16), 0x38, np.uint8)
+    y, s = og.gemm_w4a4(xc, xs, 1.0, wc, ws, 1.0)
+    assert np.all(y == -K / 2) and np.all(s == K / 2)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_quantization_gb300 import _lib
+    from nvfp4_block_quantization_gb300.build import build
+
+    build()
+    return _lib
+
+
+def test_mma_scale_bytes(lib):
+    assert lib.nvfp4_mma_scales_bytes(200, 512) == 256 * 32
+    assert lib.nvfp4_mma_scales_bytes(128, 64) == 128 * 4
+    assert lib.nvfp4_mma_scales_bytes(1, 16) == 128 * 4
+    assert lib.nvfp4_mma_scales_bytes(7040, 3072) == 7040 * 192
+    assert lib.nvfp4_mma_scales_bytes(8, 24) == 0
+
+
+def test_gemm_argument_errors(lib):
+    p = ctypes.c_void_p()
+    for M, N, K in ((0, 64, 64), (8, 24, 64), (8, 64, 48), (8, 64, 16), (1 << 31, 64, 64)):
+        assert lib.nvfp4_gemm_plan_create(M, N, K, p) == lib.NVFP4_ESHAPE
+        assert not p.value
+    assert lib.load().nvfp4_gemm_plan_create(8, 64, 64, None) == lib.NVFP4_EINVAL
+    g = 1 << 20
+    assert lib.nvfp4_gemm_w4a4(None, g, g, g, g, g, g, g, g, 1 << 26, None) == lib.NVFP4_EINVAL
+    assert lib.nvfp4_scales_to_mma(g, 8, 24, g, None) == lib.NVFP4_ESHAPE
+    assert lib.nvfp4_w2d_scales_to_mma(g, 24, 64, g, None) == lib.NVFP4_ESHAPE
+    assert lib.nvfp4_scales_to_mma(None, 8, 64, g, None) == lib.NVFP4_EINVAL

@@ -1,0 +1,123 @@
+"""GPU: the W4A4 NVFP4 GEMM through the C ABI against the oracle reference.
+
+Operands come from this library's quantizers (1-D activation blocks, 16x16 weight
+tiles), whose bits are checked against the oracle elsewhere.  The GPU sums exact
+products in fp32 on the tensor cores and rounds the scaled result to bf16, so each
+output must satisfy
+    |y - ref| <= 2^-8 |ref| + (1 + 2^-8) * 2 K 2^-24 * sum_k |x w| * gX gW
+(bf16 rounding of the result, plus the worst case of an fp32 summation of K
+terms, doubled), with ref and the absolute sum from the oracle in binary64.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def nv():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    from nvfp4_block_quantization_gb300.build import build
+
+    build()
+    import nvfp4_block_quantization_gb300 as nv
+
+    nv.load_library()
+    return nv
+
+
+def bf16_dev(a: np.ndarray):
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    return torch.from_numpy(W.to_bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def quantized_operands(nv, X, Wm):
+    M, K = X.shape
+    xq = nv.kv_smooth_quant(bf16_dev(X).view(M, 1, K), False)
+    wq = nv.weight_quant_2d(bf16_dev(Wm))
+    torch.cuda.synchronize()
+    assert int(host(xq.status)[0]) == 0 and int(host(wq.status)[0]) == 0
+    return xq, wq
+
+
+def run_gemm(nv, xq, wq, M, N, K):
+    xs = nv.mma_scales(xq.scales.view(M, K // 16), K)
+    ws = nv.mma_scales(wq.scales, K, tile2d=True)
+    plan = nv.GemmPlan(M, N, K)
+    y = nv.gemm_w4a4(plan, xq.codes.view(M, K // 2), xs, xq.tensor_scale, wq.codes, ws, wq.tensor_scale,
+                     nv.gemm_workspace())
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def check(y, ref, sabs, K):
+    tol = 2.0 ** -8 * np.abs(ref) + (1 + 2.0 ** -8) * 2 * K * 2.0 ** -24 * sabs
+    bad = np.abs(y - ref) > tol
+    assert not bad.any(), (int(bad.sum()), float(np.max(np.abs(y - ref) - tol)))
+
+
+def test_scale_layout_matches_its_definition(nv):
+    """Block (r, c) lands in tile (r / 128, c / 4) at (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4;
+    the padding is zero; a weight tile's scale covers its 16 rows."""
+    rng = np.random.default_rng(3)
+    rows, K = 300, 16 * 13
+    KB = K // 16
+    s = rng.integers(1, 255, size=(rows, KB), dtype=np.uint8)
+    got = host(nv.mma_scales(torch.from_numpy(s).cuda(), K))
+    kbt = (KB + 3) // 4
+    want = np.zeros(((rows + 127) // 128) * 128 * kbt * 4, np.uint8)
+    for r in range(rows):
+        for c in range(KB):
+            want[((r // 128) * kbt + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4] = s[r, c]
+    assert np.array_equal(got[:want.size], want)
+    t = rng.integers(1, 255, size=(rows // 16 + 1, KB), dtype=np.uint8)
+    got2 = host(nv.mma_scales(torch.from_numpy(t).cuda(), K, tile2d=True))
+    rows2 = t.shape[0] * 16
+    want2 = np.zeros(((rows2 + 127) // 128) * 128 * kbt * 4, np.uint8)
+    for r in range(rows2):
+        for c in range(KB):
+            want2[((r // 128) * kbt + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4] = t[r // 16, c]
+    assert np.array_equal(got2[:want2.size], want2)
+
+
+def test_w4a4_small_ragged(nv):
+    """M = 200 (not a multiple of the 128-row scale tile), N = 384, K = 512."""
+    from oracle import gemm as og
+
+    rng = np.random.default_rng(11)
+    M, N, K = 200, 384, 512
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    Wm = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Wm.flat[rng.choice(Wm.size, Wm.size // 1000, replace=False)] *= 30.0
+    xq, wq = quantized_operands(nv, X, Wm)
+    y = run_gemm(nv, xq, wq, M, N, K)
+    ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2), host(xq.scales).reshape(M, K // 16),
+                             float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
+                             float(host(wq.tensor_scale)[0]))
+    check(y, ref, sabs, K)
+
+
+def test_w4a4_linear_sizes_sampled_rows(nv):
+    """Activations 7040 x 3072 ~ N(0, 1) and a 3072 x 3072 weight ~ N(0, 0.02^2) with 0.1% x30,
+    as the GEMM of a W4A4 linear layer; 64 sampled rows against the oracle."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+    from oracle import gemm as og
+
+    M, N, K = 7040, 3072, 3072
+    X = W.activations(T=M, D=K)
+    Wm = W.weight(0, N, K)
+    xq, wq = quantized_operands(nv, X, Wm)
+    y = run_gemm(nv, xq, wq, M, N, K)
+    rows = np.sort(np.random.default_rng(5).choice(M, 64, replace=False))
+    ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2)[rows], host(xq.scales).reshape(M, K // 16)[rows],
+                             float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
+                             float(host(wq.tensor_scale)[0]))
+    check(y[rows], ref, sabs, K)

@@ -644,8 +644,36 @@ def row_gemm_w4a4(nv, W, torch, dev, peak):
     ms_lin = _time_graph(torch, linear, 8, 20)
     fl = 2.0 * M * N * K
     pk, src = fp4_peak_tflops()
-    return {"TFLOP/s": fl / ms / 1e9, "ms_gemm": ms, "ms_linear_step": ms_lin, "flops": fl,
-            "peak_tflops": pk, "peak_source": src, "frac": fl / ms / 1e9 / pk}
+    out = {"TFLOP/s": fl / ms / 1e9, "ms_gemm": ms, "ms_linear_step": ms_lin, "flops": fl,
+           "peak_tflops": pk, "peak_source": src, "frac": fl / ms / 1e9 / pk}
+
+    # random Hadamard transform of the activation (bf16 in, fp32 out: 6 bytes per element)
+    signs = int(torch.randint(0, 1 << 16, (1,), generator=gen, device=dev).item())
+    xr = torch.empty((M, K), dtype=torch.float32, device=dev)
+    ms_rht = _time_graph(torch, lambda i: nv.rht16(x.view(M, K), signs, out=xr), 8, 20)
+    out["rht16_activation"] = {"ms": ms_rht, "bytes": 6.0 * M * K, "GB/s": 6.0 * M * K / ms_rht / 1e6,
+                               "frac": 6.0 * M * K / ms_rht / 1e6 / peak}
+    # error of Y against the exact product, without and with the transform, on a weight with the
+    # workload's outliers (0.1% of entries x30)
+    w = torch.randn((N, K), generator=gen, device=dev) * 0.02
+    idx = torch.randperm(N * K, generator=gen, device=dev)[: N * K // 1000]
+    w.view(-1)[idx] *= 30.0
+    w = w.to(torch.bfloat16)
+    exact = x.view(M, K).double() @ w.double().T
+
+    def rel(y):
+        return float(torch.linalg.norm(y.double() - exact) / torch.linalg.norm(exact))
+
+    xq = nv.kv_smooth_quant(x, False)
+    wq = nv.weight_quant_2d(w)
+    y0 = nv.gemm_w4a4(plan, xq.codes.view(M, K // 2), nv.mma_scales(xq.scales.view(M, K // 16), K),
+                      xq.tensor_scale, wq.codes, nv.mma_scales(wq.scales, K, tile2d=True), wq.tensor_scale, ws)
+    xrq = nv.kv_smooth_quant(nv.rht16(x.view(M, K), signs).view(M, 1, K), False)
+    wrq = nv.weight_quant_2d(nv.rht16(w, signs))
+    y1 = nv.gemm_w4a4(plan, xrq.codes.view(M, K // 2), nv.mma_scales(xrq.scales.view(M, K // 16), K),
+                      xrq.tensor_scale, wrq.codes, nv.mma_scales(wrq.scales, K, tile2d=True), wrq.tensor_scale, ws)
+    out["rel_frobenius_error_vs_exact"] = {"w4a4": rel(y0), "w4a4_with_rht16": rel(y1)}
+    return out
 
 
 def row_weight_quant_2d(nv, W, torch, dev, peak):

@@ -371,6 +371,19 @@ nvfp4_status nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t K,
  * tensor-core layout for N rows (each tile's scale repeated for its 16 rows). */
 nvfp4_status nvfp4_w2d_scales_to_mma(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out, void* stream);
 
+/* Random Hadamard transform against outliers (the GEMM path's RHT): along each
+ * row of x[rows][K] (bf16 or fp32, 32-byte aligned, K % 16 == 0), every block
+ * of 16 elements becomes y = (x D) H / 4 in fp32: D = diag(+-1), element i
+ * negated where bit i of `signs` (the random draw, 16 bits, an input) is set;
+ * H the 16-point Sylvester Hadamard matrix, applied by the radix-2 butterflies
+ * with strides 1, 2, 4, 8, each pair (a, b) -> (fl(a + b), fl(a - b)); the
+ * final * 1/4 is exact.  The transform is orthogonal, so transforming both
+ * GEMM operands along K with the same signs leaves X W^T unchanged:
+ * quantize rht16(X) and rht16(W) and multiply as usual.  out: device fp32
+ * [rows][K], 16-byte aligned.  NVFP4_EINVAL for signs above 0xFFFF. */
+nvfp4_status nvfp4_rht16(const void* x, nvfp4_in_dtype dt, int64_t rows, int64_t K, uint32_t signs, float* out,
+                         void* stream);
+
 /* Device workspace of nvfp4_gemm_w4a4 (256-byte aligned; no zero-fill needed). */
 size_t nvfp4_gemm_workspace_bytes(void);
 

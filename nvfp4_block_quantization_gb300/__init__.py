@@ -21,7 +21,7 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "GemmPlan", "gemm_w4a4",
+    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "rht16", "GemmPlan", "gemm_w4a4",
     "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
     "weight_dequant_2d", "load_library",
 ]
@@ -316,6 +316,19 @@ def mma_scales(scales, K: int, tile2d: bool = False, out=None, stream=None):
         out = torch.empty(max(n, 16), dtype=torch.uint8, device=scales.device)
     fn = _lib.nvfp4_w2d_scales_to_mma if tile2d else _lib.nvfp4_scales_to_mma
     _lib.check(fn(_ptr(scales), rows, K, _ptr(out), _stream(stream)), fn.__name__)
+    return out
+
+
+def rht16(x, signs: int, out=None, stream=None):
+    """Random Hadamard transform of every 16-element block along the last dim (``nvfp4_rht16``):
+    x [rows, K] bf16 or fp32 -> fp32 [rows, K]."""
+    torch = _torch()
+    _check_cuda(x)
+    K = x.shape[-1]
+    rows = x.numel() // K
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _lib.check(_lib.nvfp4_rht16(_ptr(x), _dt(x), rows, K, int(signs), _ptr(out), _stream(stream)), "nvfp4_rht16")
     return out
 
 

@@ -37,6 +37,7 @@ EXPORTS = (
     "nvfp4_mma_scales_bytes",
     "nvfp4_scales_to_mma",
     "nvfp4_w2d_scales_to_mma",
+    "nvfp4_rht16",
     "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm_plan_create",
     "nvfp4_gemm_plan_destroy",
@@ -145,6 +146,8 @@ def load(path: str | None = None):
     lib.nvfp4_scales_to_mma.restype = i32
     lib.nvfp4_w2d_scales_to_mma.argtypes = [vp, i64, i64, vp, vp]
     lib.nvfp4_w2d_scales_to_mma.restype = i32
+    lib.nvfp4_rht16.argtypes = [vp, i32, i64, i64, ctypes.c_uint32, vp, vp]
+    lib.nvfp4_rht16.restype = i32
     lib.nvfp4_gemm_workspace_bytes.argtypes = []
     lib.nvfp4_gemm_workspace_bytes.restype = sz
     lib.nvfp4_gemm_plan_create.argtypes = [i64, i64, i64, P(vp)]
@@ -250,6 +253,10 @@ def nvfp4_scales_to_mma(scales, rows, K, out, stream):
 
 def nvfp4_w2d_scales_to_mma(scales, N, K, out, stream):
     return load().nvfp4_w2d_scales_to_mma(scales, N, K, out, stream)
+
+
+def nvfp4_rht16(x, dt, rows, K, signs, out, stream):
+    return load().nvfp4_rht16(x, dt, rows, K, signs, out, stream)
 
 
 def nvfp4_gemm_workspace_bytes():

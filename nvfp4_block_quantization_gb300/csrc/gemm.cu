@@ -64,6 +64,50 @@ __global__ void __launch_bounds__(256) scales_to_mma_kernel(const uint8_t* __res
   }
 }
 
+// Random Hadamard transform of 16-element blocks along the rows: one thread per
+// block.  The block x (widened exactly to fp32) has its signs flipped where the
+// bitmask `signs` has a 1 (bit i for element i), then the in-place radix-2
+// Walsh-Hadamard butterflies run with strides 1, 2, 4, 8 (each stage one fp32
+// add and one fp32 subtract per pair: (a, b) -> (a + b, a - b)), and the result
+// is scaled by 1/4 (exact).  So y = (x D) H / 4 with H the 16-point Sylvester
+// Hadamard matrix and D = diag(signs): an orthogonal transform.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ x, int64_t nblocks, uint32_t signs,
+                                                    float* __restrict__ out) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += (int64_t)gridDim.x * blockDim.x) {
+    float v[16];
+    if (kBF16) {
+      uint32_t w[8];
+      ld_nc_v8(static_cast<const uint16_t*>(x) + b * 16, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { v[2 * i] = bf16lo(w[i]); v[2 * i + 1] = bf16hi(w[i]); }
+    } else {
+      uint32_t w[16];
+      ld_nc_v8(static_cast<const float*>(x) + b * 16, w);
+      ld_nc_v8(static_cast<const float*>(x) + b * 16 + 8, w + 8);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(w[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((signs >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if ((i & h) == 0) {
+          const float a = v[i], c = v[i + h];
+          v[i] = __fadd_rn(a, c);
+          v[i + h] = __fsub_rn(a, c);
+        }
+    float4* o = reinterpret_cast<float4*>(out + b * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = make_float4(__fmul_rn(v[4 * q], 0.25f), __fmul_rn(v[4 * q + 1], 0.25f), __fmul_rn(v[4 * q + 2], 0.25f),
+                         __fmul_rn(v[4 * q + 3], 0.25f));
+  }
+}
+
 __global__ void alpha_kernel(const float* __restrict__ gx, const float* __restrict__ gw, float* __restrict__ ab) {
   ab[0] = __fmul_rn(*gx, *gw);
   ab[1] = 0.0f;
@@ -121,6 +165,26 @@ nvfp4_status nvfp4_w2d_scales_to_mma(const uint8_t* scales, int64_t N, int64_t K
   if (N < 0 || (N % 16) != 0 || K < 16 || (K % 16) != 0) return NVFP4_ESHAPE;
   if (N > 0 && (!scales || !out)) return NVFP4_EINVAL;
   return nvfp4::launch_scales(scales, N, K / 16, true, out, stream);
+}
+
+nvfp4_status nvfp4_rht16(const void* x, nvfp4_in_dtype dt, int64_t rows, int64_t K, uint32_t signs, float* out,
+                         void* stream) {
+  if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
+  if (rows < 0 || K < 16 || (K % 16) != 0) return NVFP4_ESHAPE;
+  if (rows > 0 && K > ((int64_t)1 << 46) / rows) return NVFP4_ESHAPE;
+  if (signs > 0xFFFFu) return NVFP4_EINVAL;
+  if (rows == 0) return NVFP4_OK;
+  if (!x || !out) return NVFP4_EINVAL;
+  if (!nvfp4::aligned_to(x, 32) || !nvfp4::aligned_to(out, 16)) return NVFP4_EALIGN;
+  const int sms = nvfp4::sm_count();
+  if (sms <= 0) return NVFP4_ECUDA;
+  const int64_t nb = rows * (K / 16);
+  int64_t grid = (nb + 255) / 256;
+  if (grid > (int64_t)sms * 16) grid = (int64_t)sms * 16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dt == NVFP4_IN_BF16) nvfp4::rht16_kernel<true><<<(unsigned)grid, 256, 0, s>>>(x, nb, signs, out);
+  else nvfp4::rht16_kernel<false><<<(unsigned)grid, 256, 0, s>>>(x, nb, signs, out);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
 size_t nvfp4_gemm_workspace_bytes(void) { return nvfp4::kScalarBytes + nvfp4::kGemmWorkspace; }

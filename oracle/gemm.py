@@ -63,3 +63,25 @@ def gemm_w4a4(x_codes, x_scales, x_g: float, w_codes, w_scales, w_g: float):
     Wv = dequant_2d(w_codes, w_scales)
     g = float(x_g) * float(w_g)
     return (X @ Wv.T) * g, (np.abs(X) @ np.abs(Wv).T) * abs(g)
+
+
+def rht16(x: np.ndarray, signs: int) -> np.ndarray:
+    """The GEMM path's random Hadamard transform along the rows, in fp32, step by step:
+    each block of 16 elements has element i negated where bit i of ``signs`` is set, then
+    the radix-2 Walsh-Hadamard butterflies with strides 1, 2, 4, 8 replace each pair (a, b)
+    by (fl(a + b), fl(a - b)), and the result is multiplied by 1/4."""
+    v = np.array(x, dtype=np.float32, copy=True)
+    rows, K = v.shape
+    b = v.reshape(rows, K // 16, 16)
+    for i in range(16):
+        if (signs >> i) & 1:
+            b[:, :, i] = -b[:, :, i]
+    h = 1
+    while h < 16:
+        for i in range(16):
+            if i & h == 0:
+                a, c = b[:, :, i].copy(), b[:, :, i + h].copy()
+                b[:, :, i] = a + c
+                b[:, :, i + h] = a - c
+        h *= 2
+    return (b * np.float32(0.25)).reshape(rows, K)

@@ -67,3 +67,40 @@ def test_gemm_argument_errors(lib):
     assert lib.nvfp4_scales_to_mma(g, 8, 24, g, None) == lib.NVFP4_ESHAPE
     assert lib.nvfp4_w2d_scales_to_mma(g, 24, 64, g, None) == lib.NVFP4_ESHAPE
     assert lib.nvfp4_scales_to_mma(None, 8, 64, g, None) == lib.NVFP4_EINVAL
+
+
+def test_rht16_unit_vectors_give_hadamard_rows():
+    """The transform of unit vector e_i is row i of the Sylvester Hadamard matrix over 4,
+    (-1)^popcount(i & j) / 4, negated when sign bit i is set."""
+    E = np.eye(16, dtype=np.float32)
+    H = np.array([[(-1.0) ** bin(i & j).count("1") for j in range(16)] for i in range(16)]) / 4
+    assert np.array_equal(og.rht16(E, 0), H.astype(np.float32))
+    signs = 0b1010000000010011
+    D = np.array([-1.0 if (signs >> i) & 1 else 1.0 for i in range(16)])
+    assert np.array_equal(og.rht16(E, signs), (D[:, None] * H).astype(np.float32))
+
+
+def test_rht16_is_orthogonal():
+    """R = D H / 4 has R R^T = I: on small integers (every sum exact) the transform of the
+    transform, with the signs applied after the butterflies, returns the input; and
+    (X R)(W R)^T = X W^T exactly."""
+    rng = np.random.default_rng(2)
+    X = rng.integers(-8, 9, size=(6, 64)).astype(np.float32)
+    Wm = rng.integers(-8, 9, size=(5, 64)).astype(np.float32)
+    s = 0x5A3C
+    Y = og.rht16(X, s)
+    back = og.rht16(Y, 0)  # (x D H / 4) H / 4 = x D: undo D by the signs
+    D = np.tile(np.array([-1.0 if (s >> i) & 1 else 1.0 for i in range(16)], np.float32), 4)
+    assert np.array_equal(back * D, X)
+    assert np.array_equal(Y.astype(np.float64) @ og.rht16(Wm, s).astype(np.float64).T,
+                          X.astype(np.float64) @ Wm.astype(np.float64).T)
+
+
+def test_rht16_argument_errors(lib):
+    g = 1 << 20
+    assert lib.nvfp4_rht16(g, 0, 4, 24, 0, g, None) == lib.NVFP4_ESHAPE
+    assert lib.nvfp4_rht16(g, 0, 4, 32, 1 << 16, g, None) == lib.NVFP4_EINVAL
+    assert lib.nvfp4_rht16(g, 2, 4, 32, 0, g, None) == lib.NVFP4_EINVAL
+    assert lib.nvfp4_rht16(g + 16, 0, 4, 32, 0, g, None) == lib.NVFP4_EALIGN
+    assert lib.nvfp4_rht16(None, 0, 4, 32, 0, g, None) == lib.NVFP4_EINVAL
+    assert lib.nvfp4_rht16(None, 0, 0, 32, 0, None, None) == lib.NVFP4_OK

@@ -121,3 +121,41 @@ def test_w4a4_linear_sizes_sampled_rows(nv):
                              float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
                              float(host(wq.tensor_scale)[0]))
     check(y[rows], ref, sabs, K)
+
+
+def test_rht16_bit_exact(nv):
+    """The transform against the oracle's butterflies, fp32 and bf16 inputs, bit for bit."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+    from oracle import gemm as og
+
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((37, 80)) * 3).astype(np.float32)
+    got = host(nv.rht16(torch.from_numpy(x).cuda(), 0xB16B))
+    assert np.array_equal(got.view(np.uint32), og.rht16(x, 0xB16B).view(np.uint32))
+    xb = W.to_bf16_bits(W.activations(T=64, D=3072))
+    xf = (xb.astype(np.uint32) << 16).view(np.float32)
+    got = host(nv.rht16(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda(), 0x0F0F))
+    assert np.array_equal(got.view(np.uint32), og.rht16(xf, 0x0F0F).view(np.uint32))
+
+
+def test_w4a4_with_rht(nv):
+    """Both operands transformed with the same signs, then quantized (fp32 inputs) and multiplied:
+    within the bound of the oracle's product of the transformed, quantized operands."""
+    from oracle import gemm as og
+
+    rng = np.random.default_rng(13)
+    M, N, K = 256, 512, 1024
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    Wm = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Wm.flat[rng.choice(Wm.size, Wm.size // 1000, replace=False)] *= 30.0
+    signs = int(rng.integers(0, 1 << 16))
+    xr = nv.rht16(bf16_dev(X), signs)
+    wr = nv.rht16(bf16_dev(Wm), signs)
+    xq = nv.kv_smooth_quant(xr.view(M, 1, K), False)
+    wq = nv.weight_quant_2d(wr)
+    torch.cuda.synchronize()
+    y = run_gemm(nv, xq, wq, M, N, K)
+    ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2), host(xq.scales).reshape(M, K // 16),
+                             float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
+                             float(host(wq.tensor_scale)[0]))
+    check(y, ref, sabs, K)

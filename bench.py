@@ -647,6 +647,19 @@ def row_gemm_w4a4(nv, W, torch, dev, peak):
     out = {"TFLOP/s": fl / ms / 1e9, "ms_gemm": ms, "ms_linear_step": ms_lin, "flops": fl,
            "peak_tflops": pk, "peak_source": src, "frac": fl / ms / 1e9 / pk}
 
+    # the wide weight shape of the workload: 14336 outputs from 3072 inputs
+    N2 = 14336
+    w2 = (torch.randn((N2, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    w2q = nv.weight_quant_2d(w2)
+    w2s = nv.mma_scales(w2q.scales, K, tile2d=True)
+    del w2
+    plan2 = nv.GemmPlan(M, N2, K)
+    y2 = torch.empty((M, N2), dtype=torch.bfloat16, device=dev)
+    ms2 = _time_graph(torch, lambda i: nv.gemm_w4a4(plan2, xc, xs, xq.tensor_scale, w2q.codes, w2s,
+                                                    w2q.tensor_scale, ws, out=y2), 4, 20)
+    fl2 = 2.0 * M * N2 * K
+    out["gemm_7040x14336x3072"] = {"TFLOP/s": fl2 / ms2 / 1e9, "ms": ms2, "frac": fl2 / ms2 / 1e9 / pk}
+
     # random Hadamard transform of the activation (bf16 in, fp32 out: 6 bytes per element)
     signs = int(torch.randint(0, 1 << 16, (1,), generator=gen, device=dev).item())
     xr = torch.empty((M, K), dtype=torch.float32, device=dev)

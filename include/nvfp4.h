@@ -364,7 +364,8 @@ nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales
 int64_t nvfp4_mma_scales_bytes(int64_t rows, int64_t K);
 
 /* Row-major 1-D block scales [rows][K/16] (device) -> the tensor-core layout
- * (device, nvfp4_mma_scales_bytes(rows, K) bytes, padding zeroed). */
+ * (device, nvfp4_mma_scales_bytes(rows, K) bytes, 16-byte aligned, padding
+ * zeroed). */
 nvfp4_status nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* out, void* stream);
 
 /* 16x16-tile weight scales [N/16][K/16] (device) -> per-row block scales in the

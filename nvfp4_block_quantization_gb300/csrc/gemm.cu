@@ -44,22 +44,28 @@ constexpr size_t kScalarBytes = 256;                 // alpha and beta at the fr
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-// One thread per output byte, in output order (coalesced stores); the gather
-// from the row-major input hits a few cache lines per warp.
+// One thread per output word: the four blocks of one row inside one tile sit
+// in consecutive bytes, so word w of tile (rt, ct) holds blocks 4 ct .. 4 ct + 3
+// of row 128 rt + (w % 4) * 32 + w / 4.  Stores are in output order (coalesced);
+// the gather from the row-major input is four byte loads.
 //   kTile: the input is a 16x16-tile scale grid [rows / 16][kblocks].
 template <bool kTile>
 __global__ void __launch_bounds__(256) scales_to_mma_kernel(const uint8_t* __restrict__ in, int64_t rows,
-                                                            int64_t kblocks, uint8_t* __restrict__ out,
-                                                            int64_t out_bytes) {
+                                                            int64_t kblocks, uint32_t* __restrict__ out,
+                                                            int64_t out_words) {
   const int64_t kbt = (kblocks + 3) / 4;
-  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < out_bytes; o += (int64_t)gridDim.x * blockDim.x) {
-    // invert the layout: tile, then position inside the tile
-    const int64_t tile = o >> 9, within = o & 511;
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < out_words; o += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = o >> 7;
+    const int w = (int)(o & 127);
     const int64_t rt = tile / kbt, ct = tile - rt * kbt;
-    const int64_t rr = (within >> 4) + ((within >> 2) & 3) * 32, cc = within & 3;
-    const int64_t r = rt * 128 + rr, kb = ct * 4 + cc;
-    uint8_t v = 0;
-    if (r < rows && kb < kblocks) v = kTile ? in[(r >> 4) * kblocks + kb] : in[r * kblocks + kb];
+    const int64_t r = rt * 128 + (w & 3) * 32 + (w >> 2), kb0 = ct * 4;
+    uint32_t v = 0;
+    if (r < rows) {
+      const uint8_t* src = in + (kTile ? (r >> 4) : r) * kblocks;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (kb0 + c < kblocks) v |= (uint32_t)src[kb0 + c] << (8 * c);
+    }
     out[o] = v;
   }
 }
@@ -127,11 +133,13 @@ nvfp4_status launch_scales(const uint8_t* in, int64_t rows, int64_t kblocks, boo
   if (bytes == 0) return NVFP4_OK;
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ECUDA;
-  int64_t grid = (bytes + 255) / 256;
+  const int64_t words = bytes / 4;  // a whole number of 512-byte tiles
+  int64_t grid = (words + 255) / 256;
   if (grid > (int64_t)sms * 16) grid = (int64_t)sms * 16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (tile) scales_to_mma_kernel<true><<<(unsigned)grid, 256, 0, s>>>(in, rows, kblocks, out, bytes);
-  else scales_to_mma_kernel<false><<<(unsigned)grid, 256, 0, s>>>(in, rows, kblocks, out, bytes);
+  uint32_t* o = reinterpret_cast<uint32_t*>(out);
+  if (tile) scales_to_mma_kernel<true><<<(unsigned)grid, 256, 0, s>>>(in, rows, kblocks, o, words);
+  else scales_to_mma_kernel<false><<<(unsigned)grid, 256, 0, s>>>(in, rows, kblocks, o, words);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
@@ -158,12 +166,14 @@ int64_t nvfp4_mma_scales_bytes(int64_t rows, int64_t K) {
 nvfp4_status nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t K, uint8_t* out, void* stream) {
   if (rows < 0 || K < 16 || (K % 16) != 0) return NVFP4_ESHAPE;
   if (rows > 0 && (!scales || !out)) return NVFP4_EINVAL;
+  if (!nvfp4::aligned_to(out, 16)) return NVFP4_EALIGN;
   return nvfp4::launch_scales(scales, rows, K / 16, false, out, stream);
 }
 
 nvfp4_status nvfp4_w2d_scales_to_mma(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out, void* stream) {
   if (N < 0 || (N % 16) != 0 || K < 16 || (K % 16) != 0) return NVFP4_ESHAPE;
   if (N > 0 && (!scales || !out)) return NVFP4_EINVAL;
+  if (!nvfp4::aligned_to(out, 16)) return NVFP4_EALIGN;
   return nvfp4::launch_scales(scales, N, K / 16, true, out, stream);
 }
 

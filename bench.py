@@ -686,6 +686,36 @@ def row_gemm_w4a4(nv, W, torch, dev, peak):
     y1 = nv.gemm_w4a4(plan, xrq.codes.view(M, K // 2), nv.mma_scales(xrq.scales.view(M, K // 16), K),
                       xrq.tensor_scale, wrq.codes, nv.mma_scales(wrq.scales, K, tile2d=True), wrq.tensor_scale, ws)
     out["rel_frobenius_error_vs_exact"] = {"w4a4": rel(y0), "w4a4_with_rht16": rel(y1)}
+
+    # the activation side fused (transform, quantize, scales in the tensor-core layout) against
+    # the separate calls, each followed by the GEMM with a weight prepared once
+    wr_s = nv.mma_scales(wrq.scales, K, tile2d=True)
+    aq = nv.act_quant_mma(x.view(M, K))
+    aws2 = torch.empty(nv._lib.nvfp4_act_quant_workspace_bytes(), dtype=torch.uint8, device=dev)
+    xw = nv.kv_workspace(M, 1, K, 1, dev)
+    xrq_o = nv.kv_smooth_quant(xr.view(M, 1, K), False)
+    xr_s = nv.mma_scales(xrq_o.scales.view(M, K // 16), K)
+    yy = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def fused_plain(i):
+        nv.act_quant_mma(x.view(M, K), None, workspace=aws2, out=aq)
+        nv.gemm_w4a4(plan, aq.codes, aq.scales_mma, aq.tensor_scale, wts[i % 4][0].codes, wts[i % 4][1],
+                     wts[i % 4][0].tensor_scale, ws, out=ys[i % 4])
+
+    def composed_rht(i):
+        nv.rht16(x.view(M, K), signs, out=xr)
+        nv.kv_smooth_quant(xr.view(M, 1, K), False, workspace=xw, out=xrq_o)
+        nv.mma_scales(xrq_o.scales.view(M, K // 16), K, out=xr_s)
+        nv.gemm_w4a4(plan, xrq_o.codes.view(M, K // 2), xr_s, xrq_o.tensor_scale, wrq.codes, wr_s,
+                     wrq.tensor_scale, ws, out=yy)
+
+    def fused_rht(i):
+        nv.act_quant_mma(x.view(M, K), signs, workspace=aws2, out=aq)
+        nv.gemm_w4a4(plan, aq.codes, aq.scales_mma, aq.tensor_scale, wrq.codes, wr_s, wrq.tensor_scale, ws, out=yy)
+
+    out["linear_step_ms"] = {"quantize+scales+gemm": ms_lin, "fused_quant+gemm": _time_graph(torch, fused_plain, 8, 20),
+                             "rht+quantize+scales+gemm": _time_graph(torch, composed_rht, 8, 20),
+                             "fused_rht_quant+gemm": _time_graph(torch, fused_rht, 8, 20)}
     return out
 
 

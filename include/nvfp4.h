@@ -385,6 +385,24 @@ nvfp4_status nvfp4_w2d_scales_to_mma(const uint8_t* scales, int64_t N, int64_t K
 nvfp4_status nvfp4_rht16(const void* x, nvfp4_in_dtype dt, int64_t rows, int64_t K, uint32_t signs, float* out,
                          void* stream);
 
+/* The activation side of a W4A4 layer in one call pair: optionally the
+ * transform above (use_rht = 1, with `signs`), then the 1-D Four-Over-Six
+ * quantizer, with the block scales written straight into the tensor-core
+ * layout.  Bit for bit the same as nvfp4_rht16 (if used), then
+ * nvfp4_kv_smooth_quant (H = 1, D = K, no smoothing) on the fp32 result (on x
+ * itself without the transform), then nvfp4_scales_to_mma; the transformed
+ * values never leave registers.
+ *   x           device [M][K] bf16, 32-byte aligned, M >= 1, K % 16 == 0
+ *   codes       device [M][K/2]
+ *   scales_mma  device, nvfp4_mma_scales_bytes(M, K) bytes, padding written
+ *   tensor_scale, dev_status  as nvfp4_kv_smooth_quant
+ *   workspace   device, nvfp4_act_quant_workspace_bytes(), 256-byte aligned,
+ *               no zero-fill needed (one amax partial per CTA) */
+size_t nvfp4_act_quant_workspace_bytes(void);
+nvfp4_status nvfp4_act_quant_mma(const void* x, int64_t M, int64_t K, int use_rht, uint32_t signs, uint8_t* codes,
+                                 uint8_t* scales_mma, float* tensor_scale, int* dev_status, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Device workspace of nvfp4_gemm_w4a4 (256-byte aligned; no zero-fill needed). */
 size_t nvfp4_gemm_workspace_bytes(void);
 

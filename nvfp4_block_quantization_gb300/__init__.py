@@ -21,7 +21,8 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "rht16", "GemmPlan", "gemm_w4a4",
+    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "rht16", "ActQuantized", "act_quant_mma", "GemmPlan",
+    "gemm_w4a4",
     "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
     "weight_dequant_2d", "load_library",
 ]
@@ -329,6 +330,35 @@ def rht16(x, signs: int, out=None, stream=None):
     if out is None:
         out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     _lib.check(_lib.nvfp4_rht16(_ptr(x), _dt(x), rows, K, int(signs), _ptr(out), _stream(stream)), "nvfp4_rht16")
+    return out
+
+
+class ActQuantized(NamedTuple):
+    codes: "torch.Tensor"         # uint8 [M, K/2]
+    scales_mma: "torch.Tensor"    # uint8, tensor-core layout
+    tensor_scale: "torch.Tensor"  # float32 [1]
+    status: "torch.Tensor"        # int32 [1]
+
+
+def act_quant_mma(x, rht_signs: Optional[int] = None, workspace=None, out: Optional[ActQuantized] = None,
+                  stream=None) -> ActQuantized:
+    """Activation x [M, K] bf16 -> NVFP4 codes and tensor-core-layout scales in one call pair
+    (``nvfp4_act_quant_mma``), with the random Hadamard transform first when ``rht_signs`` is given."""
+    torch = _torch()
+    _check_cuda(x)
+    M, K = x.shape
+    if out is None:
+        out = ActQuantized(torch.empty((M, K // 2), dtype=torch.uint8, device=x.device),
+                           torch.empty(max(_lib.nvfp4_mma_scales_bytes(M, K), 16), dtype=torch.uint8,
+                                       device=x.device),
+                           torch.empty(1, dtype=torch.float32, device=x.device),
+                           torch.empty(1, dtype=torch.int32, device=x.device))
+    if workspace is None:
+        workspace = torch.empty(_lib.nvfp4_act_quant_workspace_bytes(), dtype=torch.uint8, device=x.device)
+    st = _lib.nvfp4_act_quant_mma(_ptr(x), M, K, 0 if rht_signs is None else 1, int(rht_signs or 0),
+                                  _ptr(out.codes), _ptr(out.scales_mma), _ptr(out.tensor_scale), _ptr(out.status),
+                                  _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_act_quant_mma")
     return out
 
 

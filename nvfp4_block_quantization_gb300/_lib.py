@@ -38,6 +38,8 @@ EXPORTS = (
     "nvfp4_scales_to_mma",
     "nvfp4_w2d_scales_to_mma",
     "nvfp4_rht16",
+    "nvfp4_act_quant_workspace_bytes",
+    "nvfp4_act_quant_mma",
     "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm_plan_create",
     "nvfp4_gemm_plan_destroy",
@@ -148,6 +150,10 @@ def load(path: str | None = None):
     lib.nvfp4_w2d_scales_to_mma.restype = i32
     lib.nvfp4_rht16.argtypes = [vp, i32, i64, i64, ctypes.c_uint32, vp, vp]
     lib.nvfp4_rht16.restype = i32
+    lib.nvfp4_act_quant_workspace_bytes.argtypes = []
+    lib.nvfp4_act_quant_workspace_bytes.restype = sz
+    lib.nvfp4_act_quant_mma.argtypes = [vp, i64, i64, i32, ctypes.c_uint32, vp, vp, vp, vp, vp, sz, vp]
+    lib.nvfp4_act_quant_mma.restype = i32
     lib.nvfp4_gemm_workspace_bytes.argtypes = []
     lib.nvfp4_gemm_workspace_bytes.restype = sz
     lib.nvfp4_gemm_plan_create.argtypes = [i64, i64, i64, P(vp)]
@@ -257,6 +263,16 @@ def nvfp4_w2d_scales_to_mma(scales, N, K, out, stream):
 
 def nvfp4_rht16(x, dt, rows, K, signs, out, stream):
     return load().nvfp4_rht16(x, dt, rows, K, signs, out, stream)
+
+
+def nvfp4_act_quant_workspace_bytes():
+    return load().nvfp4_act_quant_workspace_bytes()
+
+
+def nvfp4_act_quant_mma(x, M, K, use_rht, signs, codes, scales_mma, tensor_scale, dev_status, workspace,
+                        workspace_bytes, stream):
+    return load().nvfp4_act_quant_mma(x, M, K, use_rht, signs, codes, scales_mma, tensor_scale, dev_status,
+                                      workspace, workspace_bytes, stream)
 
 
 def nvfp4_gemm_workspace_bytes():

@@ -26,6 +26,7 @@
 
 #include "nvfp4.h"
 #include "common.cuh"
+#include "rht16.cuh"
 
 struct nvfp4_gemm_plan {
   int64_t M, N, K;
@@ -70,13 +71,8 @@ __global__ void __launch_bounds__(256) scales_to_mma_kernel(const uint8_t* __res
   }
 }
 
-// Random Hadamard transform of 16-element blocks along the rows: one thread per
-// block.  The block x (widened exactly to fp32) has its signs flipped where the
-// bitmask `signs` has a 1 (bit i for element i), then the in-place radix-2
-// Walsh-Hadamard butterflies run with strides 1, 2, 4, 8 (each stage one fp32
-// add and one fp32 subtract per pair: (a, b) -> (a + b, a - b)), and the result
-// is scaled by 1/4 (exact).  So y = (x D) H / 4 with H the 16-point Sylvester
-// Hadamard matrix and D = diag(signs): an orthogonal transform.
+// Random Hadamard transform of 16-element blocks along the rows (rht16_block):
+// one thread per block, widened exactly to fp32 first.
 template <bool kBF16>
 __global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ x, int64_t nblocks, uint32_t signs,
                                                     float* __restrict__ out) {
@@ -94,23 +90,10 @@ __global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ x, 
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(w[i]);
     }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if ((signs >> i) & 1u) v[i] = -v[i];
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if ((i & h) == 0) {
-          const float a = v[i], c = v[i + h];
-          v[i] = __fadd_rn(a, c);
-          v[i + h] = __fsub_rn(a, c);
-        }
+    rht16_block(v, signs);
     float4* o = reinterpret_cast<float4*>(out + b * 16);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      o[q] = make_float4(__fmul_rn(v[4 * q], 0.25f), __fmul_rn(v[4 * q + 1], 0.25f), __fmul_rn(v[4 * q + 2], 0.25f),
-                         __fmul_rn(v[4 * q + 3], 0.25f));
+    for (int q = 0; q < 4; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
 }
 

@@ -159,3 +159,55 @@ def test_w4a4_with_rht(nv):
                              float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
                              float(host(wq.tensor_scale)[0]))
     check(y, ref, sabs, K)
+
+
+def unswizzle(buf: np.ndarray, rows: int, KB: int) -> np.ndarray:
+    """Block scales [rows][KB] read back out of the tensor-core layout."""
+    kbt = (KB + 3) // 4
+    r = np.arange(rows)[:, None]
+    kb = np.arange(KB)[None, :]
+    off = ((r // 128) * kbt + kb // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4
+    return buf[off]
+
+
+@pytest.mark.parametrize("rht", [None, 0x9C3A], ids=["plain", "rht"])
+@pytest.mark.parametrize("shape", [(200, 80), (7040, 3072)], ids=["200x80", "7040x3072"])
+def test_act_quant_mma_equals_composition(nv, rht, shape):
+    """The fused activation quantizer gives the separate calls' bits: codes, the whole scale
+    buffer (padding included), tensor scale, status."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    M, K = shape
+    X = W.activations(T=M, D=K, seed=5300 + K)
+    X[:, ::97] *= 20.0  # outlier channels
+    xb = bf16_dev(X)
+    fused = nv.act_quant_mma(xb, rht)
+    src = nv.rht16(xb, rht) if rht is not None else xb
+    q = nv.kv_smooth_quant(src.view(M, 1, K), False)
+    sm = nv.mma_scales(q.scales.view(M, K // 16), K)
+    torch.cuda.synchronize()
+    assert int(host(fused.status)[0]) == 0 and int(host(q.status)[0]) == 0
+    assert torch.equal(fused.codes, q.codes.view(M, K // 2))
+    n = nv._lib.nvfp4_mma_scales_bytes(M, K)
+    assert torch.equal(fused.scales_mma[:n], sm[:n])
+    assert torch.equal(fused.tensor_scale.view(torch.int32), q.tensor_scale.view(torch.int32))
+
+
+@pytest.mark.parametrize("rht", [None, 0x2F51], ids=["plain", "rht"])
+def test_act_quant_mma_matches_oracle(nv, oracle, rht):
+    """Against the oracle's composition: (transform,) 1-D quantization, bit for bit."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+    from oracle import gemm as og
+
+    M, K = 150, 208
+    X = W.activations(T=M, D=K, seed=5400)
+    X[:, 5] *= 40.0
+    bits = W.to_bf16_bits(X)
+    fused = nv.act_quant_mma(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda(), rht)
+    torch.cuda.synchronize()
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)
+    src = og.rht16(xf, rht) if rht is not None else bits
+    ref = oracle.kv_smooth_quant(src.reshape(M, 1, K), smooth=False)
+    assert np.array_equal(host(fused.codes), ref["codes"].reshape(M, K // 2))
+    assert np.array_equal(unswizzle(host(fused.scales_mma), M, K // 16), ref["scales"].reshape(M, K // 16))
+    assert np.float32(host(fused.tensor_scale)[0]).view(np.uint32) == np.float32(ref["g"]).view(np.uint32)

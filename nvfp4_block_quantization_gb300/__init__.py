@@ -370,10 +370,17 @@ class GemmPlan:
         self._p = ctypes.c_void_p()
         _lib.check(_lib.nvfp4_gemm_plan_create(M, N, K, self._p), "nvfp4_gemm_plan_create")
 
+    def close(self):
+        """Free the plan now (it is also freed when the object is collected)."""
+        p, self._p = getattr(self, "_p", None), None
+        if p is not None and p.value:
+            _lib.nvfp4_gemm_plan_destroy(p)
+
     def __del__(self):
-        if getattr(self, "_p", None) is not None and self._p.value:
-            _lib.nvfp4_gemm_plan_destroy(self._p)
-            self._p = None
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may already be unloaded
+            pass
 
 
 def gemm_workspace(device=None):

@@ -58,7 +58,7 @@ def parse():
     p.add_argument("--no-rows", action="store_true", help="skip the secondary rows (dequant, weights, 30 layers)")
     p.add_argument("--rows", nargs="+", default=None, metavar="ROW",
                    help="run only these secondary rows: kv_write_30_layers kv_cache_read_dequant kv_cache_view_gather "
-                        "gemm_w4a4 weight_quant_2d activation_quant_1d k_only_smooth_quant")
+                        "kv_attention_decode gemm_w4a4 weight_quant_2d activation_quant_1d k_only_smooth_quant")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=30)
     return p.parse_args()
@@ -594,6 +594,47 @@ def row_kv_cache_view_gather(nv, W, torch, dev, peak):
             "view_frames": 21, "slots_per_pool": 5}
 
 
+def row_kv_attention_decode(nv, W, torch, dev, peak):
+    """Attention reading the NVFP4 cache: 1 and 4 query tokens per head over the 21-frame view (3 sink
+    + 18 rolling frames x 880 tokens, 24 heads x 128) of two layers' K and V pools, K and V dequantized
+    in registers.  Bytes: the view's K and V codes and scales (0.5625 B per cached element each)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3200)
+    F, Lf = 8, 880
+    layers = []
+    for layer in range(2):
+        cache = nv.KvCache(F, Lf, 3, 3, 18)
+        pk = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=True, device=dev)
+        pv = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=False, device=dev)
+        for c in range(5):
+            slot = cache.append()
+            k = _chunk_k_device(torch, gen, dev)
+            v = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev).to(torch.bfloat16)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            nv.kv_smooth_quant_batched([k, v], [True, False],
+                                       outs=[pk.slot_outputs(cache, slot, st), pv.slot_outputs(cache, slot, st)],
+                                       status=st)
+            del k, v
+        fi, fr, fs = cache.view()
+        layers.append((pk, pv, fr, fs))
+    n_tok = 21 * Lf
+    b = 2 * n_tok * HEADS * HEAD_DIM * (0.5 + 1.0 / 16.0)
+    out = {"bytes": b, "view_tokens": n_tok}
+    for n_q in (1, 4):
+        q = torch.randn((n_q, HEADS, HEAD_DIM), generator=gen, device=dev)
+        wsp = torch.empty(nv._lib.nvfp4_kv_attention_workspace_bytes(21, Lf, HEADS, HEAD_DIM, n_q),
+                          dtype=torch.uint8, device=dev)
+        o = torch.empty((n_q, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+
+        def call(i):
+            pk, pv, fr, fs = layers[i % 2]
+            nv.kv_attention_decode(q, pk, pv, fr, fs, Lf, HEAD_DIM ** -0.5, workspace=wsp, out=o)
+
+        ms = _time_graph(torch, call, 8, 20)
+        out[f"n_q={n_q}"] = {"ms": ms, "GB/s": b / ms / 1e6, "frac": b / ms / 1e6 / peak}
+    return out
+
+
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates of the part
 
@@ -765,7 +806,8 @@ def row_k_only_smooth_quant(nv, W, torch, dev, peak):
 
 
 ROWS = {"kv_write_30_layers": row_kv_write_30_layers, "kv_cache_read_dequant": row_kv_cache_read_dequant,
-        "kv_cache_view_gather": row_kv_cache_view_gather, "gemm_w4a4": row_gemm_w4a4,
+        "kv_cache_view_gather": row_kv_cache_view_gather, "kv_attention_decode": row_kv_attention_decode,
+        "gemm_w4a4": row_gemm_w4a4,
         "weight_quant_2d": row_weight_quant_2d, "activation_quant_1d": row_activation_quant_1d,
         "k_only_smooth_quant": row_k_only_smooth_quant}
 

@@ -270,6 +270,29 @@ nvfp4_status nvfp4_kv_gather_dequant(const uint8_t* codes_pool, const uint8_t* s
                                      const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
                                      void* out_bf16, void* stream);
 
+/* Attention that reads the cache (inference steps 7 and 9): n_q query tokens
+ * per head attend over one view, K and V dequantized in registers from their
+ * pools, so the cache is read at 0.5625 bytes per element.  Per view token t
+ * (pool row frame_row[t / L_f] + t % L_f, slot frame_meta[t / L_f]) and channel d:
+ *   k = fl(fl(Q * fl(E * k_g[slot])) + k_mean[slot][h][d])   (k_mean may be NULL)
+ *   v = fl(Q * fl(E * v_g[slot]))
+ *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t
+ * scores and the softmax in fp32 (split over 256-token ranges, merged exactly
+ * as a softmax of the union), out fp32.
+ *   q          device [n_q][H][D] fp32, n_q in 1..4, D 64 or 128
+ *   k_*, v_*   the pools of nvfp4_kv_gather_dequant (pool_rows rows, n_meta slots;
+ *              codes 16-byte aligned, k_mean 16-byte aligned)
+ *   frame_row, frame_meta  HOST arrays of n_frames (<= NVFP4_MAX_VIEW_FRAMES)
+ *              entries, validated before anything is enqueued (NVFP4_ESHAPE)
+ *   workspace  device, nvfp4_kv_attention_workspace_bytes(...), 256-byte aligned */
+size_t nvfp4_kv_attention_workspace_bytes(int n_frames, int64_t tokens_per_frame, int H, int D, int n_q);
+nvfp4_status nvfp4_kv_attention_decode(const float* q, int n_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                                       const float* k_g, const float* k_mean, const uint8_t* v_codes,
+                                       const uint8_t* v_scales, const float* v_g, int64_t pool_rows, int n_meta,
+                                       const int64_t* frame_row, const int* frame_meta, int n_frames,
+                                       int64_t tokens_per_frame, int H, int D, float scale, float* out,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weights with 16x16 2-D blocks (LongLive-2.0 summary page, training        */
 /* pipeline step 4: "2-D block scales for weights").                         */

@@ -21,7 +21,7 @@ from ._lib import NVFP4_IN_BF16, NVFP4_IN_FP32, NVFP4Error, nvfp4_kv_job, nvfp4_
 __all__ = [
     "NVFP4Error", "KvQuantized", "W2dQuantized", "kv_workspace", "kv_smooth_quant", "kv_smooth_quant_batched",
     "kv_stats_batched", "kv_quant_batched",
-    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "mma_scales", "rht16", "ActQuantized", "act_quant_mma", "GemmPlan",
+    "kv_dequant", "KvCache", "KvCachePool", "kv_gather_dequant", "kv_attention_decode", "mma_scales", "rht16", "ActQuantized", "act_quant_mma", "GemmPlan",
     "gemm_w4a4",
     "w2d_workspace", "weight_quant_2d", "w2d_batched_workspace", "weight_quant_2d_batched",
     "weight_dequant_2d", "load_library",
@@ -400,6 +400,32 @@ def gemm_w4a4(plan: GemmPlan, x_codes, x_scales_mma, x_tensor_scale, w_codes, w_
                               _ptr(w_scales_mma), _ptr(w_tensor_scale), _ptr(out), _ptr(workspace),
                               workspace.numel(), _stream(stream))
     _lib.check(st, "nvfp4_gemm_w4a4")
+    return out
+
+
+def kv_attention_decode(q, k_pool: KvCachePool, v_pool: KvCachePool, frame_row, frame_slot, tokens_per_frame: int,
+                        scale: float, workspace=None, out=None, stream=None):
+    """Attention of q [n_q, H, D] (fp32) over a cache view read straight from the NVFP4 pools
+    (``nvfp4_kv_attention_decode``); K's means are re-added when its pool has them.  fp32 [n_q, H, D]."""
+    import numpy as np
+
+    torch = _torch()
+    _check_cuda(q, k_pool.codes, v_pool.codes)
+    n_q, H, D = q.shape
+    fr = np.ascontiguousarray(frame_row, dtype=np.int64)
+    fs = np.ascontiguousarray(frame_slot, dtype=np.int32)
+    n = int(fr.shape[0])
+    if workspace is None:
+        workspace = torch.empty(max(_lib.nvfp4_kv_attention_workspace_bytes(n, tokens_per_frame, H, D, n_q), 256),
+                                dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((n_q, H, D), dtype=torch.float32, device=q.device)
+    st = _lib.nvfp4_kv_attention_decode(_ptr(q), n_q, _ptr(k_pool.codes), _ptr(k_pool.scales), _ptr(k_pool.g),
+                                        _ptr(k_pool.mean), _ptr(v_pool.codes), _ptr(v_pool.scales), _ptr(v_pool.g),
+                                        k_pool.codes.shape[0], int(k_pool.g.numel()), fr.ctypes.data,
+                                        fs.ctypes.data, n, tokens_per_frame, H, D, float(scale), _ptr(out),
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_kv_attention_decode")
     return out
 
 

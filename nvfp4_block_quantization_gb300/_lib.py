@@ -34,6 +34,8 @@ EXPORTS = (
     "nvfp4_kvcache_new_shot",
     "nvfp4_kvcache_view",
     "nvfp4_kv_gather_dequant",
+    "nvfp4_kv_attention_workspace_bytes",
+    "nvfp4_kv_attention_decode",
     "nvfp4_mma_scales_bytes",
     "nvfp4_scales_to_mma",
     "nvfp4_w2d_scales_to_mma",
@@ -142,6 +144,11 @@ def load(path: str | None = None):
     lib.nvfp4_kvcache_view.restype = i32
     lib.nvfp4_kv_gather_dequant.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.nvfp4_kv_gather_dequant.restype = i32
+    lib.nvfp4_kv_attention_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
+    lib.nvfp4_kv_attention_workspace_bytes.restype = sz
+    lib.nvfp4_kv_attention_decode.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32,
+                                              i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.nvfp4_kv_attention_decode.restype = i32
     lib.nvfp4_mma_scales_bytes.argtypes = [i64, i64]
     lib.nvfp4_mma_scales_bytes.restype = i64
     lib.nvfp4_scales_to_mma.argtypes = [vp, i64, i64, vp, vp]
@@ -247,6 +254,18 @@ def nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_row
                             n_frames, tokens_per_frame, H, D, out_bf16, stream):
     return load().nvfp4_kv_gather_dequant(codes_pool, scales_pool, g_pool, mean_pool, pool_rows, n_meta, frame_row,
                                           frame_meta, n_frames, tokens_per_frame, H, D, out_bf16, stream)
+
+
+def nvfp4_kv_attention_workspace_bytes(n_frames, tokens_per_frame, H, D, n_q):
+    return load().nvfp4_kv_attention_workspace_bytes(n_frames, tokens_per_frame, H, D, n_q)
+
+
+def nvfp4_kv_attention_decode(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g, pool_rows, n_meta,
+                              frame_row, frame_meta, n_frames, tokens_per_frame, H, D, scale, out, workspace,
+                              workspace_bytes, stream):
+    return load().nvfp4_kv_attention_decode(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g,
+                                            pool_rows, n_meta, frame_row, frame_meta, n_frames, tokens_per_frame,
+                                            H, D, scale, out, workspace, workspace_bytes, stream)
 
 
 def nvfp4_mma_scales_bytes(rows, K):

@@ -212,3 +212,25 @@ def test_gather_dequant_argument_errors(lib):
     assert call(codes=None) == lib.NVFP4_EINVAL
     assert call(out=dev + 8) == lib.NVFP4_EALIGN
     assert call(n=0) == lib.NVFP4_OK  # nothing to do, nothing enqueued
+
+
+def test_attention_argument_errors(lib):
+    """Checks that return before any CUDA call (fake device addresses are never touched)."""
+    dev = 1 << 20
+    fr = np.array([0, 16], np.int64)
+    fm = np.array([0, 1], np.int32)
+
+    def call(n_q=1, D=64, fr_=fr, fm_=fm, n=None, pool_rows=64, n_meta=2, kmean=dev, ws=dev, wsb=1 << 20):
+        n = len(fr_) if n is None else n
+        return lib.nvfp4_kv_attention_decode(dev, n_q, dev, dev, dev, kmean, dev, dev, dev, pool_rows, n_meta,
+                                             fr_.ctypes.data, fm_.ctypes.data, n, 16, 2, D, 0.125, dev, ws, wsb, None)
+
+    assert call(n_q=0) == lib.NVFP4_ESHAPE and call(n_q=5) == lib.NVFP4_ESHAPE
+    assert call(D=96) == lib.NVFP4_ESHAPE
+    assert call(fr_=np.array([0, 49], np.int64)) == lib.NVFP4_ESHAPE  # frame past the pool
+    assert call(fm_=np.array([0, 2], np.int32)) == lib.NVFP4_ESHAPE   # slot past the metadata
+    assert call(n=0) == lib.NVFP4_ESHAPE
+    assert call(kmean=dev + 4) == lib.NVFP4_EALIGN
+    assert call(ws=None) == lib.NVFP4_EWORKSPACE and call(wsb=16) == lib.NVFP4_EWORKSPACE
+    # 2 heads x 1 split x 1 query x (64 + 2) floats = 528 bytes, rounded up to 256-byte units
+    assert lib.nvfp4_kv_attention_workspace_bytes(2, 16, 2, 64, 1) == 768

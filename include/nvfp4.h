@@ -23,8 +23,11 @@
  *
  * Conventions for every entry point:
  *   - Device pointers name GPU global memory owned by the caller; the library
- *     never allocates, frees, synchronizes or prints, and keeps no mutable
- *     global state (it is safe to call from several host threads).
+ *     never allocates device memory, never frees, synchronizes or prints, and
+ *     keeps no mutable global state (it is safe to call from several host
+ *     threads).  Two entry points say otherwise where they are declared: the
+ *     GEMM plan is a host object the library allocates for the caller, and
+ *     nvfp4_weight_quant_2d_static uses a scratch array inside the library.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously; outputs are valid once the stream
  *     reaches that point.

@@ -9,10 +9,13 @@
 // over the global sink, the shot sink and the rolling frames.
 //
 // Per view token t (pool row frame_row[t / L_f] + t % L_f, slot
-// frame_slot[t / L_f]) and channel d of head h:
-//   k = fl(fl(Q_k * fl(E_k * g_k[slot])) + mean[slot][h][d]),
-//   v = fl(Q_v * fl(E_v * g_v[slot])),
-// s_i(t) = scale * sum_d q_i[h][d] k_d (fp32), and o_i = sum_t softmax_t(s_i) v_t.
+// frame_slot[t / L_f]) and channel d of head h, with S = fl(E * g[slot]) the
+// scale of d's 16-channel block:
+//   k = Q_k S_k + mean[slot][h][d],  v = Q_v S_v,
+// s_i(t) = scale * q_i[h] . k and o_i = sum_t softmax_t(s_i) v_t, in fp32.  The
+// block scale is common to the block's 16 channels, so q . k over a block is
+// evaluated as S_k (q . Q_k) + q . mean (the second sum once per slot), and p v as
+// (p S_v) Q_v: the same values up to fp32 rounding order.
 //
 // Split-KV: CTA (h, s) takes the view tokens [s R, (s + 1) R) of head h; a group
 // of D / 16 lanes owns a few tokens per step (one 16-channel scale block per lane
@@ -40,19 +43,13 @@ struct AttnView {
   int meta[NVFP4_MAX_VIEW_FRAMES];
 };
 
-// Sixteen channels of one token (one scale block) from its 8 code bytes: Q * S (+ mean).
-template <bool kMean>
-__device__ __forceinline__ void dequant16(uint2 codes, float S, const float (&mu)[16], float out[16]) {
+// The E2M1 values of one token's 16-channel block (one scale block) from its 8 code bytes.
+__device__ __forceinline__ void decode16(uint2 codes, float out[16]) {
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
     const uint32_t q = e2m1x2_to_f16x2(((p < 4 ? codes.x : codes.y) >> (8 * (p & 3))) & 0xFFu);
-    float a = __fmul_rn(f16lo(q), S), b = __fmul_rn(f16hi(q), S);
-    if (kMean) {
-      a = __fadd_rn(a, mu[2 * p]);
-      b = __fadd_rn(b, mu[2 * p + 1]);
-    }
-    out[2 * p] = a;
-    out[2 * p + 1] = b;
+    out[2 * p] = f16lo(q);
+    out[2 * p + 1] = f16hi(q);
   }
 }
 
@@ -92,9 +89,9 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
   int64_t fend = -1, delta = 0;
   int slot = -1, mslot = -1;
   float gk = 0.0f, gv = 0.0f;
-  float mu[16];
+  float cq[NQ];  // sum over this lane's 16 channels of q_i * mean (K's means of the current slot)
 #pragma unroll
-  for (int j = 0; j < 16; ++j) mu[j] = 0.0f;
+  for (int i = 0; i < NQ; ++i) cq[i] = 0.0f;
   for (int64_t t0 = t_begin + (int64_t)warp * TPW * U; t0 < t_end; t0 += (int64_t)W * TPW * U) {
     uint2 kcode[U], vcode[U];
     uint32_t ke[U], ve[U];
@@ -124,7 +121,7 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
     // group), the online softmax update, dequantize V and accumulate
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float sc[NQ], kd[16], vd[16];
+      float sc[NQ], kq[16], vq[16];
 #pragma unroll
       for (int i = 0; i < NQ; ++i) sc[i] = 0.0f;
       if (on[u]) {
@@ -133,23 +130,31 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
           gk = __ldg(kg + mslot);
           gv = __ldg(vg + mslot);
           if (kmean) {
+            float mu[16];
             const float4* mp = reinterpret_cast<const float4*>(kmean + (size_t)mslot * C + (size_t)h * D + 16 * gl);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               const float4 a = __ldg(mp + k4);
               mu[4 * k4] = a.x; mu[4 * k4 + 1] = a.y; mu[4 * k4 + 2] = a.z; mu[4 * k4 + 3] = a.w;
             }
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {
+              float a = 0.0f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) a = __fmaf_rn(qv[i][j], mu[j], a);
+              cq[i] = a;
+            }
           }
         }
+        // q . k over the block = S_k * (q . Q_k) + q . mean: the scale is common to the block
         const float Sk = __fmul_rn(e4m3_value(ke[u]), gk);
-        if (kmean) dequant16<true>(kcode[u], Sk, mu, kd);
-        else dequant16<false>(kcode[u], Sk, mu, kd);
+        decode16(kcode[u], kq);
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
           float acc = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc = __fmaf_rn(qv[i][j], kd[j], acc);
-          sc[i] = acc;
+          for (int j = 0; j < 16; ++j) acc = __fmaf_rn(qv[i][j], kq[j], acc);
+          sc[i] = __fmaf_rn(acc, Sk, cq[i]);
         }
       }
 #pragma unroll
@@ -157,7 +162,9 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
 #pragma unroll
         for (int off = G / 2; off > 0; off >>= 1) sc[i] += __shfl_xor_sync(0xffffffffu, sc[i], off);
       if (on[u]) {
-        dequant16<false>(vcode[u], __fmul_rn(e4m3_value(ve[u]), gv), mu, vd);
+        // p * v = (p * S_v) * Q_v: the scale is folded into the weight
+        const float Sv = __fmul_rn(e4m3_value(ve[u]), gv);
+        decode16(vcode[u], vq);
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
           const float sv = __fmul_rn(sc[i], scale);
@@ -170,8 +177,9 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
           }
           const float p = __expf(sv - m[i]);
           l[i] = __fadd_rn(l[i], p);
+          const float pS = __fmul_rn(p, Sv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o[i][j] = __fmaf_rn(p, vd[j], o[i][j]);
+          for (int j = 0; j < 16; ++j) o[i][j] = __fmaf_rn(pS, vq[j], o[i][j]);
         }
       }
     }

@@ -1,13 +1,14 @@
 """GPU: attention over the NVFP4 cache (nvfp4_kv_attention_decode) against the oracle.
 
 Chunks are quantized into pool slots by the cache manager and the quantizer; queries
-attend over each chunk's view.  The GPU evaluates scores and the softmax in fp32 (each
-lane a fused chain over 8 channels, a shuffle tree over the token's lanes, an online
-softmax over at most 256 tokens per split, then exact merging), so each output obeys
+attend over each chunk's view.  The GPU evaluates scores and the softmax in fp32: per
+lane and 16-channel block, a fused chain over q . Q_k, times the block scale, plus the
+slot's q . mean (itself a 16-term chain); a shuffle tree over the token's lanes; an online
+softmax over at most 256 tokens per split; then exact merging.  So each output obeys
     |o - o_ref| <= Vmax * (64 * 2^-24 * A + 1e-5)
-with A = max_t |scale| sum_d |q_d k_td| and Vmax = max |v| of the head, both from the
-oracle: a score error of at most (8 + log2 G + 1) units of 2^-24 relative to A moves each
-softmax weight by at most twice that, and 1e-5 covers the fast exponential and the
+with A = max_t |scale| sum_d |q_d| (|Q S|_td + |mean_d|) and Vmax = max |v| of the head,
+both from the oracle: a score error of at most about 23 units of 2^-24 relative to A moves
+each softmax weight by at most twice that, and 1e-5 covers the fast exponential and the
 fp32 sums of at most a few hundred terms.
 """
 import numpy as np
@@ -63,10 +64,15 @@ def reference(oracle_attn, cache, pk, pv, q, scale):
     L = cache.state.tokens_per_frame
     rows = np.concatenate([np.arange(r, r + L) for r in fr])
     slot_of = np.repeat(fs, L)
-    k = oracle_attn.dequant_fp32(host(pk.codes)[rows], host(pk.scales)[rows], host(pk.g)[slot_of],
-                                 host(pk.mean)[slot_of])
+    mean = host(pk.mean)[slot_of]
+    k0 = oracle_attn.dequant_fp32(host(pk.codes)[rows], host(pk.scales)[rows], host(pk.g)[slot_of])
+    k = oracle_attn.dequant_fp32(host(pk.codes)[rows], host(pk.scales)[rows], host(pk.g)[slot_of], mean)
     v = oracle_attn.dequant_fp32(host(pv.codes)[rows], host(pv.scales)[rows], host(pv.g)[slot_of])
-    return (fr, fs) + oracle_attn.attention_decode(q, k, v, scale)
+    out, _, Vmax = oracle_attn.attention_decode(q, k, v, scale)
+    # the scale of the score's rounding: |scale| sum_d |q_d| (|Q S| + |mean|), worst token
+    parts = np.abs(k0.astype(np.float64)) + np.abs(mean.astype(np.float64))
+    A = np.einsum("ihd,thd->iht", np.abs(q.astype(np.float64)), parts).max(axis=2) * abs(scale)
+    return fr, fs, out, A, Vmax
 
 
 def check(out, ref, A, Vmax):

@@ -276,12 +276,13 @@ nvfp4_status nvfp4_kv_gather_dequant(const uint8_t* codes_pool, const uint8_t* s
 /* Attention that reads the cache (inference steps 7 and 9): n_q query tokens
  * per head attend over one view, K and V dequantized in registers from their
  * pools, so the cache is read at 0.5625 bytes per element.  Per view token t
- * (pool row frame_row[t / L_f] + t % L_f, slot frame_meta[t / L_f]) and channel d:
- *   k = fl(fl(Q * fl(E * k_g[slot])) + k_mean[slot][h][d])   (k_mean may be NULL)
- *   v = fl(Q * fl(E * v_g[slot]))
+ * (pool row frame_row[t / L_f] + t % L_f, slot frame_meta[t / L_f]) and channel d,
+ * with S = fl(E * g[slot]) the scale of d's 16-channel block:
+ *   k = Q S_k + k_mean[slot][h][d]   (k_mean may be NULL),   v = Q S_v
  *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t
- * scores and the softmax in fp32 (split over 256-token ranges, merged exactly
- * as a softmax of the union), out fp32.
+ * all in fp32: over each block q . k is taken as S_k (q . Q) + q . mean and p v
+ * as (p S_v) Q; the softmax is online over 256-token ranges, merged exactly as a
+ * softmax of the union; out fp32.
  *   q          device [n_q][H][D] fp32, n_q in 1..4, D 64 or 128
  *   k_*, v_*   the pools of nvfp4_kv_gather_dequant (pool_rows rows, n_meta slots;
  *              codes 16-byte aligned, k_mean 16-byte aligned)

@@ -1,0 +1,68 @@
+"""Pins of the attention reference (``oracle/attention.py``) without a GPU.
+
+- Its fp32 dequant, rounded to bf16, is the C oracle's cache read (``kv_dequant``), bit
+  for bit: two independent statements of the same formula.
+- Closed forms of softmax attention: identical keys give the plain mean of V; one key
+  far ahead of the others gives that token's V; adding a constant to every score
+  changes nothing.
+"""
+import numpy as np
+
+from oracle import attention as oa
+
+
+def bf16_rne(x: np.ndarray) -> np.ndarray:
+    """torch's round-to-nearest-even cast to bf16, as bit patterns."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_dequant_matches_the_c_oracle(oracle):
+    rng = np.random.default_rng(4)
+    T, H, D = 40, 3, 32
+    x = (rng.standard_normal((T, H, D)) * 2 + rng.standard_normal((1, H, D)) * 5).astype(np.float32)
+    q = oracle.kv_smooth_quant(x, smooth=True)
+    g = np.full(T, q["g"], np.float32)
+    mean = np.broadcast_to(q["mean"], (T, H, D))
+    v32 = oa.dequant_fp32(q["codes"], q["scales"], g, mean)
+    ref = oracle.kv_dequant(q["codes"], q["scales"], q["g"], mean=q["mean"])
+    assert np.array_equal(bf16_rne(v32), ref)
+    v32n = oa.dequant_fp32(q["codes"], q["scales"], g)
+    assert np.array_equal(bf16_rne(v32n), oracle.kv_dequant(q["codes"], q["scales"], q["g"]))
+
+
+def test_identical_keys_give_the_mean_of_v():
+    rng = np.random.default_rng(5)
+    T, H, D = 9, 2, 16
+    k = np.broadcast_to(rng.standard_normal((1, H, D)), (T, H, D))
+    v = rng.standard_normal((T, H, D))
+    q = rng.standard_normal((3, H, D))
+    out, _, _ = oa.attention_decode(q, k, v, 0.25)
+    assert np.allclose(out, np.broadcast_to(v.mean(axis=0), out.shape), rtol=0, atol=1e-12)
+
+
+def test_a_dominant_key_selects_its_value():
+    rng = np.random.default_rng(6)
+    T, H, D = 7, 1, 16
+    q = np.ones((1, H, D))
+    k = rng.standard_normal((T, H, D)) * 0.01
+    k[4] = 10.0  # score 160 / 4 = 40 above the others: weight 1 - O(e^-38)
+    v = rng.standard_normal((T, H, D))
+    out, _, _ = oa.attention_decode(q, k, v, 0.25)
+    assert np.allclose(out[0, 0], v[4, 0], rtol=0, atol=1e-12)
+
+
+def test_scores_shifted_by_a_constant_change_nothing():
+    """Adding the same vector u to every key adds q . u to every score of a query: the
+    softmax, and so the output, do not change."""
+    rng = np.random.default_rng(7)
+    T, H, D = 11, 2, 16
+    q = rng.standard_normal((2, H, D))
+    k = rng.standard_normal((T, H, D))
+    v = rng.standard_normal((T, H, D))
+    base, _, _ = oa.attention_decode(q, k, v, 0.3)
+    u = rng.standard_normal((1, H, D))
+    out_u, _, _ = oa.attention_decode(q, k + u, v, 0.3)
+    assert np.allclose(out_u, base, rtol=0, atol=1e-12)

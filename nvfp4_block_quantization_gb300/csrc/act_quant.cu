@@ -29,7 +29,7 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kActThreads = 256;
-constexpr int kActCtasPerSm = 4;
+constexpr int kActCtasPerSm = 4;     // amax pass; the quantization pass runs 3 per SM
 
 template <bool kRHT>
 __device__ __forceinline__ void act_block(const uint16_t* x, int64_t b, uint32_t signs, float v[16]) {
@@ -70,7 +70,7 @@ __device__ __forceinline__ int64_t mma_offset(int64_t r, int64_t kb, int64_t kbt
 }
 
 template <bool kRHT>
-__global__ void __launch_bounds__(kActThreads, 2) act_quant_kernel(const uint16_t* __restrict__ x, int64_t M,
+__global__ void __launch_bounds__(kActThreads, 3) act_quant_kernel(const uint16_t* __restrict__ x, int64_t M,
                                                                    int64_t KB, uint32_t signs,
                                                                    const float* __restrict__ part, int nparts,
                                                                    uint8_t* __restrict__ codes,
@@ -98,15 +98,26 @@ __global__ void __launch_bounds__(kActThreads, 2) act_quant_kernel(const uint16_
     if (dev_status) *dev_status = nonfinite ? NVFP4_DEV_NONFINITE : NVFP4_DEV_OK;
   }
   const int64_t nblocks = M * KB, kbt = (KB + 3) / 4;
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += (int64_t)gridDim.x * blockDim.x) {
+  // block b is (row r, block kb) with b = r KB + kb; the grid stride moves both by
+  // constants, so they advance without a division per block
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t dr = stride / KB, dkb = stride - dr * KB;
+  int64_t r = b0 / KB, kb = b0 - r * KB;
+  for (int64_t b = b0; b < nblocks; b += stride) {
     float z[16];
     act_block<kRHT>(x, b, signs, z);
     uint2 code;
     uint32_t sc;
     quant_block(z, tab, k6, k4, nonfinite, code, sc);
     reinterpret_cast<uint2*>(codes)[b] = code;
-    const int64_t r = b / KB, kb = b - r * KB;
     sf[mma_offset(r, kb, kbt)] = (uint8_t)sc;
+    r += dr;
+    kb += dkb;
+    if (kb >= KB) {
+      kb -= KB;
+      ++r;
+    }
   }
   // the layout's padding: rows [M, roundup(M, 128)) and blocks [KB, roundup(KB, 4)) of the others
   const int64_t Mp = (M + 127) / 128 * 128, KBp = kbt * 4;
@@ -166,12 +177,12 @@ nvfp4_status nvfp4_act_quant_mma(const void* x, int64_t M, int64_t K, int use_rh
   const int64_t KB = K / 16, nb = M * KB;
   if (use_rht) {
     nvfp4::act_amax_kernel<true><<<ctas, nvfp4::kActThreads, 0, s>>>(xb, nb, signs, part);
-    nvfp4::act_quant_kernel<true><<<ctas / 2, nvfp4::kActThreads, 0, s>>>(xb, M, KB, signs, part, ctas, codes,
-                                                                          scales_mma, tensor_scale, dev_status);
+    nvfp4::act_quant_kernel<true><<<ctas / 4 * 3, nvfp4::kActThreads, 0, s>>>(xb, M, KB, signs, part, ctas, codes,
+                                                                              scales_mma, tensor_scale, dev_status);
   } else {
     nvfp4::act_amax_kernel<false><<<ctas, nvfp4::kActThreads, 0, s>>>(xb, nb, signs, part);
-    nvfp4::act_quant_kernel<false><<<ctas / 2, nvfp4::kActThreads, 0, s>>>(xb, M, KB, signs, part, ctas, codes,
-                                                                           scales_mma, tensor_scale, dev_status);
+    nvfp4::act_quant_kernel<false><<<ctas / 4 * 3, nvfp4::kActThreads, 0, s>>>(xb, M, KB, signs, part, ctas, codes,
+                                                                               scales_mma, tensor_scale, dev_status);
   }
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }

@@ -23,7 +23,7 @@
  *   The NVFP4 format itself (E2M1 element values {0, .5, 1, 1.5, 2, 3, 4, 6}
  *   with sign, 16-element blocks, an E4M3 block scale and an fp32 per-tensor
  *   scale; E4M3 cast round-to-nearest-even with saturation; ties of the 4/6
- *   comparison going to 6) is the benchmark spec's definition of NVFP4.
+ *   comparison going to 6) is the standard NVFP4 definition this library uses.
  *
  * Where the pages are silent the readings below are used (each one is listed
  * with its reason in the design notes):

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
 
-Bars (stated in the task's target for this path):
+Bars:
   * codes, scales and the tensor scale bit-exact when both sides use the same
     mean (mean_in = the oracle's mean), and for every unsmoothed tensor;
   * end to end (GPU-computed mean): at most 1e-5 of blocks may differ, each by

@@ -104,3 +104,31 @@ def test_rht16_argument_errors(lib):
     assert lib.nvfp4_rht16(g + 16, 0, 4, 32, 0, g, None) == lib.NVFP4_EALIGN
     assert lib.nvfp4_rht16(None, 0, 4, 32, 0, g, None) == lib.NVFP4_EINVAL
     assert lib.nvfp4_rht16(None, 0, 0, 32, 0, None, None) == lib.NVFP4_OK
+
+
+def test_act_quant_argument_errors(lib):
+    """Checks that return before any CUDA call (the workspace check needs the device's SM count)."""
+    g = 1 << 20
+    L = lib.load()
+    q = lambda x=g, M=64, K=128, rht=0, signs=0, codes=g, sf=g, ts=g: L.nvfp4_act_quant_mma(
+        x, M, K, rht, signs, codes, sf, ts, None, g, 1 << 20, None)
+    assert q(M=0) == lib.NVFP4_ESHAPE and q(K=24) == lib.NVFP4_ESHAPE and q(K=0) == lib.NVFP4_ESHAPE
+    assert q(rht=2) == lib.NVFP4_EINVAL and q(signs=1 << 16) == lib.NVFP4_EINVAL
+    assert q(x=None) == lib.NVFP4_EINVAL and q(ts=None) == lib.NVFP4_EINVAL
+    assert q(x=g + 16) == lib.NVFP4_EALIGN and q(codes=g + 8) == lib.NVFP4_EALIGN and q(sf=g + 4) == lib.NVFP4_EALIGN
+
+
+def test_bench_byte_accounting():
+    """The bench's algorithmic bytes per element: 2 in + 0.5 codes + 1/16 scales (1-D blocks),
+    0.5 + 1/16 in + 2 out (cache read), 2 + 0.5 + 1/256 (16x16 weight tiles)."""
+    import importlib.util
+    import os
+
+    spec = importlib.util.spec_from_file_location(
+        "bench_mod", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    assert b.QUANT_BYTES_PER_ELEM == 2.5625
+    assert b.DEQUANT_BYTES_PER_ELEM == 2.5625
+    assert b.W2D_BYTES_PER_ELEM == 2 + 0.5 + 1 / 256
+    assert b.FP4_OVER_BF16 == 6.0

@@ -66,3 +66,27 @@ def test_scores_shifted_by_a_constant_change_nothing():
     u = rng.standard_normal((1, H, D))
     out_u, _, _ = oa.attention_decode(q, k + u, v, 0.3)
     assert np.allclose(out_u, base, rtol=0, atol=1e-12)
+
+
+def test_two_keys_weighted_by_the_scaled_score_gap():
+    """Two keys whose scores differ by c, with scale * c = ln 3: the softmax weights are
+    exactly 1/4 and 3/4.  This fixes the softmax scale (dropped, squared or inverted, the
+    weights move).  A and Vmax follow their definitions by hand."""
+    D = 16
+    q = np.zeros((1, 2, D))
+    q[0, 0, :] = 1.0
+    q[0, 1, 3] = -2.0
+    c = 8.0
+    scale = np.log(3.0) / c
+    k = np.zeros((2, 2, D))
+    k[1, 0, :] = c / D                   # head 0: q . k1 = c
+    k[1, 1, 3] = -c / 2                  # head 1: q . k1 = c
+    v = np.zeros((2, 2, D))
+    v[0, :, :] = 4.0
+    v[1, :, :] = -8.0
+    v[1, 1, 5] = 12.0
+    out, A, Vmax = oa.attention_decode(q, k, v, scale)
+    want = 0.25 * v[0] + 0.75 * v[1]
+    assert np.allclose(out[0], want, rtol=0, atol=1e-12)
+    assert np.allclose(A[0], [scale * c, scale * c], rtol=1e-15, atol=0)
+    assert np.array_equal(Vmax, [8.0, 12.0])

@@ -39,6 +39,26 @@ def test_reference_nibble_order_and_sign():
     assert np.all(y == -K / 2) and np.all(s == K / 2)
 
 
+def test_reference_one_hot_rows_read_out_w():
+    """X row m is 1.0 at k = m and 0 elsewhere, all scales 1: Y[m, n] is W's element (n, m).
+    W's elements are all different along k and n, so a transposed operand, a swapped index
+    or a wrong nibble order moves values.  E2M1 codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+    bit 3 is the sign."""
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    M, N, K = 32, 32, 32
+    wcode = np.array([[(5 * n + 3 * k + n // 7) % 16 for k in range(K)] for n in range(N)], np.uint8)
+    wc = (wcode[:, 0::2] | (wcode[:, 1::2] << 4)).astype(np.uint8)
+    xcode = np.zeros((M, K), np.uint8)
+    xcode[np.arange(M), np.arange(M)] = 2              # 1.0
+    xc = (xcode[:, 0::2] | (xcode[:, 1::2] << 4)).astype(np.uint8)
+    xs = np.full((M, K // 16), 0x38, np.uint8)
+    ws = np.full((N // 16, K // 16), 0x38, np.uint8)
+    y, s = og.gemm_w4a4(xc, xs, 1.0, wc, ws, 1.0)
+    for m in range(M):
+        for n in range(N):
+            assert y[m, n] == e2m1[wcode[n, m]] and s[m, n] == abs(e2m1[wcode[n, m]])
+
+
 @pytest.fixture(scope="module")
 def lib():
     from nvfp4_block_quantization_gb300 import _lib

@@ -39,7 +39,7 @@ METRIC = "NVFP4 smooth+quantize GB/s and fraction of GB300 HBM peak per KV chunk
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of each kernel on this step's workload, from one ncu
-# capture of this script (profiles/kv_chunk_7040x24x128_launch_list.md); drop an entry when its
+# capture of this script (dram__bytes_read.sum + dram__bytes_write.sum); drop an entry when its
 # kernel changes.  The quantization kernel's entry is dropped: its wait loop's sleep interval
 # changed after that capture (22.0 MB per launch then).
 NCU_TRAFFIC = {"kv_stats": 114275200, "kv_quant": None}

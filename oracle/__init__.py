@@ -76,6 +76,11 @@ def _load():
         lib.oracle_kv_smooth_quant.argtypes = [c_void_p, c_int, c_int64, c_int64, c_int64, c_int,
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
         lib.oracle_kv_smooth_quant.restype = c_int
+        lib.oracle_kv_smooth_quant_headroom.argtypes = [c_void_p, c_int, c_int64, c_int64, c_int64, c_int,
+                                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+        lib.oracle_kv_smooth_quant_headroom.restype = c_int
+        lib.oracle_tensor_scale_headroom.argtypes = [c_float]
+        lib.oracle_tensor_scale_headroom.restype = c_float
         lib.oracle_kv_dequant.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
                                           c_int64, c_int64, c_void_p]
         lib.oracle_kv_dequant.restype = c_int
@@ -159,9 +164,11 @@ def block_detail(z: np.ndarray, g: float) -> dict:
                 sum6=float(f[2][0]), sum4=float(f[3][0]))
 
 
-def kv_smooth_quant(x: np.ndarray, smooth: bool, mean_in: np.ndarray | None = None) -> dict:
+def kv_smooth_quant(x: np.ndarray, smooth: bool, mean_in: np.ndarray | None = None,
+                    headroom: bool = False) -> dict:
     """Quantize x[T, H, D] (bf16 bits as uint16, or float32).
 
+    headroom: take the tensor scale g = amax / 1792 (4 x 448) instead of amax / 2688.
     Returns dict(codes [T, H, D/2] uint8, scales [T, H, D/16] uint8, g float,
     mean [H, D] float32 or None, chose4 [T, H, D/16] uint8, status int).
     """
@@ -173,8 +180,10 @@ def kv_smooth_quant(x: np.ndarray, smooth: bool, mean_in: np.ndarray | None = No
     g = np.zeros(1, dtype=np.float32)
     mean_out = np.zeros((H, D), dtype=np.float32) if smooth else None
     mi = None if mean_in is None else np.ascontiguousarray(mean_in, dtype=np.float32).reshape(H, D)
-    rc = _load().oracle_kv_smooth_quant(_ptr(x), dt, T, H, D, int(bool(smooth)), _ptr(mi), _ptr(mean_out),
-                                        _ptr(codes), _ptr(scales), _ptr(g), _ptr(chose4))
+    lib = _load()
+    fn = lib.oracle_kv_smooth_quant_headroom if headroom else lib.oracle_kv_smooth_quant
+    rc = fn(_ptr(x), dt, T, H, D, int(bool(smooth)), _ptr(mi), _ptr(mean_out),
+            _ptr(codes), _ptr(scales), _ptr(g), _ptr(chose4))
     if rc == EINVAL:
         raise ValueError("oracle_kv_smooth_quant: invalid arguments")
     return dict(codes=codes, scales=scales, g=float(g[0]), mean=mean_out, chose4=chose4, status=rc)

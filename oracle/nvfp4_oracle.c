@@ -32,6 +32,7 @@
  *       taken in binary64 in token order, rounded once to fp32.
  *   R3  Z = fl(X - mean) in fp32; V and activations are not smoothed (Z = X).
  *   R4  amax = max |Z| over the tensor; g = fl(amax / 2688), 2688 = 6 * 448.
+ *       H1 (headroom variant, separate entry points): g = fl(amax / 1792), 1792 = 4 * 448.
  *       A non-finite Z makes the call report NONFINITE with filler outputs.
  *   R5  per-tensor candidate factors k_M = fl(1 / fl(M * g)), M in {6, 4};
  *       block candidate scale s_M = fl(a_b * k_M) with a_b = max |Z| over the
@@ -157,6 +158,11 @@ float oracle_bf16_widen(uint16_t b) {
 
 float oracle_tensor_scale(float amax) { return amax / 2688.0f; }
 
+/* Headroom variant of R4 (reading H1): g = fl(amax / 1792), 1792 = 4 * 448, the largest
+ * denominator under which the 4-candidate of the block that holds the tensor's amax maps
+ * to 448 and so never saturates in E4M3.  Everything after g is unchanged. */
+float oracle_tensor_scale_headroom(float amax) { return amax / 1792.0f; }
+
 static void candidate_factors(float g, float* k6, float* k4) {
   float m6 = 6.0f * g;
   float m4 = 4.0f * g;
@@ -271,9 +277,9 @@ void oracle_channel_mean(const void* x, int dtype, int64_t T, int64_t C, float* 
 /* Returns ORACLE_OK, ORACLE_NONFINITE (filler: codes 0, scales 0x7F,        */
 /* g = NaN) or ORACLE_EINVAL.                                                */
 /* ------------------------------------------------------------------------ */
-int oracle_kv_smooth_quant(const void* x, int dtype, int64_t T, int64_t H, int64_t D, int smooth,
-                           const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
-                           float* g_out, uint8_t* chose4) {
+static int kv_smooth_quant_impl(const void* x, int dtype, int64_t T, int64_t H, int64_t D, int smooth,
+                                const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
+                                float* g_out, uint8_t* chose4, int headroom) {
   if (T < 0 || H <= 0 || D <= 0 || (D % 16) != 0 || (dtype != 0 && dtype != 1)) return ORACLE_EINVAL;
   if (!smooth && (mean_in || mean_out)) return ORACLE_EINVAL;
   const int64_t C = H * D;
@@ -306,7 +312,7 @@ int oracle_kv_smooth_quant(const void* x, int dtype, int64_t T, int64_t H, int64
     free(z); free(mean);
     return ORACLE_NONFINITE;
   }
-  float g = oracle_tensor_scale(amax);
+  float g = headroom ? oracle_tensor_scale_headroom(amax) : oracle_tensor_scale(amax);
   *g_out = g;
   float k6 = 0.0f, k4 = 0.0f;
   if (g != 0.0f) candidate_factors(g, &k6, &k4);
@@ -321,6 +327,19 @@ int oracle_kv_smooth_quant(const void* x, int dtype, int64_t T, int64_t H, int64
   }
   free(z); free(mean);
   return ORACLE_OK;
+}
+
+int oracle_kv_smooth_quant(const void* x, int dtype, int64_t T, int64_t H, int64_t D, int smooth,
+                           const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
+                           float* g_out, uint8_t* chose4) {
+  return kv_smooth_quant_impl(x, dtype, T, H, D, smooth, mean_in, mean_out, codes, scales, g_out, chose4, 0);
+}
+
+/* The same with the headroom tensor scale (H1). */
+int oracle_kv_smooth_quant_headroom(const void* x, int dtype, int64_t T, int64_t H, int64_t D, int smooth,
+                                    const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
+                                    float* g_out, uint8_t* chose4) {
+  return kv_smooth_quant_impl(x, dtype, T, H, D, smooth, mean_in, mean_out, codes, scales, g_out, chose4, 1);
 }
 
 /* ------------------------------------------------------------------------ */

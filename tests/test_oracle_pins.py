@@ -501,3 +501,47 @@ def test_dequant_groups_and_mean(oracle):
     out = oracle.bf16_bits_to_f32(oracle.kv_dequant(codes, scales, g, mean=mean, tokens_per_group=2))
     assert np.array_equal(out[0, 0], B)
     assert np.array_equal(out[2, 0], 2 * B + 0.5)
+
+
+# ------------------------------------------------------------ headroom variant (reading H1)
+def test_headroom_tensor_scale_closed_form(oracle):
+    """g = amax / 1792 (4 x 448): 1792 -> 1, 7 -> 2^-8, both exact."""
+    lib = oracle._load()
+    assert lib.oracle_tensor_scale_headroom(1792.0) == 1.0
+    assert lib.oracle_tensor_scale_headroom(7.0) == 2.0 ** -8
+
+
+def test_headroom_amax_block_can_pick_four(oracle):
+    """Worked by hand.  Tensor = one block [7, +-5.25 x 15] (75% of its amax), g = 7/1792 = 2^-8.
+    4-candidate: 7 / (4 g) = 448, E4M3 448 (0x7E), S = 1.75: 7 -> 4 and 5.25 -> 3 (code 6 and
+    code 5, sign bit 8), error about 0.  6-candidate: 7 / (6 g) = 298.7 -> E4M3 288, S = 1.125:
+    7 -> 6.22 saturates to 6, error > 0.  So 4 wins, and the read gives back 7 and +-5.25
+    exactly.  With g = amax / 2688 the block holding the amax ties and keeps 6 instead."""
+    x = np.array([7.0] + [5.25 if i % 2 else -5.25 for i in range(15)], np.float32).reshape(1, 1, 16)
+    q = oracle.kv_smooth_quant(x, smooth=False, headroom=True)
+    assert q["g"] == 2.0 ** -8
+    assert q["scales"].ravel().tolist() == [0x7E] and q["chose4"].ravel().tolist() == [1]
+    want = [6] + [5 if i % 2 else 13 for i in range(15)]
+    codes = q["codes"].ravel()
+    got = [int(codes[j // 2] >> (4 * (j % 2))) & 0xF for j in range(16)]
+    assert got == want
+    back = oracle.kv_dequant(q["codes"], q["scales"], q["g"]).view(np.uint16)
+    assert np.array_equal(back.ravel(), (x.ravel().view(np.uint32) >> 16).astype(np.uint16))  # exact in bf16
+    std = oracle.kv_smooth_quant(x, smooth=False)
+    assert std["chose4"].ravel().tolist() == [0]
+
+
+def test_headroom_amax_block_scale_is_448_or_288(oracle):
+    """On random tensors the block holding the amax has 7 / (4 g) = 448 exactly up to the
+    rounding of g: its scale byte is 0x7E with 4 kept, or 0x79 (E4M3 288, the 6-candidate
+    298.7 rounded) with 6 kept.  The standard scale gives 0x7E with 6 kept."""
+    rng = np.random.default_rng(11)
+    for t in range(20):
+        x = (rng.standard_normal((8, 2, 64)) * (1 + t)).astype(np.float32)
+        q = oracle.kv_smooth_quant(x, smooth=False, headroom=True)
+        flat = np.abs(x).reshape(-1, 16).max(axis=1)
+        b = int(np.argmax(flat))
+        byte, c4 = int(q["scales"].ravel()[b]), int(q["chose4"].ravel()[b])
+        assert (byte, c4) in ((0x7E, 1), (0x79, 0)), (t, hex(byte), c4)
+        s = oracle.kv_smooth_quant(x, smooth=False)
+        assert (int(s["scales"].ravel()[b]), int(s["chose4"].ravel()[b])) == (0x7E, 0)

@@ -165,3 +165,16 @@ def test_workloads_are_seeded_and_shaped():
     k = W.chunk_k(2000, T=64, H=4, D=32)
     assert k.shape == (64, 4, 32)
     assert W.CHUNK_TOKENS == 7040
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the compiled library the binding raises; there is no other path to fall back to."""
+    from nvfp4_block_quantization_gb300 import _lib
+
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            _lib.load(str(tmp_path / "libnvfp4_gb300.so"))
+    finally:
+        _lib._lib = saved

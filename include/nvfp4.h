@@ -115,10 +115,13 @@ size_t nvfp4_kv_workspace_bytes(int64_t T, int H, int D);
  *                the same workspace serves later calls on one stream without
  *                clearing.  Calls that share a workspace must not overlap.
  *   stream       cudaStream_t
- * Implementation: one persistent cooperative kernel (one CTA per SM).  Its
- * cross-CTA waits are bounded (about 2 s); if one runs out, *dev_status gets
- * NVFP4_DEV_TIMEOUT, the affected outputs are left unwritten and the
- * workspace must be zero-filled again before reuse.
+ * Implementation: a cooperative statistics grid (one CTA per SM: channel sums,
+ * minima and maxima, the means and the tensor's absolute maximum) followed by a
+ * quantization grid launched as its programmatic dependent, whose CTAs wait
+ * for their own tensor's statistics.  Both grids' cross-CTA waits are bounded
+ * (about 2 s); if one runs out, *dev_status gets NVFP4_DEV_TIMEOUT, the
+ * affected outputs are left unwritten and the workspace must be zero-filled
+ * again before reuse.
  * Errors: NVFP4_EINVAL (NULL x/codes/scales/tensor_scale, bad dt or smooth,
  * mean pointers with smooth == 0), NVFP4_ESHAPE (also T*H*D > 2^46),
  * NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUDA. */
@@ -184,6 +187,24 @@ nvfp4_status nvfp4_kv_quant_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_
 nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
                               const float* mean, int64_t tokens_per_group, int64_t T, int H, int D,
                               void* out_bf16, void* stream);
+
+/* Self-test of the conversion instructions (the pages have no counterpart):
+ * runs, on caller-provided values, exactly the rounding and decoding steps the
+ * quantizers above use, so that a test can compare them with a software
+ * statement of the formats.
+ *   x                device [n] fp32 inputs (4-byte aligned)
+ *   e2m1_codes       device [n]: byte i holds x[i]'s E2M1 code (round to nearest
+ *                    even, saturating at 6, sign kept) in both nibbles -- one per
+ *                    lane of the paired conversion the quantizers use
+ *   e4m3_codes       device [n] uint16: x[i]'s E4M3 code (round to nearest even,
+ *                    saturating at 448; NaN in, NaN code out) in both bytes
+ *   e2m1_pair_f16x2  device [256]: entry b is byte b decoded as two E2M1 codes,
+ *                    f16 pair (low half = low nibble)
+ *   e4m3_values      device [256]: entry b is E4M3 code b as fp32 (0x7F/0xFF: NaN)
+ * Errors: NVFP4_ESHAPE (n < 0), NVFP4_EINVAL (NULL pointers), NVFP4_EALIGN,
+ * NVFP4_ECUDA. */
+nvfp4_status nvfp4_selftest_cvt(const float* x, int64_t n, uint8_t* e2m1_codes, uint16_t* e4m3_codes,
+                                uint32_t* e2m1_pair_f16x2, float* e4m3_values, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Multi-shot NVFP4 KV cache (LongLive-2.0 summary page, inference step 9:  */
@@ -355,9 +376,11 @@ nvfp4_status nvfp4_weight_quant_2d_batched(const nvfp4_w2d_job* jobs, int n_jobs
  * tensors it reads and writes, or code that must not call into an allocator
  * at that point.  Its scratch (the per-CTA amax partials, 4 per SM) is a
  * file-scope device array inside the library of 4096 entries: the call returns
- * NVFP4_EWORKSPACE on a device with more than 1024 SMs.  The first call on a
- * device looks up that array's address (once per device, with the device
- * current); make that first call before capturing a stream.  All calls on a
+ * NVFP4_EWORKSPACE on a device with more than 1024 SMs.  Every call looks up
+ * the array's device address (cudaGetSymbolAddress with the caller's device
+ * current), so a call after a device reset uses the array of the new context.
+ * The first call on a device may load the library's device code: make it
+ * before capturing a stream.  All calls on a
  * device share the one array, so calls that overlap in time (several streams
  * or host threads) race: order them.  Results, arguments and other errors are
  * those of nvfp4_weight_quant_2d. */

@@ -208,6 +208,23 @@ def kv_dequant(codes, scales, tensor_scale, mean=None, tokens_per_group: Optiona
     return out
 
 
+def selftest_cvt(x, stream=None):
+    """Run the quantizers' conversion instructions on a CUDA fp32 tensor ``x``: returns
+    (E2M1 code bytes [n] -- the code in both nibbles, E4M3 codes [n] uint16 -- the code in
+    both bytes, the f16 pair decode of every byte [256] int32, every E4M3 code's value [256])."""
+    torch = _torch()
+    _check_cuda(x)
+    x = x.contiguous().view(-1)
+    n = x.numel()
+    e2m1 = torch.empty(n, dtype=torch.uint8, device=x.device)
+    e4m3 = torch.empty(n, dtype=torch.int16, device=x.device)
+    dec = torch.empty(256, dtype=torch.int32, device=x.device)
+    val = torch.empty(256, dtype=torch.float32, device=x.device)
+    st = _lib.nvfp4_selftest_cvt(_ptr(x), n, _ptr(e2m1), _ptr(e4m3), _ptr(dec), _ptr(val), _stream(stream))
+    _lib.check(st, "nvfp4_selftest_cvt")
+    return e2m1, e4m3, dec, val
+
+
 class KvCache:
     """Host bookkeeping of a multi-shot NVFP4 KV cache (``nvfp4_kvcache_*``): which chunk
     slot holds which chunk, the global sink, the shot sink (START/LEN) and the rolling

@@ -15,7 +15,7 @@ NVFP4_OK, NVFP4_EINVAL, NVFP4_ESHAPE, NVFP4_EALIGN, NVFP4_EWORKSPACE, NVFP4_ECUD
 NVFP4_KVCACHE_MAX_SLOTS = 64
 NVFP4_MAX_VIEW_FRAMES = 512
 NVFP4_IN_BF16, NVFP4_IN_FP32 = 0, 1
-NVFP4_DEV_OK, NVFP4_DEV_NONFINITE = 0, 1
+NVFP4_DEV_OK, NVFP4_DEV_NONFINITE, NVFP4_DEV_TIMEOUT = 0, 1, 2
 
 # Every entry point declared in include/nvfp4.h.
 EXPORTS = (
@@ -28,6 +28,7 @@ EXPORTS = (
     "nvfp4_kv_stats_batched",
     "nvfp4_kv_quant_batched",
     "nvfp4_kv_dequant",
+    "nvfp4_selftest_cvt",
     "nvfp4_kvcache_slots_needed",
     "nvfp4_kvcache_init",
     "nvfp4_kvcache_append",
@@ -131,6 +132,8 @@ def load(path: str | None = None):
     lib.nvfp4_kv_quant_batched.restype = i32
     lib.nvfp4_kv_dequant.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.nvfp4_kv_dequant.restype = i32
+    lib.nvfp4_selftest_cvt.argtypes = [vp, i64, vp, vp, vp, vp, vp]
+    lib.nvfp4_selftest_cvt.restype = i32
     P = ctypes.POINTER
     lib.nvfp4_kvcache_slots_needed.argtypes = [i32, i32, i32, i32]
     lib.nvfp4_kvcache_slots_needed.restype = i32
@@ -227,6 +230,10 @@ def nvfp4_kv_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspace, wor
 
 def nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream):
     return load().nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, D, out_bf16, stream)
+
+
+def nvfp4_selftest_cvt(x, n, e2m1_codes, e4m3_codes, e2m1_pair_f16x2, e4m3_values, stream):
+    return load().nvfp4_selftest_cvt(x, n, e2m1_codes, e4m3_codes, e2m1_pair_f16x2, e4m3_values, stream)
 
 
 def nvfp4_kvcache_slots_needed(frames_per_chunk, global_sink, shot_sink, window):

@@ -4,7 +4,6 @@
 // enqueued on an error), carves its workspace, and enqueues the kernels on the
 // caller's stream.  No allocation, no synchronization, no printing.
 #include <algorithm>
-#include <atomic>
 #include <cstring>
 
 #include "nvfp4.h"
@@ -245,22 +244,14 @@ namespace {
 // nothing in it has to start at zero.  All calls on one device share it.
 constexpr int kW2dStaticPartials = 4096;  // room for 1024 SMs
 static __device__ __align__(256) float g_w2d_static_scratch[kW2dStaticPartials];
-constexpr int kMaxDevices = 64;
-
-// Device address of the scratch on the current device, looked up once per device
-// (cudaGetSymbolAddress with that device current); nullptr if the lookup fails.
+// Device address of the scratch in the current context, looked up on every call
+// (cudaGetSymbolAddress with the caller's device current), so that a call after a
+// device reset -- which loads the module into a new context -- never reuses an
+// address of the old one; nullptr if the lookup fails.
 float* w2d_static_scratch() {
-  static std::atomic<void*> cache[kMaxDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* p = cache[dev].load(std::memory_order_acquire);
-  if (!p) {
-    void* q = nullptr;
-    if (cudaGetSymbolAddress(&q, g_w2d_static_scratch) != cudaSuccess || !q) return nullptr;
-    cache[dev].store(q, std::memory_order_release);
-    p = q;
-  }
-  return static_cast<float*>(p);
+  void* q = nullptr;
+  if (cudaGetSymbolAddress(&q, g_w2d_static_scratch) != cudaSuccess || !q) return nullptr;
+  return static_cast<float*>(q);
 }
 
 }  // namespace

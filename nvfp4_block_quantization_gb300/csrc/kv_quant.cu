@@ -61,6 +61,13 @@ __device__ __forceinline__ void load_block(const uint8_t* p, RawBlock<kBF16>& r)
   for (int i = 0; i < (kBF16 ? 2 : 4); ++i) r.v[i] = ld_nc_v4(p + 16 * i);
 }
 
+__device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_cs_u8(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <bool kBF16>
 __device__ __forceinline__ void smooth_block(const RawBlock<kBF16>& r, const float mu[16], float z[16]) {
   if (kBF16) {
@@ -87,8 +94,8 @@ __device__ __forceinline__ void quant_store(const RawBlock<kBF16>& r, const floa
   uint2 code;
   uint32_t sc;
   quant_block(z, tab, k6, k4, nonfinite, code, sc);
-  *pc = code;
-  *ps = (uint8_t)sc;
+  st_cs_v2(pc, code);
+  st_cs_u8(ps, sc);
 }
 
 }  // namespace

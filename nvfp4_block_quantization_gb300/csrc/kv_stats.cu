@@ -280,28 +280,34 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
   if (threadIdx.x >= consumers) {
     // producer: one thread streams the CTA's rows of every job and slab, stage by stage
     if (threadIdx.x == consumers) {
-      int f = 0;
+      const int T = (int)G.T, row_step = G.P * G.rows_per_stage;
+      int st = 0, used = 0;  // ring slot; stages issued so far
+      unsigned ph = 0;        // phase of the slot's current round
       for (int job = 0; job < b.n; ++job) {
         const uint8_t* x = static_cast<const uint8_t*>(b.job[job].x);
         for (int sl = 0; sl < nslab; ++sl) {
           const int s0 = sl * slab_ch, sb = min(slab_ch, G.C - s0) * es;  // slab bytes of this slab
-          for (int64_t row = (int64_t)c * G.rows_per_stage; row < G.T; row += (int64_t)G.P * G.rows_per_stage, ++f) {
-            const int rows = (int)min((int64_t)G.rows_per_stage, G.T - row);
-            const int st = f % kStatsStages;
-            if (f >= kStatsStages && !sm.abort &&
-                !mbar_wait(&sm.empty[st], (unsigned)(f / kStatsStages - 1) & 1u)) {
+          for (int row = c * G.rows_per_stage; row < T; row += row_step) {
+            const int rows = min(G.rows_per_stage, T - row);
+            if (used >= kStatsStages && !sm.abort && !mbar_wait(&sm.empty[st], ph ^ 1u)) {
               sm.abort = 1;
               atomicOr(G.header + 1, kStatusTimeout);
             }
+            const int cur = st;
+            if (++st == kStatsStages) {
+              st = 0;
+              ph ^= 1u;
+            }
+            ++used;
             if (sm.abort) continue;
-            uint8_t* dst = ring + (size_t)st * kStatsStageBytes;
-            mbar_expect_tx(&sm.full[st], (unsigned)(rows * sb));
+            uint8_t* dst = ring + (size_t)cur * kStatsStageBytes;
+            mbar_expect_tx(&sm.full[cur], (unsigned)(rows * sb));
             if (nslab == 1) {  // whole rows: the stage is one contiguous range
-              bulk_load(dst, x + (size_t)row * rs, (unsigned)(rows * sb), &sm.full[st]);
+              bulk_load(dst, x + (size_t)row * rs, (unsigned)(rows * sb), &sm.full[cur]);
             } else {
               for (int i = 0; i < rows; ++i)
                 bulk_load(dst + (size_t)i * sb, x + (size_t)(row + i) * rs + (size_t)s0 * es, (unsigned)sb,
-                          &sm.full[st]);
+                          &sm.full[cur]);
             }
           }
         }
@@ -311,7 +317,9 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
     // consumers
     const int chunk = threadIdx.x % G.tpr, rl = threadIdx.x / G.tpr;
     const bool lane_on = rl < G.rpp;  // threads beyond tpr * rpp idle
-    int f = 0;
+    const int T = (int)G.T, row_step = G.P * G.rows_per_stage;
+    int st = 0;
+    unsigned ph = 0;
     for (int job = 0; job < b.n; ++job) {
       const KvJob& J = b.job[job];
       const bool smooth = J.smooth != 0;
@@ -322,10 +330,9 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
         const bool on = lane_on && ch < G.C;
         Acc8 a;
         acc_reset(a);
-        for (int64_t row = (int64_t)c * G.rows_per_stage; row < G.T; row += (int64_t)G.P * G.rows_per_stage, ++f) {
-          const int rows = (int)min((int64_t)G.rows_per_stage, G.T - row);
-          const int st = f % kStatsStages;
-          if (!sm.abort && !mbar_wait(&sm.full[st], (unsigned)(f / kStatsStages) & 1u)) {
+        for (int row = c * G.rows_per_stage; row < T; row += row_step) {
+          const int rows = min(G.rows_per_stage, T - row);
+          if (!sm.abort && !mbar_wait(&sm.full[st], ph)) {
             sm.abort = 1;
             atomicOr(G.header + 1, kStatusTimeout);
           }
@@ -336,6 +343,10 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
           }
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[st]);
+          if (++st == kStatsStages) {
+            st = 0;
+            ph ^= 1u;
+          }
         }
         if (smooth) {
           if (on) {

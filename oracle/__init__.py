@@ -65,6 +65,10 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint]
         lib.oracle_e4m3_decode.restype = c_float
+        lib.oracle_e2m1_encode_n.argtypes = [c_void_p, c_void_p, c_int64]
+        lib.oracle_e2m1_encode_n.restype = None
+        lib.oracle_e4m3_encode_n.argtypes = [c_void_p, c_void_p, c_int64]
+        lib.oracle_e4m3_encode_n.restype = None
         lib.oracle_bf16_rne.argtypes = [c_float]
         lib.oracle_bf16_rne.restype = ctypes.c_uint16
         lib.oracle_tensor_scale.argtypes = [c_float]
@@ -125,6 +129,22 @@ def e4m3_encode(s: float) -> int:
 
 def e4m3_decode(code: int) -> float:
     return float(_load().oracle_e4m3_decode(int(code)))
+
+
+def e2m1_encode_array(y: np.ndarray) -> np.ndarray:
+    """E2M1 codes (uint8) of a float32 array, element by element."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    _load().oracle_e2m1_encode_n(_ptr(y), _ptr(out), y.size)
+    return out
+
+
+def e4m3_encode_array(s: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) of a float32 array, element by element."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty(s.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_n(_ptr(s), _ptr(out), s.size)
+    return out
 
 
 def bf16_rne(x: float) -> int:

@@ -126,6 +126,14 @@ float oracle_e4m3_decode(unsigned code) {
   return (float)((code & 0x80u) ? -v : v);
 }
 
+/* Array forms of the two encoders (element by element, same arithmetic). */
+void oracle_e2m1_encode_n(const float* y, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e2m1_encode(y[i]);
+}
+void oracle_e4m3_encode_n(const float* s, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e4m3_encode(s[i]);
+}
+
 /* bfloat16 = the upper 16 bits of an fp32; rounding keeps 8 significant    */
 /* bits with round-to-nearest-even, done here on the value with nearbyint.  */
 uint16_t oracle_bf16_rne(float x) {

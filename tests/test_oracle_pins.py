@@ -545,3 +545,22 @@ def test_headroom_amax_block_scale_is_448_or_288(oracle):
         assert (byte, c4) in ((0x7E, 1), (0x79, 0)), (t, hex(byte), c4)
         s = oracle.kv_smooth_quant(x, smooth=False)
         assert (int(s["scales"].ravel()[b]), int(s["chose4"].ravel()[b])) == (0x7E, 0)
+
+
+def test_candidate_scale_at_an_e4m3_tie(oracle):
+    """Reading R5 pinned at the bit level: a block at 3/4 of the tensor amax whose
+    6-candidate scale is an E4M3 tie in exact arithmetic (tests/golden/candidate_scale_tie.json).
+    The reciprocal-multiply reading lands one ulp above the tie and keeps 0x7B; the
+    divide-then-divide reading would give 0x7A."""
+    with open(os.path.join(HERE, "golden", "candidate_scale_tie.json")) as f:
+        fx = json.load(f)
+    x = np.zeros((1, 1, 32), np.float32)
+    x[0, 0, 0] = 23.0
+    x[0, 0, 16] = 17.25
+    r = oracle.kv_smooth_quant(x, smooth=False)
+    assert r["status"] == oracle.OK
+    assert np.float32(r["g"]).view(np.uint32) == 0x3C0C30C3
+    assert int(r["scales"][0, 0, 0]) == fx["block_0"]["scale"]
+    assert int(r["scales"][0, 0, 1]) == fx["block_1"]["scale"]
+    assert [int(v) for v in r["codes"][0, 0, :8]] == fx["block_0"]["codes"]
+    assert [int(v) for v in r["codes"][0, 0, 8:]] == fx["block_1"]["codes"]

@@ -153,6 +153,21 @@ nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs,
                                            int64_t T, int H, int D, int* dev_status, void* workspace,
                                            size_t workspace_bytes, void* stream);
 
+/* nvfp4_kv_smooth_quant_batched with E4M3 headroom in the tensor scale:
+ * g = fl(amax / 1792), 1792 = 4 * 448, instead of amax / 2688.  The pages fix
+ * no per-tensor scale formula.  With 2688 (the standard two-level NVFP4 scale)
+ * a block above 2/3 of the tensor amax has its 4-candidate saturate at 448, so
+ * the block holding the amax always keeps 6; 1792 is the largest denominator
+ * at which every block's 4-candidate fits under 448, so every block can choose
+ * between the two ranges ("LongLive-2.0" summary page, "full-stack NVFP4"
+ * paragraph: Four-Over-Six).  Everything else -- candidates, errors, ties,
+ * layouts, dequant -- is unchanged; the dequant of these outputs is
+ * nvfp4_kv_dequant with the tensor scale this call writes.  Arguments,
+ * workspace and errors as nvfp4_kv_smooth_quant_batched. */
+nvfp4_status nvfp4_kv_smooth_quant_headroom(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T,
+                                            int H, int D, int* dev_status, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* The two passes of nvfp4_kv_smooth_quant_batched as separate enqueues, for a
  * caller that wants to schedule them apart (e.g. the statistics of one tensor
  * on one stream while another tensor is quantized on a second stream).
@@ -205,6 +220,39 @@ nvfp4_status nvfp4_kv_dequant(const uint8_t* codes, const uint8_t* scales, const
  * NVFP4_ECUDA. */
 nvfp4_status nvfp4_selftest_cvt(const float* x, int64_t n, uint8_t* e2m1_codes, uint16_t* e4m3_codes,
                                 uint32_t* e2m1_pair_f16x2, float* e4m3_values, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Head shards of a quantized KV tensor for a sequence-parallel exchange     */
+/* ("LongLive-2.0" summary page: Ulysses SP all-to-all; the page credits the */
+/* 4-bit KV cache with the time saved at SP = 2 and 4, Table 6).             */
+/* ------------------------------------------------------------------------ */
+/* A quantized tensor [T][H][..] (codes, scales, tensor scale, optional mean)
+ * is cut into P head shards of H / P heads.  Shard p is one contiguous,
+ * 16-byte aligned segment of nvfp4_kv_shard_bytes(T, H, D, P, with_mean)
+ * bytes, so one all-to-all of P equal segments sends shard p to rank p:
+ *   [16 B: tensor scale g (fp32), then zeros]
+ *   [the shard's mean, (H / P) * D fp32, only with_mean]
+ *   [codes of the shard, [T][H/P][D/2], padded to a multiple of 16 bytes]
+ *   [scales of the shard, [T][H/P][D/16], padded to a multiple of 16 bytes]
+ * Returns 0 for invalid shapes (H % P != 0 among them). */
+size_t nvfp4_kv_shard_bytes(int64_t T, int H, int D, int P, int with_mean);
+
+/* Packs codes [T][H][D/2], scales [T][H][D/16], tensor_scale (device [1]) and
+ * mean (device [H][D] or NULL) into out (device, P segments, 16-byte aligned).
+ * Errors: NVFP4_ESHAPE (also H % P != 0), NVFP4_EINVAL, NVFP4_EALIGN,
+ * NVFP4_ECUDA. */
+nvfp4_status nvfp4_kv_pack_head_shards(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                                       const float* mean, int64_t T, int H, int D, int P, void* out, void* stream);
+
+/* Unpacks P segments (segment r from rank r, each holding that rank's T tokens
+ * of this rank's H / P heads) by stacking them along the token axis:
+ * codes [P*T][H/P][D/2], scales [P*T][H/P][D/16], tensor_scales device [P]
+ * (segment r's g), means device [P][H/P][D] (with_mean) or NULL.  The result
+ * is a cache of P groups of T tokens: nvfp4_kv_dequant with tokens_per_group
+ * = T reads it.  Errors as nvfp4_kv_pack_head_shards. */
+nvfp4_status nvfp4_kv_unpack_head_shards(const void* in, int64_t T, int H, int D, int P, int with_mean,
+                                         uint8_t* codes, uint8_t* scales, float* tensor_scales, float* means,
+                                         void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Multi-shot NVFP4 KV cache (LongLive-2.0 summary page, inference step 9:  */

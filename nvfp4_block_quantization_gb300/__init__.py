@@ -156,17 +156,19 @@ def _batch_jobs(xs, smooth, outs, status):
 
 
 def kv_smooth_quant_batched(xs: Sequence, smooth: Sequence[bool], workspace=None, outs=None, status=None,
-                            stream=None):
+                            stream=None, headroom: bool = False):
     """Quantize several same-shape chunk tensors (e.g. K and V of every layer) in one enqueue.
 
     Returns (list of KvQuantized, status) with one shared device status word (OR over tensors).
+    headroom=True takes the tensor scale g = amax / 1792 instead of amax / 2688
+    (nvfp4_kv_smooth_quant_headroom).
     """
     jobs, outs, status, (T, H, D) = _batch_jobs(xs, smooth, outs, status)
     if workspace is None:
         workspace = kv_workspace(T, H, D, len(xs), xs[0].device)
-    st = _lib.nvfp4_kv_smooth_quant_batched(jobs, len(xs), _dt(xs[0]), T, H, D, _ptr(status), _ptr(workspace),
-                                            workspace.numel(), _stream(stream))
-    _lib.check(st, "nvfp4_kv_smooth_quant_batched")
+    fn = _lib.nvfp4_kv_smooth_quant_headroom if headroom else _lib.nvfp4_kv_smooth_quant_batched
+    st = fn(jobs, len(xs), _dt(xs[0]), T, H, D, _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check(st, "nvfp4_kv_smooth_quant_headroom" if headroom else "nvfp4_kv_smooth_quant_batched")
     return outs, status
 
 
@@ -223,6 +225,57 @@ def selftest_cvt(x, stream=None):
     st = _lib.nvfp4_selftest_cvt(_ptr(x), n, _ptr(e2m1), _ptr(e4m3), _ptr(dec), _ptr(val), _stream(stream))
     _lib.check(st, "nvfp4_selftest_cvt")
     return e2m1, e4m3, dec, val
+
+
+def kv_shard_bytes(T: int, H: int, D: int, P: int, with_mean: bool) -> int:
+    """Bytes of one head-shard segment (nvfp4_kv_shard_bytes); 0 for invalid shapes."""
+    return int(_lib.nvfp4_kv_shard_bytes(T, H, D, P, int(bool(with_mean))))
+
+
+def kv_pack_head_shards(q: "KvQuantized", P: int, out=None, stream=None):
+    """Pack a quantized tensor into P head-shard segments (uint8 [P, segment bytes])."""
+    torch = _torch()
+    _check_cuda(q.codes, q.scales, q.tensor_scale, q.mean)
+    T, H, D2 = q.codes.shape
+    D = 2 * D2
+    seg = kv_shard_bytes(T, H, D, P, q.mean is not None)
+    if seg == 0:
+        raise ValueError("invalid shard shape (H % P must be 0)")
+    if out is None:
+        out = torch.empty((P, seg), dtype=torch.uint8, device=q.codes.device)
+    st = _lib.nvfp4_kv_pack_head_shards(_ptr(q.codes), _ptr(q.scales), _ptr(q.tensor_scale), _ptr(q.mean), T, H, D,
+                                        P, _ptr(out), _stream(stream))
+    _lib.check(st, "nvfp4_kv_pack_head_shards")
+    return out
+
+
+def kv_unpack_head_shards(segments, T: int, H: int, D: int, P: int, with_mean: bool, stream=None):
+    """Unpack P received segments into this rank's head shard of a P-group cache: returns
+    (codes [P T, H/P, D/2], scales [P T, H/P, D/16], tensor scales [P], means [P, H/P, D] or None)."""
+    torch = _torch()
+    _check_cuda(segments)
+    hs = H // P
+    dev = segments.device
+    codes = torch.empty((P * T, hs, D // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((P * T, hs, D // 16), dtype=torch.uint8, device=dev)
+    gs = torch.empty(P, dtype=torch.float32, device=dev)
+    means = torch.empty((P, hs, D), dtype=torch.float32, device=dev) if with_mean else None
+    st = _lib.nvfp4_kv_unpack_head_shards(_ptr(segments), T, H, D, P, int(bool(with_mean)), _ptr(codes),
+                                          _ptr(scales), _ptr(gs), _ptr(means), _stream(stream))
+    _lib.check(st, "nvfp4_kv_unpack_head_shards")
+    return codes, scales, gs, means
+
+
+def kv_exchange_head_shards(segments, group=None):
+    """All-to-all of packed head-shard segments ([P, segment bytes], equal splits): segment p
+    goes to rank p and row r of the result came from rank r.  Uses torch.distributed
+    (NCCL between GPUs; any backend with all_to_all_single)."""
+    torch = _torch()
+    import torch.distributed as dist
+
+    out = torch.empty_like(segments)
+    dist.all_to_all_single(out.view(-1), segments.contiguous().view(-1), group=group)
+    return out
 
 
 class KvCache:

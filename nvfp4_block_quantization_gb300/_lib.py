@@ -25,10 +25,14 @@ EXPORTS = (
     "nvfp4_kv_smooth_quant",
     "nvfp4_kv_batched_workspace_bytes",
     "nvfp4_kv_smooth_quant_batched",
+    "nvfp4_kv_smooth_quant_headroom",
     "nvfp4_kv_stats_batched",
     "nvfp4_kv_quant_batched",
     "nvfp4_kv_dequant",
     "nvfp4_selftest_cvt",
+    "nvfp4_kv_shard_bytes",
+    "nvfp4_kv_pack_head_shards",
+    "nvfp4_kv_unpack_head_shards",
     "nvfp4_kvcache_slots_needed",
     "nvfp4_kvcache_init",
     "nvfp4_kvcache_append",
@@ -126,6 +130,9 @@ def load(path: str | None = None):
     lib.nvfp4_kv_smooth_quant_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp,
                                                   sz, vp]
     lib.nvfp4_kv_smooth_quant_batched.restype = i32
+    lib.nvfp4_kv_smooth_quant_headroom.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp,
+                                                   sz, vp]
+    lib.nvfp4_kv_smooth_quant_headroom.restype = i32
     lib.nvfp4_kv_stats_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, sz, vp]
     lib.nvfp4_kv_stats_batched.restype = i32
     lib.nvfp4_kv_quant_batched.argtypes = [ctypes.POINTER(nvfp4_kv_job), i32, i32, i64, i32, i32, vp, vp, sz, vp]
@@ -134,6 +141,12 @@ def load(path: str | None = None):
     lib.nvfp4_kv_dequant.restype = i32
     lib.nvfp4_selftest_cvt.argtypes = [vp, i64, vp, vp, vp, vp, vp]
     lib.nvfp4_selftest_cvt.restype = i32
+    lib.nvfp4_kv_shard_bytes.argtypes = [i64, i32, i32, i32, i32]
+    lib.nvfp4_kv_shard_bytes.restype = sz
+    lib.nvfp4_kv_pack_head_shards.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp]
+    lib.nvfp4_kv_pack_head_shards.restype = i32
+    lib.nvfp4_kv_unpack_head_shards.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.nvfp4_kv_unpack_head_shards.restype = i32
     P = ctypes.POINTER
     lib.nvfp4_kvcache_slots_needed.argtypes = [i32, i32, i32, i32]
     lib.nvfp4_kvcache_slots_needed.restype = i32
@@ -220,6 +233,11 @@ def nvfp4_kv_smooth_quant_batched(jobs, n_jobs, dt, T, H, D, dev_status, workspa
                                                 stream)
 
 
+def nvfp4_kv_smooth_quant_headroom(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream):
+    return load().nvfp4_kv_smooth_quant_headroom(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes,
+                                                 stream)
+
+
 def nvfp4_kv_stats_batched(jobs, n_jobs, dt, T, H, D, workspace, workspace_bytes, stream):
     return load().nvfp4_kv_stats_batched(jobs, n_jobs, dt, T, H, D, workspace, workspace_bytes, stream)
 
@@ -234,6 +252,19 @@ def nvfp4_kv_dequant(codes, scales, tensor_scale, mean, tokens_per_group, T, H, 
 
 def nvfp4_selftest_cvt(x, n, e2m1_codes, e4m3_codes, e2m1_pair_f16x2, e4m3_values, stream):
     return load().nvfp4_selftest_cvt(x, n, e2m1_codes, e4m3_codes, e2m1_pair_f16x2, e4m3_values, stream)
+
+
+def nvfp4_kv_shard_bytes(T, H, D, P, with_mean):
+    return load().nvfp4_kv_shard_bytes(T, H, D, P, with_mean)
+
+
+def nvfp4_kv_pack_head_shards(codes, scales, tensor_scale, mean, T, H, D, P, out, stream):
+    return load().nvfp4_kv_pack_head_shards(codes, scales, tensor_scale, mean, T, H, D, P, out, stream)
+
+
+def nvfp4_kv_unpack_head_shards(src, T, H, D, P, with_mean, codes, scales, tensor_scales, means, stream):
+    return load().nvfp4_kv_unpack_head_shards(src, T, H, D, P, with_mean, codes, scales, tensor_scales, means,
+                                              stream)
 
 
 def nvfp4_kvcache_slots_needed(frames_per_chunk, global_sink, shot_sink, window):

@@ -88,8 +88,12 @@ nvfp4_status check_job(const nvfp4_kv_job& j, int64_t T) {
 
 enum KvPhase : int { kPhaseStats = 1, kPhaseQuant = 2, kPhaseBoth = 3 };
 
+constexpr float kDenomStandard = 6.0f * 448.0f;  // g maps the tensor amax to 6 x the largest E4M3
+constexpr float kDenomHeadroom = 4.0f * 448.0f;  // g leaves every block's 4-candidate under 448
+
 nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H, int D,
-                    int* dev_status, void* workspace, size_t workspace_bytes, void* stream, int phases) {
+                    int* dev_status, void* workspace, size_t workspace_bytes, void* stream, int phases,
+                    float denom = kDenomStandard) {
   if (!jobs || n_jobs < 1) return NVFP4_EINVAL;
   if (dt != NVFP4_IN_BF16 && dt != NVFP4_IN_FP32) return NVFP4_EINVAL;
   if (!kv_shape_ok(T, H, D)) return NVFP4_ESHAPE;
@@ -133,6 +137,7 @@ nvfp4_status kv_run(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int
       j.part = reinterpret_cast<float4*>(base + plan.ctr_bytes + plan.mean_bytes);
     }
     KvGeom g = plan.geo;
+    g.denom = denom;
     g.rows_per_stage = stats_stage_rows(g, bf16);
     g.header = reinterpret_cast<unsigned*>(ws);
     g.dev_status = dev_status;
@@ -198,6 +203,13 @@ nvfp4_status nvfp4_kv_smooth_quant_batched(const nvfp4_kv_job* jobs, int n_jobs,
                                            int H, int D, int* dev_status, void* workspace, size_t workspace_bytes,
                                            void* stream) {
   return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream, kPhaseBoth);
+}
+
+nvfp4_status nvfp4_kv_smooth_quant_headroom(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T,
+                                            int H, int D, int* dev_status, void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  return kv_run(jobs, n_jobs, dt, T, H, D, dev_status, workspace, workspace_bytes, stream, kPhaseBoth,
+                kDenomHeadroom);
 }
 
 nvfp4_status nvfp4_kv_stats_batched(const nvfp4_kv_job* jobs, int n_jobs, nvfp4_in_dtype dt, int64_t T, int H,

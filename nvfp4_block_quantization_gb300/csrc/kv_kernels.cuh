@@ -46,6 +46,7 @@ struct KvGeom {
   int rpp;  // rows in parallel: kStatsConsumers / tpr
   int rows_per_stage;
   double inv_T;  // binary64 reciprocal of T: mean = fl32(sum * inv_T)
+  float denom;   // tensor scale g = fl(amax / denom): 2688 (6 * 448), or 1792 (4 * 448) with headroom
   unsigned* header;  // [0] quant CTAs finished, [1] status flags
   int* dev_status;
   int first_launch;  // 1: write *dev_status, 0: OR into it

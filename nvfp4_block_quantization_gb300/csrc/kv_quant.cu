@@ -20,7 +20,7 @@
 // The grid is a programmatic dependent of the statistics grid and may run beside
 // it: each CTA fetches its first rows, waits (bounded) until every statistics
 // CTA has counted itself ready for this CTA's job, reads the job's amax, and
-// builds the per-tensor table: g = fl(amax / 2688) and, per E4M3 code E,
+// builds the per-tensor table: g = fl(amax / 2688) (or / 1792 with headroom) and, per E4M3 code E,
 // fl(1 / fl(E * g)) and E * E.  Once every CTA has read the counters it needs
 // (before its rows), the last of them resets the jobs' counters in the
 // workspace and publishes the status word.
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256, 2) kv_quant_kernel(const __grid_constant_
   const unsigned amax_bits = qc.ok ? *reinterpret_cast<volatile const unsigned*>(J.ctr) : 0x7fc00000u;
   const float amax = __uint_as_float(amax_bits);
   const bool nonfinite = !finite_f(amax);
-  const float g = nonfinite ? __int_as_float(0x7fc00000) : __fdiv_rn(amax, kTensorDenom);
+  const float g = nonfinite ? __int_as_float(0x7fc00000) : __fdiv_rn(amax, G.denom);
   for (int e = threadIdx.x; e < 128; e += blockDim.x) {
     const float E = e4m3_value((uint32_t)e);
     const float Sc = __fmul_rn(E, g);

@@ -151,3 +151,26 @@ def test_many_tensor_batch_matches_the_oracle(nv, oracle, n_jobs):
             assert np.array_equal(o.mean.cpu().numpy().view(np.uint32), ref["mean"].view(np.uint32)), j
         assert np.array_equal(o.scales.cpu().numpy(), ref["scales"]), j
         assert np.array_equal(o.codes.cpu().numpy(), ref["codes"]), j
+
+
+def test_headroom_tensor_scale_matches_the_oracle(nv, oracle):
+    """g = amax / 1792 (every block's 4-candidate under 448): codes, scales and g
+    bit-exact against the oracle's headroom statement, K smoothed and V not."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K, V = W.tiny_kv(0)
+    Kb = W.to_bf16_bits(W.random_kv(21, 96, 3, 64))
+    for arrays in ((K, V), (Kb, W.to_bf16_bits(W.random_kv(22, 96, 3, 64, offset_sd=0.0)))):
+        xs = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda() if a.dtype == np.uint16
+              else torch.from_numpy(a).cuda() for a in arrays]
+        outs, status = nv.kv_smooth_quant_batched(xs, [True, False], headroom=True)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for a, smooth, o in zip(arrays, (True, False), outs):
+            ref = oracle.kv_smooth_quant(a, smooth=smooth, headroom=True)
+            assert np.float32(o.tensor_scale.item()).view(np.uint32) == np.float32(ref["g"]).view(np.uint32)
+            assert np.array_equal(o.scales.cpu().numpy(), ref["scales"])
+            assert np.array_equal(o.codes.cpu().numpy(), ref["codes"])
+            # the amax block can now pick 4: with the standard scale it never does
+            std = oracle.kv_smooth_quant(a, smooth=smooth)
+            assert not np.array_equal(std["scales"], ref["scales"])

@@ -446,11 +446,12 @@ nvfp4_status nvfp4_weight_dequant_2d(const uint8_t* codes, const uint8_t* scales
 /* step 6: a W4A4 model).                                                   */
 /* ------------------------------------------------------------------------ */
 /* Y[M][N] = bf16_rne(fl(gX * gW) * sum_k (QX * EX)[m][k] * (QW * EW)[n][k]), the
- * sum accumulated in fp32 by the tensor cores (cuBLASLt, E2M1 operands with
- * VEC16 UE4M3 block scales).  X is an activation quantized by the 1-D
- * quantizer (nvfp4_kv_smooth_quant with H = 1, D = K, no smoothing): codes
- * [M][K/2], scales [M][K/16].  W is a weight quantized by
- * nvfp4_weight_quant_2d: codes [N][K/2], scales [N/16][K/16].
+ * sum accumulated in fp32 by the tensor cores (a hand-written tcgen05 kernel:
+ * E2M1 operands with one UE4M3 block scale per 16 elements of K, fp32
+ * accumulation in TMEM).  X is an activation quantized by the 1-D quantizer
+ * (nvfp4_kv_smooth_quant with H = 1, D = K, no smoothing): codes [M][K/2],
+ * scales [M][K/16].  W is a weight quantized by nvfp4_weight_quant_2d: codes
+ * [N][K/2], scales [N/16][K/16].
  *
  * The tensor cores read block scales in their own layout: per operand, tiles
  * of 128 rows x 4 blocks (64 elements of K), 512 bytes each, K tiles fastest;
@@ -501,14 +502,19 @@ nvfp4_status nvfp4_act_quant_mma(const void* x, int64_t M, int64_t K, int use_rh
                                  uint8_t* scales_mma, float* tensor_scale, int* dev_status, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
-/* Device workspace of nvfp4_gemm_w4a4 (256-byte aligned; no zero-fill needed). */
+/* Device workspace of nvfp4_gemm_w4a4 (256-byte aligned).  Its first int32 is
+ * an error flag: the kernel sets it to 1 when one of its bounded waits (about
+ * two seconds each) gave up, in which case Y is incomplete.  The kernel never
+ * clears it: zero the workspace once, before the first call, to read it. */
 size_t nvfp4_gemm_workspace_bytes(void);
 
-/* A GEMM plan for one shape: the cuBLASLt handle, descriptors and algorithm.
- * It is the one object the library allocates, in host memory; the caller owns
- * it and frees it with nvfp4_gemm_plan_destroy.  A plan serves one host thread
- * at a time.  M >= 1, N a multiple of 16, K a multiple of 32 (NVFP4_ESHAPE
- * otherwise); NVFP4_ECUDA when cuBLASLt has no algorithm for the shape. */
+/* A GEMM plan for one shape: the shape, the SM count (the kernel is
+ * persistent, one CTA per SM) and the driver's tensor-map encoder.  It is the
+ * one object the library allocates, in host memory; the caller owns it and
+ * frees it with nvfp4_gemm_plan_destroy.  A plan serves one host thread at a
+ * time.  M >= 1, N a multiple of 16, K a multiple of 32, M * N <= 2^46
+ * (NVFP4_ESHAPE otherwise); NVFP4_ECUDA when the device or the driver's
+ * encoder is unavailable. */
 typedef struct nvfp4_gemm_plan nvfp4_gemm_plan;
 nvfp4_status nvfp4_gemm_plan_create(int64_t M, int64_t N, int64_t K, nvfp4_gemm_plan** plan);
 void nvfp4_gemm_plan_destroy(nvfp4_gemm_plan* plan);
@@ -518,7 +524,10 @@ void nvfp4_gemm_plan_destroy(nvfp4_gemm_plan* plan);
  *   x_scales_mma, w_scales_mma device, the tensor-core layout, 16-byte aligned
  *   x_tensor_scale, w_tensor_scale  device fp32 [1] (gX, gW)
  *   y_bf16                    device [M][N] bf16, 16-byte aligned
- *   workspace                 device, nvfp4_gemm_workspace_bytes() */
+ *   workspace                 device, nvfp4_gemm_workspace_bytes(), the error flag above
+ * The codes are read through TMA tensor maps encoded on the host at each call
+ * (boxes of 128 bytes of K by 128 or 256 rows); NVFP4_ECUDA if encoding or the
+ * launch fails. */
 nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, const uint8_t* x_scales_mma,
                              const float* x_tensor_scale, const uint8_t* w_codes, const uint8_t* w_scales_mma,
                              const float* w_tensor_scale, void* y_bf16, void* workspace, size_t workspace_bytes,

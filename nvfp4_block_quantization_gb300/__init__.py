@@ -455,7 +455,7 @@ class GemmPlan:
 
 def gemm_workspace(device=None):
     torch = _torch()
-    return torch.empty(_lib.nvfp4_gemm_workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(_lib.nvfp4_gemm_workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
 
 
 def gemm_w4a4(plan: GemmPlan, x_codes, x_scales_mma, x_tensor_scale, w_codes, w_scales_mma, w_tensor_scale,

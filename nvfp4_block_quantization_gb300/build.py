@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         objs = list(ex.map(compile_one, _sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
-    r = subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib],
+    r = subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-Xlinker", "-rpath=" + cuda_lib],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

@@ -7,41 +7,73 @@
 // scales for weights and 1-D block scales for activations; inference step 6
 // merges the weights into a W4A4 model.
 //
-// The contraction is a dense block-scaled FP4 GEMM, so it runs on the tensor
-// cores through cuBLASLt (E2M1 operands, VEC16 UE4M3 block scales, fp32
-// accumulation).  This file adds what the library needs around it:
-//   - the block scales rearranged into the tensor cores' scale layout: tiles of
-//     128 rows x 4 blocks (512 bytes, rows r % 32 at 16-byte steps, r / 32 at
-//     4-byte steps, the block within the tile at 1-byte steps), K tiles
-//     fastest, zeros in the padding; a weight tile's scale is repeated for its
-//     16 rows;
-//   - alpha = gX * gW computed on the device, so the call never reads device
-//     memory on the host;
-//   - a caller-owned plan holding the cuBLASLt handle, descriptors and the
-//     chosen algorithm.
+// The contraction is a dense block-scaled FP4 GEMM on the 5th-generation
+// tensor cores, written here directly (tcgen05.mma kind::mxf4nvf4, one UE4M3
+// scale per 16 elements of K on each operand, fp32 accumulation in TMEM), in a
+// persistent kernel, one CTA per SM walking 128 x 256 tiles of Y:
+//   - a TMA thread streams 128-byte-swizzled K slices of 256 elements of X and
+//     W codes, with the matching scale tiles (plain bulk copies), into a
+//     4-stage shared-memory ring that runs on across tiles;
+//   - four scale warps move each slice's scales from shared memory into TMEM
+//     (tcgen05.st), so the tensor-pipe queue holds MMAs only;
+//   - one MMA thread issues the slice's four 128 x 256 x 64 MMAs;
+//     tcgen05.commit frees the stage;
+//   - eight epilogue warps read the accumulator, scale it by
+//     alpha = fl(gX * gW), round to bf16, hand TMEM back to the MMA thread and
+//     write Y through a swizzled shared-memory buffer in whole 32-byte sectors.
+// The block scales sit in the tensor cores' scale layout: tiles of 128 rows x
+// 4 blocks (512 bytes, rows r % 32 at 16-byte steps, r / 32 at 4-byte steps,
+// the block within the tile at 1-byte steps), K tiles fastest, zeros in the
+// padding; a weight tile's scale is repeated for its 16 rows.  In TMEM the
+// MMA reads a K step's scales of row r from lane r % 32 of every 32-lane
+// quadrant, column r / 32 of that step's 4 columns: one 512-byte tile, lane l
+// taking bytes 16 l .. 16 l + 15, written to all four quadrants.
 #include <cstring>
 #include <new>
 
-#include <cublasLt.h>
+#include <cuda.h>  // CUtensorMap and its enums; the encoder comes through the runtime's driver entry point
 
 #include "nvfp4.h"
+#include "bulk.cuh"
 #include "common.cuh"
 #include "rht16.cuh"
 
+typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                         const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                         CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
 struct nvfp4_gemm_plan {
   int64_t M, N, K;
-  cublasLtHandle_t handle;
-  cublasLtMatmulDesc_t op;
-  cublasLtMatrixLayout_t lw, lx, ly;
-  cublasLtMatmulAlgo_t algo;
-  size_t algo_workspace;
+  int sms;  // persistent grid: one CTA per SM
+  TensorMapEncodeTiled encode;
 };
 
 namespace nvfp4 {
 namespace {
 
-constexpr size_t kGemmWorkspace = (size_t)32 << 20;  // cuBLASLt workspace offered to the heuristic
-constexpr size_t kScalarBytes = 256;                 // alpha and beta at the front of the workspace
+// ---- the tcgen05 GEMM's tile and pipeline ---------------------------------
+constexpr int kBM = 128;                     // rows of X (and of Y) per CTA
+constexpr int kBN = 256;                     // rows of W (columns of Y) per CTA
+constexpr int kBK = 256;                     // K elements per pipeline stage: 128 bytes of codes per row
+constexpr int kStages = 4;
+constexpr int kMmaK = 64;                    // K elements per tcgen05.mma (kind::mxf4nvf4)
+constexpr int kABytes = kBM * kBK / 2;       // 16 KB of X codes per stage
+constexpr int kBBytes = kBN * kBK / 2;       // 32 KB of W codes per stage
+constexpr int kSfaBytes = kBM * kBK / 16;    // 2 KB: 4 scale tiles of 512 bytes
+constexpr int kSfbBytes = kBN * kBK / 16;    // 4 KB: 2 row tiles x 4 scale tiles
+constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
+constexpr int kEpiStageBytes = 32 * 32;      // per epilogue warp: 32 rows x 16 bf16 columns
+constexpr int kGemmSmem = kStages * kStageBytes + kEpiWarps * kEpiStageBytes + 1024 + 256;  // + alignment + barriers
+constexpr int kTmemCols = 512;
+constexpr int kTmemSf = 256;                 // scale columns follow the 256 accumulator columns
+constexpr int kSfColsPerMma = 16;            // W's two row tiles at +0 (8 columns), X's tile at +8 (4), 4 spare
+constexpr int kSfColsPerStage = (kBK / kMmaK) * kSfColsPerMma;
+static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
+static_assert(kGemmSmem <= 232448, "shared memory per CTA");
+static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of 128-byte swizzling");
+
+constexpr size_t kScalarBytes = 256;         // the workspace: word 0 is the bounded-wait error flag
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -97,9 +129,280 @@ __global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ x, 
   }
 }
 
-__global__ void alpha_kernel(const float* __restrict__ gx, const float* __restrict__ gw, float* __restrict__ ab) {
-  ab[0] = __fmul_rn(*gx, *gw);
-  ab[1] = 0.0f;
+// Shared-memory matrix descriptor of tcgen05 (start address, leading and
+// stride byte offsets in 16-byte units, version 1, layout type in bits 61-63).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+constexpr uint32_t kLayoutNone = 0, kLayoutSw128 = 2;
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+struct GemmArgs {
+  const uint8_t* sfa;   // X scales, tensor-core layout
+  const uint8_t* sfb;   // W scales, tensor-core layout
+  const float* gx;
+  const float* gw;
+  uint16_t* y;          // bf16 [M][N]
+  int M, N, K;
+  int kbt;              // scale tiles along K: ceil(K / 64)
+  int* err;
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t r[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Persistent: one CTA per SM walks the 128 x 256 tiles of Y (tile t = blockIdx.x
+// + i gridDim.x, W tiles fastest).  Fourteen warps:
+//   warp 0, one lane   loads: the stage ring runs on across tiles, so the next
+//                      tile's first stages arrive while the epilogue drains;
+//   warp 1, one lane   issues each stage's four MMAs once its scales are in
+//                      TMEM; waits for the epilogue to hand the accumulator back
+//                      before a new tile's first MMA;
+//   warps 2..5         scales: warp w writes TMEM lane quadrant w % 4 with
+//                      tcgen05.st -- for K step j of stage s, the 16 columns at
+//                      256 + 64 s + 16 j hold W's row tiles 0 and 1 (4 columns
+//                      each) and X's tile (4 columns), lane l of every quadrant
+//                      holding rows l, l + 32, l + 64, l + 96 of a tile in
+//                      consecutive columns; the tensor-pipe queue then carries
+//                      MMAs only;
+//   warps 6..13        the epilogue: warp w reads lane quadrant w % 4 (its 32
+//                      rows) and one half of the 256 columns, rounds alpha * acc
+//                      to bf16 in registers, frees the accumulator, then writes
+//                      the rows through a swizzled shared-memory buffer (16
+//                      columns at a time) so that each store instruction covers
+//                      whole 32-byte sectors of 16 rows.
+// A stage's TMEM scale slot is rewritten only after its smem stage was
+// refilled, which waits for the MMAs that read the slot.  Every wait is bounded;
+// on a timeout the CTA records it, stops issuing work, waits (bounded) for what
+// it issued and frees TMEM.
+constexpr int kScaleWarps = 4;
+constexpr int kGemmThreads = 32 * (2 + kScaleWarps + kEpiWarps);
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_x,
+                                                                    const __grid_constant__ CUtensorMap map_w,
+                                                                    GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* epi_stage = smem + kStages * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + kEpiWarps * kEpiStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* sf_ready = empty + kStages;
+  uint64_t* acc_full = sf_ready + kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* failed = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* vfailed = failed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_n = (a.N + kBN - 1) / kBN;
+  const int tiles = tiles_n * ((a.M + kBM - 1) / kBM);
+  const int nkb = (a.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], kScaleWarps);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);
+    mbar_init(drain, 1);
+    *failed = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- loads ----
+      uint32_t g = 0;  // stages issued so far (all tiles)
+      for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x) {
+        const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
+        const int n_rt = min(kBN, a.N - n0) > 128 ? 2 : 1;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1)) { atomicExch(failed, 1); break; }
+          uint8_t* st = smem + s * kStageBytes;
+          const int kt0 = kb * (kBK / kMmaK);
+          const int nkt = min(kBK / kMmaK, a.kbt - kt0);
+          mbar_expect_tx(&full[s], kABytes + kBBytes + 512u * nkt * (1 + n_rt));
+          tma_load_2d(st, &map_x, kb * (kBK / 2), m0, &full[s]);
+          tma_load_2d(st + kABytes, &map_w, kb * (kBK / 2), n0, &full[s]);
+          bulk_load(st + kABytes + kBBytes, a.sfa + ((size_t)(m0 / 128) * a.kbt + kt0) * 512, 512u * nkt, &full[s]);
+          for (int rt = 0; rt < n_rt; ++rt)
+            bulk_load(st + kABytes + kBBytes + kSfaBytes + rt * (kSfbBytes / 2),
+                      a.sfb + ((size_t)(n0 / 128 + rt) * a.kbt + kt0) * 512, 512u * nkt, &full[s]);
+        }
+      }
+      // copies still in flight land before the CTA leaves
+      for (uint32_t q = g > (uint32_t)kStages ? g - kStages : 0; q < g; ++q)
+        if (!mbar_wait(&full[q % kStages], (q / kStages) & 1)) atomicExch(failed, 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMAs ----
+      uint32_t g = 0;
+      int i = 0;
+      for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x, ++i) {
+        const int n_tile = min(kBN, a.N - (t % tiles_n) * kBN);
+        const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(((n_tile + 15) & ~15) >> 3) << 17) |
+                               ((uint32_t)(kBM >> 4) << 24);  // E2M1 x E2M1, UE4M3 scales, K-major, fp32 D
+        if (i > 0 && !mbar_wait(acc_empty, (i - 1) & 1)) { atomicExch(failed, 1); break; }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&sf_ready[s], (g / kStages) & 1)) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t st = smem_u32(smem + s * kStageBytes);
+          const int nkt = min(kBK / kMmaK, a.kbt - kb * (kBK / kMmaK));
+          for (int j = 0; j < nkt; ++j) {
+            const uint32_t sfb_col = tmem + kTmemSf + s * kSfColsPerStage + j * kSfColsPerMma, sfa_col = sfb_col + 8;
+            const uint64_t da = umma_desc(st + j * (kMmaK / 2), 16, 1024, kLayoutSw128);
+            const uint64_t db = umma_desc(st + kABytes + j * (kMmaK / 2), 16, 1024, kLayoutSw128);
+            const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                ::"r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(sfa_col), "r"(sfb_col), "r"(acc) : "memory");
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) { atomicExch(failed, 1); break; }
+        umma_commit(acc_full);
+      }
+      // every MMA issued above has finished before TMEM is freed
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0)) atomicExch(failed, 1);
+    }
+  } else if (warp < 2 + kScaleWarps) {
+    // ---- scales: shared memory -> registers -> TMEM ----
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t g = 0;
+    for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x) {
+      const int n_rt = min(kBN, a.N - (t % tiles_n) * kBN) > 128 ? 2 : 1;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1));  // warp-uniform: tcgen05.st is .aligned
+        if (!ok) break;
+        const uint8_t* sf = smem + s * kStageBytes + kABytes + kBBytes;
+        const int nkt = min(kBK / kMmaK, a.kbt - kb * (kBK / kMmaK));
+        for (int j = 0; j < nkt; ++j) {
+          uint32_t r[16];
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sf + kSfaBytes + j * 512 + lane * 16);
+          const uint4 b1 = n_rt == 2 ? *reinterpret_cast<const uint4*>(sf + kSfaBytes + kSfbBytes / 2 + j * 512 + lane * 16)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 a0 = *reinterpret_cast<const uint4*>(sf + j * 512 + lane * 16);
+          r[0] = b0.x; r[1] = b0.y; r[2] = b0.z; r[3] = b0.w;
+          r[4] = b1.x; r[5] = b1.y; r[6] = b1.z; r[7] = b1.w;
+          r[8] = a0.x; r[9] = a0.y; r[10] = a0.z; r[11] = a0.w;
+          r[12] = 0u; r[13] = 0u; r[14] = 0u; r[15] = 0u;
+          tmem_st16(lane_base + kTmemSf + s * kSfColsPerStage + j * kSfColsPerMma, r);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[s]);
+      }
+      if (!ok) { atomicExch(failed, 1); break; }
+    }
+  } else {
+    // ---- epilogue: TMEM -> alpha * acc -> bf16 registers -> shared -> Y ----
+    const int e = warp - 2 - kScaleWarps;
+    const int quad = warp & 3, half = e >> 2;  // half 0: columns 0..127, half 1: columns 128..255
+    uint8_t* stg = epi_stage + e * kEpiStageBytes;
+    const float alpha = __fmul_rn(*a.gx, *a.gw);
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, i & 1));  // warp-uniform: tcgen05.ld is .aligned
+      if (!ok) { atomicExch(failed, 1); break; }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
+      const int cols = min(128, a.N - n0 - half * 128);  // this warp's valid columns (a multiple of 16, maybe <= 0)
+      uint32_t o[64];  // row `lane`, 128 columns as bf16 pairs
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 32 * c4, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(__fmul_rn(alpha, __uint_as_float(v[2 * q])),
+                                                                     __fmul_rn(alpha, __uint_as_float(v[2 * q + 1]))));
+          o[16 * c4 + q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);  // the MMAs of the next tile may overwrite TMEM now
+#pragma unroll
+      for (int h8 = 0; h8 < 8; ++h8) {
+        if (h8 * 16 >= cols) break;
+        // row `lane` of this warp's 32 rows: 2 chunks of 16 bytes, chunk c at (c ^ ((lane / 4) % 2)) * 16
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          *reinterpret_cast<uint4*>(stg + lane * 32 + ((c ^ ((lane >> 2) & 1)) << 4)) =
+              make_uint4(o[8 * h8 + 4 * c], o[8 * h8 + 4 * c + 1], o[8 * h8 + 4 * c + 2], o[8 * h8 + 4 * c + 3]);
+        __syncwarp();
+        // sixteen rows per store instruction: lanes 2 j, 2 j + 1 write the two chunks of row 16 r + j
+        const int c = lane & 1;
+        const int col = n0 + half * 128 + h8 * 16 + c * 8;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int rr = 16 * r + (lane >> 1);
+          const int row = m0 + quad * 32 + rr;
+          const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 32 + ((c ^ ((rr >> 2) & 1)) << 4));
+          if (row < a.M) *reinterpret_cast<uint4*>(a.y + (size_t)row * a.N + col) = val;
+        }
+        __syncwarp();
+      }
+    }
+  }
+  __syncwarp();
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0 && *vfailed) atomicExch(a.err, 1);
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -126,14 +429,17 @@ nvfp4_status launch_scales(const uint8_t* in, int64_t rows, int64_t kblocks, boo
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
-void destroy(nvfp4_gemm_plan* p) {
-  if (!p) return;
-  if (p->ly) cublasLtMatrixLayoutDestroy(p->ly);
-  if (p->lx) cublasLtMatrixLayoutDestroy(p->lx);
-  if (p->lw) cublasLtMatrixLayoutDestroy(p->lw);
-  if (p->op) cublasLtMatmulDescDestroy(p->op);
-  if (p->handle) cublasLtDestroy(p->handle);
-  delete p;
+// A K-major code matrix [rows][K/2] bytes as a TMA tensor: boxes of 128 bytes
+// (256 elements of K) x box_rows rows, 128-byte swizzled, zeros outside.
+bool encode_codes(TensorMapEncodeTiled enc, CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K,
+                  uint32_t box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -180,57 +486,37 @@ nvfp4_status nvfp4_rht16(const void* x, nvfp4_in_dtype dt, int64_t rows, int64_t
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
-size_t nvfp4_gemm_workspace_bytes(void) { return nvfp4::kScalarBytes + nvfp4::kGemmWorkspace; }
+size_t nvfp4_gemm_workspace_bytes(void) { return nvfp4::kScalarBytes; }
 
 nvfp4_status nvfp4_gemm_plan_create(int64_t M, int64_t N, int64_t K, nvfp4_gemm_plan** plan) {
   if (!plan) return NVFP4_EINVAL;
   *plan = nullptr;
   if (M < 1 || N < 16 || (N % 16) != 0 || K < 32 || (K % 32) != 0) return NVFP4_ESHAPE;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ESHAPE;
+  if (((M + nvfp4::kBM - 1) / nvfp4::kBM) * ((N + nvfp4::kBN - 1) / nvfp4::kBN) > INT32_MAX) return NVFP4_ESHAPE;
+  if (M * N > ((int64_t)1 << 46)) return NVFP4_ESHAPE;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return NVFP4_ECUDA;
+  if (cudaFuncSetAttribute(nvfp4::gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nvfp4::kGemmSmem) !=
+      cudaSuccess)
+    return NVFP4_ECUDA;
+  const int sms = nvfp4::sm_count();
+  if (sms <= 0) return NVFP4_ECUDA;
   nvfp4_gemm_plan* p = new (std::nothrow) nvfp4_gemm_plan;
   if (!p) return NVFP4_ECUDA;
-  std::memset(p, 0, sizeof(*p));
   p->M = M;
   p->N = N;
   p->K = K;
-  bool ok = cublasLtCreate(&p->handle) == CUBLAS_STATUS_SUCCESS &&
-            cublasLtMatmulDescCreate(&p->op, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS;
-  // Y^T (N x M, column-major) = W (N x K) * X^T: both operands K-contiguous
-  const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-  const int32_t mode = CUBLASLT_MATMUL_MATRIX_SCALE_VEC16_UE4M3;
-  const cublasLtPointerMode_t pm = CUBLASLT_POINTER_MODE_DEVICE;
-  const void* placeholder = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));  // set per call
-  ok = ok && cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_A_SCALE_MODE, &mode, sizeof(mode)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_B_SCALE_MODE, &mode, sizeof(mode)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_A_SCALE_POINTER, &placeholder, sizeof(placeholder)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &placeholder, sizeof(placeholder)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulDescSetAttribute(p->op, CUBLASLT_MATMUL_DESC_POINTER_MODE, &pm, sizeof(pm)) == CUBLAS_STATUS_SUCCESS;
-  ok = ok && cublasLtMatrixLayoutCreate(&p->lw, CUDA_R_4F_E2M1, (uint64_t)K, (uint64_t)N, K) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatrixLayoutCreate(&p->lx, CUDA_R_4F_E2M1, (uint64_t)K, (uint64_t)M, K) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatrixLayoutCreate(&p->ly, CUDA_R_16BF, (uint64_t)N, (uint64_t)M, N) == CUBLAS_STATUS_SUCCESS;
-  cublasLtMatmulPreference_t pref = nullptr;
-  cublasLtMatmulHeuristicResult_t res;
-  std::memset(&res, 0, sizeof(res));
-  int found = 0;
-  const size_t cap = nvfp4::kGemmWorkspace;
-  ok = ok && cublasLtMatmulPreferenceCreate(&pref) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &cap, sizeof(cap)) == CUBLAS_STATUS_SUCCESS &&
-       cublasLtMatmulAlgoGetHeuristic(p->handle, p->op, p->lw, p->lx, p->ly, p->ly, pref, 1, &res, &found) == CUBLAS_STATUS_SUCCESS &&
-       found >= 1;
-  if (pref) cublasLtMatmulPreferenceDestroy(pref);
-  if (!ok) {
-    nvfp4::destroy(p);
-    return NVFP4_ECUDA;
-  }
-  p->algo = res.algo;
-  p->algo_workspace = res.workspaceSize;
+  p->encode = reinterpret_cast<TensorMapEncodeTiled>(fn);
+  p->sms = sms;
   *plan = p;
   return NVFP4_OK;
 }
 
-void nvfp4_gemm_plan_destroy(nvfp4_gemm_plan* plan) { nvfp4::destroy(plan); }
+void nvfp4_gemm_plan_destroy(nvfp4_gemm_plan* plan) { delete plan; }
 
 nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, const uint8_t* x_scales_mma,
                              const float* x_tensor_scale, const uint8_t* w_codes, const uint8_t* w_scales_mma,
@@ -245,20 +531,25 @@ nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, cons
     return NVFP4_EALIGN;
   if (!workspace || !nvfp4::aligned_to(workspace, 256) || workspace_bytes < nvfp4_gemm_workspace_bytes())
     return NVFP4_EWORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* ab = static_cast<float*>(workspace);  // [0] alpha = gX * gW, [1] beta = 0
-  nvfp4::alpha_kernel<<<1, 1, 0, s>>>(x_tensor_scale, w_tensor_scale, ab);
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ECUDA;
-  if (cublasLtMatmulDescSetAttribute(plan->op, CUBLASLT_MATMUL_DESC_A_SCALE_POINTER, &w_scales_mma,
-                                     sizeof(w_scales_mma)) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatmulDescSetAttribute(plan->op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &x_scales_mma,
-                                     sizeof(x_scales_mma)) != CUBLAS_STATUS_SUCCESS)
+  CUtensorMap mx, mw;
+  if (!nvfp4::encode_codes(plan->encode, &mx, x_codes, plan->M, plan->K, nvfp4::kBM) ||
+      !nvfp4::encode_codes(plan->encode, &mw, w_codes, plan->N, plan->K, nvfp4::kBN))
     return NVFP4_ECUDA;
-  char* gemm_ws = static_cast<char*>(workspace) + nvfp4::kScalarBytes;
-  const cublasStatus_t st = cublasLtMatmul(plan->handle, plan->op, ab, w_codes, plan->lw, x_codes, plan->lx, ab + 1,
-                                           y_bf16, plan->ly, y_bf16, plan->ly, &plan->algo, gemm_ws,
-                                           nvfp4::kGemmWorkspace, s);
-  return st == CUBLAS_STATUS_SUCCESS ? NVFP4_OK : NVFP4_ECUDA;
+  nvfp4::GemmArgs a;
+  a.sfa = x_scales_mma;
+  a.sfb = w_scales_mma;
+  a.gx = x_tensor_scale;
+  a.gw = w_tensor_scale;
+  a.y = static_cast<uint16_t*>(y_bf16);
+  a.M = (int)plan->M;
+  a.N = (int)plan->N;
+  a.K = (int)plan->K;
+  a.kbt = (int)((plan->K + 63) / 64);
+  a.err = static_cast<int*>(workspace);
+  const int64_t tiles = ((plan->N + nvfp4::kBN - 1) / nvfp4::kBN) * ((plan->M + nvfp4::kBM - 1) / nvfp4::kBM);
+  const unsigned grid = (unsigned)(tiles < plan->sms ? tiles : plan->sms);
+  nvfp4::gemm_w4a4_kernel<<<grid, nvfp4::kGemmThreads, nvfp4::kGemmSmem, static_cast<cudaStream_t>(stream)>>>(mx, mw, a);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 
 }  // extern "C"

@@ -1,5 +1,5 @@
 """W4A4 NVFP4 GEMM without a GPU: the oracle reference against closed forms, and the
-C entry points' argument checks (which return before any CUDA or cuBLASLt call)."""
+C entry points' argument checks (which return before any CUDA call)."""
 import ctypes
 
 import numpy as np

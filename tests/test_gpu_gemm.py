@@ -52,9 +52,10 @@ def run_gemm(nv, xq, wq, M, N, K):
     xs = nv.mma_scales(xq.scales.view(M, K // 16), K)
     ws = nv.mma_scales(wq.scales, K, tile2d=True)
     plan = nv.GemmPlan(M, N, K)
-    y = nv.gemm_w4a4(plan, xq.codes.view(M, K // 2), xs, xq.tensor_scale, wq.codes, ws, wq.tensor_scale,
-                     nv.gemm_workspace())
+    work = nv.gemm_workspace()  # zeroed: its first int32 is the kernel's bounded-wait error flag
+    y = nv.gemm_w4a4(plan, xq.codes.view(M, K // 2), xs, xq.tensor_scale, wq.codes, ws, wq.tensor_scale, work)
     torch.cuda.synchronize()
+    assert int(work[:4].view(torch.int32).item()) == 0
     return y.float().cpu().numpy().astype(np.float64)
 
 
@@ -97,6 +98,24 @@ def test_w4a4_small_ragged(nv):
     X = rng.standard_normal((M, K)).astype(np.float32)
     Wm = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
     Wm.flat[rng.choice(Wm.size, Wm.size // 1000, replace=False)] *= 30.0
+    xq, wq = quantized_operands(nv, X, Wm)
+    y = run_gemm(nv, xq, wq, M, N, K)
+    ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2), host(xq.scales).reshape(M, K // 16),
+                             float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
+                             float(host(wq.tensor_scale)[0]))
+    check(y, ref, sabs, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 48, 96), (129, 272, 320), (1, 16, 32), (385, 512, 768)])
+def test_w4a4_tails(nv, M, N, K):
+    """Edges of the 128 x 256 output tiles and of the 256-element K slices: N = 16 past a tile
+    boundary, K not a multiple of 64 (a half-filled last MMA step), M = 1, an odd number of row
+    tiles; every output against the oracle."""
+    from oracle import gemm as og
+
+    rng = np.random.default_rng(M + N + K)
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    Wm = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
     xq, wq = quantized_operands(nv, X, Wm)
     y = run_gemm(nv, xq, wq, M, N, K)
     ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2), host(xq.scales).reshape(M, K // 16),

@@ -726,6 +726,8 @@ def row_gemm_w4a4(nv, W, torch, dev, peak):
                                                     w2q.tensor_scale, ws, out=y2), 4, 20)
     fl2 = 2.0 * M * N2 * K
     out["gemm_7040x14336x3072"] = {"TFLOP/s": fl2 / ms2 / 1e9, "ms": ms2, "frac": fl2 / ms2 / 1e9 / pk}
+    torch.cuda.synchronize()
+    out["kernel_error_flag"] = int(ws[:4].view(torch.int32).item())  # set by a bounded wait that gave up
 
     # random Hadamard transform of the activation (bf16 in, fp32 out: 6 bytes per element)
     signs = int(torch.randint(0, 1 << 16, (1,), generator=gen, device=dev).item())

@@ -191,6 +191,39 @@ def cpu_oracle_run(tokens: int, reps: int = 1):
     return elems * QUANT_BYTES_PER_ELEM / dt / 1e9, dt, elems
 
 
+def cpu_oracle_threads_run(tokens: int, threads: int):
+    """The same step on `threads` host threads (the oracle's threaded driver: bit-identical results);
+    returns (GB/s, seconds, elems)."""
+    import oracle
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    oracle.build()
+    K = W.to_bf16_bits(W.chunk_k(2000))[:tokens].copy()
+    V = W.to_bf16_bits(W.chunk_v(2001))[:tokens].copy()
+    t0 = time.perf_counter()
+    oracle.kv_smooth_quant_threads(K, True, threads)
+    oracle.kv_smooth_quant_threads(V, False, threads)
+    dt = time.perf_counter() - t0
+    elems = 2 * K.size
+    return elems * QUANT_BYTES_PER_ELEM / dt / 1e9, dt, elems
+
+
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86: model name; Arm: implementer and part), or ''."""
+    try:
+        info = {}
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ":" in ln:
+                    k, v = ln.split(":", 1)
+                    info.setdefault(k.strip(), v.strip())
+        if "model name" in info:
+            return info["model name"]
+        return " ".join(f"{k} {info[k]}" for k in ("CPU implementer", "CPU part") if k in info)
+    except OSError:
+        return ""
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
@@ -463,9 +496,15 @@ def run_ours(args, ws, rank):
         line["size_ceiling"] = size_ceiling_rows(torch, dev, l2)
     if not args.no_cpu and rank == 0:
         gbs, secs, elems = cpu_oracle_run(T_CHUNK)
+        nthreads = os.cpu_count() or 1
+        tgbs, tsecs, _ = cpu_oracle_threads_run(T_CHUNK, nthreads)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+                                "cpu_model": cpu_model(),
                                 "sample": f"the whole step: K (smoothed) and V of the 7040x24x128 chunk, "
-                                          f"{elems} elements, {secs:.1f} s single-threaded"}
+                                          f"{elems} elements, {secs:.1f} s single-threaded",
+                                "all_cores": {"value": tgbs, "unit": "GB/s", "cores": nthreads, "seconds": tsecs,
+                                              "kind": "oracle, threaded driver (channel, element and block ranges "
+                                                      "split over the host's cores; bit-identical results)"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -32,7 +32,7 @@ OK = 0
 NONFINITE = 1
 EINVAL = 2
 
-CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,9 @@ def _load():
         lib.oracle_kv_smooth_quant_headroom.argtypes = [c_void_p, c_int, c_int64, c_int64, c_int64, c_int,
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
         lib.oracle_kv_smooth_quant_headroom.restype = c_int
+        lib.oracle_kv_smooth_quant_threads.argtypes = [c_void_p, c_int, c_int64, c_int64, c_int64, c_int,
+                                                       c_void_p, c_void_p, c_void_p, c_void_p, c_int]
+        lib.oracle_kv_smooth_quant_threads.restype = c_int
         lib.oracle_tensor_scale_headroom.argtypes = [c_float]
         lib.oracle_tensor_scale_headroom.restype = c_float
         lib.oracle_kv_dequant.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
@@ -207,6 +210,23 @@ def kv_smooth_quant(x: np.ndarray, smooth: bool, mean_in: np.ndarray | None = No
     if rc == EINVAL:
         raise ValueError("oracle_kv_smooth_quant: invalid arguments")
     return dict(codes=codes, scales=scales, g=float(g[0]), mean=mean_out, chose4=chose4, status=rc)
+
+
+def kv_smooth_quant_threads(x: np.ndarray, smooth: bool, threads: int) -> dict:
+    """kv_smooth_quant on `threads` host threads (channel, element and block ranges split among
+    them; bit for bit the single-threaded results).  For timing the baseline on all cores.
+    Returns dict(codes, scales, g, mean, status) as kv_smooth_quant (no chose4)."""
+    x, dt = _as_input(x)
+    T, H, D = x.shape
+    codes = np.zeros((T, H, D // 2), dtype=np.uint8)
+    scales = np.zeros((T, H, D // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    mean_out = np.zeros((H, D), dtype=np.float32) if smooth else None
+    rc = _load().oracle_kv_smooth_quant_threads(_ptr(x), dt, T, H, D, int(bool(smooth)), _ptr(mean_out),
+                                                _ptr(codes), _ptr(scales), _ptr(g), int(threads))
+    if rc == EINVAL:
+        raise ValueError("oracle_kv_smooth_quant_threads: invalid arguments")
+    return dict(codes=codes, scales=scales, g=float(g[0]), mean=mean_out, status=rc)
 
 
 def kv_dequant(codes: np.ndarray, scales: np.ndarray, g, mean=None, tokens_per_group: int | None = None) -> np.ndarray:

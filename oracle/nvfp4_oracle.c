@@ -55,10 +55,18 @@
  *   R11 dequant: Xhat = bf16_rne(fl(fl(Q * fl(E * g)) + mean)), the mean term
  *       only when a mean is supplied.
  *
- * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math (no contraction of
- * a*b+c into FMA except the explicit fmaf() of R8).
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -pthread (no
+ * contraction of a*b+c into FMA except the explicit fmaf() of R8).
+ *
+ * oracle_kv_smooth_quant_threads runs the same statement on several host
+ * threads, for timing the baseline on all cores: each thread takes a range of
+ * channels (each channel's mean is still one binary64 sum in token order), of
+ * elements (amax is a maximum, so the order of the partial maxima does not
+ * matter) or of blocks (blocks are independent).  Its results are bit for bit
+ * those of the single-threaded function, which stays the statement of record.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -348,6 +356,120 @@ int oracle_kv_smooth_quant_headroom(const void* x, int dtype, int64_t T, int64_t
                                     const float* mean_in, float* mean_out, uint8_t* codes, uint8_t* scales,
                                     float* g_out, uint8_t* chose4) {
   return kv_smooth_quant_impl(x, dtype, T, H, D, smooth, mean_in, mean_out, codes, scales, g_out, chose4, 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The same quantizer on several host threads (see the header).              */
+/* ------------------------------------------------------------------------ */
+#define ORACLE_MAX_THREADS 256
+
+typedef struct {
+  const void* x;
+  int dtype, smooth, phase;
+  int64_t T, C;
+  float* mean;
+  float* z;
+  float g, k6, k4;
+  uint8_t* codes;
+  uint8_t* scales;
+  int64_t lo, hi; /* this thread's range of channels, elements or blocks */
+  float amax;     /* phase 2: the range's max |Z| */
+  int finite;     /* phase 2: every Z of the range finite */
+} mt_range;
+
+static void* mt_range_run(void* arg) {
+  mt_range* w = (mt_range*)arg;
+  if (w->phase == 1) { /* channel means, as oracle_channel_mean */
+    for (int64_t c = w->lo; c < w->hi; ++c) {
+      double s = 0.0;
+      for (int64_t t = 0; t < w->T; ++t) s += (double)load_elem(w->x, w->dtype, (size_t)(t * w->C + c));
+      w->mean[c] = (float)(s / (double)w->T);
+    }
+  } else if (w->phase == 2) { /* Z and amax (R3, R4) */
+    for (int64_t i = w->lo; i < w->hi; ++i) {
+      float xi = load_elem(w->x, w->dtype, (size_t)i);
+      float zi = w->smooth ? xi - w->mean[i % w->C] : xi;
+      w->z[i] = zi;
+      if (!isfinite(zi)) w->finite = 0;
+      else w->amax = fmaxf(w->amax, fabsf(zi));
+    }
+  } else { /* blocks (R5-R10) */
+    unsigned blk[16];
+    for (int64_t b = w->lo; b < w->hi; ++b) {
+      block_result r = quantize_block(w->z + 16 * b, 16, w->g, w->k6, w->k4, blk);
+      w->scales[b] = (uint8_t)r.scale;
+      for (int j = 0; j < 8; ++j) w->codes[8 * b + j] = (uint8_t)(blk[2 * j] | (blk[2 * j + 1] << 4));
+    }
+  }
+  return NULL;
+}
+
+/* Splits [0, n) into nthreads ranges of `phase` and runs them; a range whose
+ * thread cannot be started runs on the calling thread. */
+static void mt_phase(const mt_range* base, int phase, int64_t n, int nthreads, mt_range* w) {
+  pthread_t th[ORACLE_MAX_THREADS];
+  int started[ORACLE_MAX_THREADS];
+  for (int i = 0; i < nthreads; ++i) {
+    w[i] = *base;
+    w[i].phase = phase;
+    w[i].lo = n * i / nthreads;
+    w[i].hi = n * (i + 1) / nthreads;
+    w[i].amax = 0.0f;
+    w[i].finite = 1;
+  }
+  for (int i = 1; i < nthreads; ++i) started[i] = pthread_create(&th[i], NULL, mt_range_run, &w[i]) == 0;
+  mt_range_run(&w[0]);
+  for (int i = 1; i < nthreads; ++i) {
+    if (started[i]) pthread_join(th[i], NULL);
+    else mt_range_run(&w[i]);
+  }
+}
+
+/* oracle_kv_smooth_quant without mean_in / chose4, on nthreads (1..256) host
+ * threads.  mean_out optional.  Same returns and filler as the single-threaded
+ * function. */
+int oracle_kv_smooth_quant_threads(const void* x, int dtype, int64_t T, int64_t H, int64_t D, int smooth,
+                                   float* mean_out, uint8_t* codes, uint8_t* scales, float* g_out, int nthreads) {
+  if (T < 0 || H <= 0 || D <= 0 || (D % 16) != 0 || (dtype != 0 && dtype != 1)) return ORACLE_EINVAL;
+  if (nthreads < 1 || nthreads > ORACLE_MAX_THREADS || (!smooth && mean_out)) return ORACLE_EINVAL;
+  const int64_t C = H * D;
+  const int64_t N = T * C;
+  const int64_t NB = N / 16;
+  mt_range base, w[ORACLE_MAX_THREADS];
+  memset(&base, 0, sizeof(base));
+  base.x = x;
+  base.dtype = dtype;
+  base.smooth = smooth;
+  base.T = T;
+  base.C = C;
+  base.mean = (float*)calloc((size_t)C, sizeof(float));
+  base.z = (float*)malloc(sizeof(float) * (size_t)(N ? N : 1));
+  base.codes = codes;
+  base.scales = scales;
+  if (smooth) {
+    if (T > 0) mt_phase(&base, 1, C, nthreads, w);
+    if (mean_out) memcpy(mean_out, base.mean, sizeof(float) * (size_t)C);
+  }
+  mt_phase(&base, 2, N, nthreads, w);
+  float amax = 0.0f;
+  int finite = 1;
+  for (int i = 0; i < nthreads; ++i) {
+    amax = fmaxf(amax, w[i].amax);
+    finite = finite && w[i].finite;
+  }
+  if (!finite) {
+    memset(codes, 0, (size_t)N / 2);
+    memset(scales, 0x7F, (size_t)NB);
+    *g_out = NAN;
+    free(base.z); free(base.mean);
+    return ORACLE_NONFINITE;
+  }
+  base.g = oracle_tensor_scale(amax);
+  *g_out = base.g;
+  if (base.g != 0.0f) candidate_factors(base.g, &base.k6, &base.k4);
+  mt_phase(&base, 3, NB, nthreads, w);
+  free(base.z); free(base.mean);
+  return ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------------ */

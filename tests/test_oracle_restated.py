@@ -100,3 +100,23 @@ def test_restated_minifloats_match_the_c_encoders(oracle):
     mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 336.0, 448.0, 464.0, 2.0 ** -10], np.float32)
     assert np.array_equal(R.e2m1_encode(mids), oracle.e2m1_encode_array(mids))
     assert np.array_equal(R.e4m3_encode(mids), oracle.e4m3_encode_array(mids))
+
+
+@pytest.mark.parametrize("threads", [1, 3, 8])
+def test_threaded_driver_equals_the_single_threaded_oracle(oracle, threads):
+    """The multi-threaded driver used to time the baseline on all cores splits channels, elements
+    and blocks among threads; its outputs must be the single-threaded statement's, bit for bit."""
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    K = W.to_bf16_bits(W.chunk_k(2000))[:200]
+    V = W.to_bf16_bits(W.chunk_v(2001))[:200]
+    for x, smooth in ((K, True), (V, False), (W.tiny_kv(0)[0], True)):
+        a, b = oracle.kv_smooth_quant(x, smooth=smooth), oracle.kv_smooth_quant_threads(x, smooth, threads)
+        assert a["status"] == b["status"]
+        assert np.float32(a["g"]).view(np.uint32) == np.float32(b["g"]).view(np.uint32)
+        if smooth:
+            assert np.array_equal(a["mean"].view(np.uint32), b["mean"].view(np.uint32))
+        assert np.array_equal(a["scales"], b["scales"]) and np.array_equal(a["codes"], b["codes"])
+    bad = np.ones((3, 1, 16), np.float32)
+    bad[2, 0, 7] = np.nan
+    assert oracle.kv_smooth_quant_threads(bad, False, threads)["status"] == oracle.NONFINITE

@@ -366,6 +366,35 @@ nvfp4_status nvfp4_kv_attention_decode(const float* q, int n_q, const uint8_t* k
                                        int64_t tokens_per_frame, int H, int D, float scale, float* out,
                                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Attention of a block of query tokens (prefill: a whole new chunk) over one
+ * view of the cache on the tensor cores (inference steps 7 and 9).  Per view
+ * token t (pool row frame_row[t / L_f] + t % L_f, slot frame_meta[t / L_f]) and
+ * channel d, as nvfp4_kv_attention_decode:
+ *   k = Q S_k + k_mean[slot][h][d] (k_mean may be NULL),   v = Q S_v,
+ *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t.
+ * Computed as: K' = Q E_k and V' = Q E_v, exact in bf16, in shared memory;
+ * s = scale * (g_k (q . K') + q . mean) with q . K' summed in fp32 by
+ * tcgen05.mma and q . mean in fp32; a first pass finds each row's max m and
+ * l = sum exp(s - m); a second accumulates P' V' in fp32 on the tensor cores
+ * with P' = bf16(exp(s - m) g_v / G), G the largest g_v of the view, and
+ * writes out = G O / l in fp32.  P' is the only value rounded below fp32
+ * (relative 2^-9).
+ *   q_bf16     device [n_q][H][D] bf16, 16-byte aligned; D = 128
+ *   k_*, v_*   the pools of nvfp4_kv_gather_dequant (codes 8-byte aligned)
+ *   frame_row, frame_meta  HOST arrays of n_frames (<= NVFP4_MAX_VIEW_FRAMES)
+ *              entries, validated before anything is enqueued; at most 16
+ *              distinct slots in one view (NVFP4_ESHAPE otherwise)
+ *   out        device [n_q][H][D] fp32, 16-byte aligned
+ *   dev_status device int or NULL: NVFP4_DEV_TIMEOUT is OR-ed in when a
+ *              bounded wait for the tensor cores gave up (out then incomplete)
+ * One CTA per 128 queries and head; no workspace. */
+nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const uint8_t* k_codes,
+                                        const uint8_t* k_scales, const float* k_g, const float* k_mean,
+                                        const uint8_t* v_codes, const uint8_t* v_scales, const float* v_g,
+                                        int64_t pool_rows, int n_meta, const int64_t* frame_row,
+                                        const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
+                                        float scale, float* out, int* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weights with 16x16 2-D blocks (LongLive-2.0 summary page, training        */
 /* pipeline step 4: "2-D block scales for weights").                         */

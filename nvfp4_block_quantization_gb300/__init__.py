@@ -374,6 +374,32 @@ def kv_gather_dequant(pool: KvCachePool, frame_row, frame_slot, tokens_per_frame
     return out
 
 
+def kv_attention_prefill(q, k_pool: KvCachePool, v_pool: KvCachePool, frame_row, frame_slot, tokens_per_frame: int,
+                         scale: float, out=None, status=None, stream=None):
+    """Attention of a block of queries q [n_q, H, 128] (bf16) over a cache view read straight from the
+    NVFP4 pools, on the tensor cores (``nvfp4_kv_attention_prefill``); K's means are re-added when its
+    pool has them.  Returns fp32 [n_q, H, 128]; ``status`` (int32 [1], optional) collects
+    NVFP4_DEV_TIMEOUT."""
+    import numpy as np
+
+    torch = _torch()
+    _check_cuda(q, k_pool.codes, v_pool.codes)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("kv_attention_prefill: q must be bf16")
+    n_q, H, D = q.shape
+    fr = np.ascontiguousarray(frame_row, dtype=np.int64)
+    fs = np.ascontiguousarray(frame_slot, dtype=np.int32)
+    if out is None:
+        out = torch.empty((n_q, H, D), dtype=torch.float32, device=q.device)
+    st = _lib.nvfp4_kv_attention_prefill(_ptr(q), n_q, _ptr(k_pool.codes), _ptr(k_pool.scales), _ptr(k_pool.g),
+                                         _ptr(k_pool.mean), _ptr(v_pool.codes), _ptr(v_pool.scales), _ptr(v_pool.g),
+                                         k_pool.codes.shape[0], int(k_pool.g.numel()), fr.ctypes.data,
+                                         fs.ctypes.data, int(fr.shape[0]), tokens_per_frame, H, D, float(scale),
+                                         _ptr(out), _ptr(status), _stream(stream))
+    _lib.check(st, "nvfp4_kv_attention_prefill")
+    return out
+
+
 def mma_scales(scales, K: int, tile2d: bool = False, out=None, stream=None):
     """Block scales in the tensor cores' layout (``nvfp4_scales_to_mma`` / ``nvfp4_w2d_scales_to_mma``).
 

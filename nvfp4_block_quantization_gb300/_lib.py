@@ -41,6 +41,7 @@ EXPORTS = (
     "nvfp4_kv_gather_dequant",
     "nvfp4_kv_attention_workspace_bytes",
     "nvfp4_kv_attention_decode",
+    "nvfp4_kv_attention_prefill",
     "nvfp4_mma_scales_bytes",
     "nvfp4_scales_to_mma",
     "nvfp4_w2d_scales_to_mma",
@@ -165,6 +166,9 @@ def load(path: str | None = None):
     lib.nvfp4_kv_attention_decode.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32,
                                               i32, ctypes.c_float, vp, vp, sz, vp]
     lib.nvfp4_kv_attention_decode.restype = i32
+    lib.nvfp4_kv_attention_prefill.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32,
+                                               i32, ctypes.c_float, vp, vp, vp]
+    lib.nvfp4_kv_attention_prefill.restype = i32
     lib.nvfp4_mma_scales_bytes.argtypes = [i64, i64]
     lib.nvfp4_mma_scales_bytes.restype = i64
     lib.nvfp4_scales_to_mma.argtypes = [vp, i64, i64, vp, vp]
@@ -304,6 +308,14 @@ def nvfp4_kv_attention_decode(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v
     return load().nvfp4_kv_attention_decode(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g,
                                             pool_rows, n_meta, frame_row, frame_meta, n_frames, tokens_per_frame,
                                             H, D, scale, out, workspace, workspace_bytes, stream)
+
+
+def nvfp4_kv_attention_prefill(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g, pool_rows, n_meta,
+                               frame_row, frame_meta, n_frames, tokens_per_frame, H, D, scale, out, dev_status,
+                               stream):
+    return load().nvfp4_kv_attention_prefill(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g,
+                                             pool_rows, n_meta, frame_row, frame_meta, n_frames, tokens_per_frame,
+                                             H, D, scale, out, dev_status, stream)
 
 
 def nvfp4_mma_scales_bytes(rows, K):

@@ -54,3 +54,16 @@ def attention_decode(q, k, v, scale: float):
     A = np.einsum("ihd,thd->iht", np.abs(q64), np.abs(k64)).max(axis=2) * abs(float(scale))
     Vmax = np.abs(v64).max(axis=(0, 2))
     return out, A, Vmax
+
+
+def attention_weighted_abs(q, k, v, scale: float):
+    """q [n_q][H][D], k and v [T][H][D] (fp32 values) -> (out [n_q][H][D] binary64,
+    B [n_q][H][D] = sum_t p_t |v_td|), p the binary64 softmax weights of each query and head.
+    B bounds how far rounding the weights moves each output: a relative error e in every
+    weight moves out by at most e * B."""
+    q64, k64, v64 = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+    s = np.einsum("ihd,thd->iht", q64, k64) * float(scale)
+    s -= s.max(axis=2, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=2, keepdims=True)
+    return np.einsum("iht,thd->ihd", p, v64), np.einsum("iht,thd->ihd", p, np.abs(v64))

@@ -59,7 +59,7 @@ def parse():
     p.add_argument("--no-rows", action="store_true", help="skip the secondary rows (dequant, weights, 30 layers)")
     p.add_argument("--rows", nargs="+", default=None, metavar="ROW",
                    help="run only these secondary rows: kv_write_30_layers kv_cache_read_dequant kv_cache_view_gather "
-                        "kv_attention_decode gemm_w4a4 weight_quant_2d activation_quant_1d k_only_smooth_quant")
+                        "kv_attention_decode kv_attention_prefill gemm_w4a4 weight_quant_2d activation_quant_1d k_only_smooth_quant")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=30)
     return p.parse_args()
@@ -700,8 +700,54 @@ def row_kv_attention_decode(nv, W, torch, dev, peak):
     return out
 
 
+def row_kv_attention_prefill(nv, W, torch, dev, peak):
+    """Attention of a whole new chunk (7040 query tokens, 24 heads x 128, bf16) over the 21-frame view
+    (3 sink + 18 rolling frames x 880 tokens) read from one layer's NVFP4 K and V pools, on the tensor
+    cores (nvfp4_kv_attention_prefill).  FLOPs: 4 n_q n_keys D per head (Q K^T and P V)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3300)
+    F, Lf = 8, 880
+    cache = nv.KvCache(F, Lf, 3, 3, 18)
+    pk = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=True, device=dev)
+    pv = nv.KvCachePool.allocate(cache, HEADS, HEAD_DIM, smooth=False, device=dev)
+    for c in range(5):
+        slot = cache.append()
+        k = _chunk_k_device(torch, gen, dev)
+        v = torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev).to(torch.bfloat16)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        nv.kv_smooth_quant_batched([k, v], [True, False],
+                                   outs=[pk.slot_outputs(cache, slot, st), pv.slot_outputs(cache, slot, st)],
+                                   status=st)
+        del k, v
+    fi, fr, fs = cache.view()
+    n_keys = len(fr) * Lf
+    q = (torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+    o = torch.empty((T_CHUNK, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call(i):
+        nv.kv_attention_prefill(q, pk, pv, fr, fs, Lf, HEAD_DIM ** -0.5, out=o, status=status)
+
+    ms = _time_graph(torch, call, 2, 5)
+    fl = 4.0 * T_CHUNK * n_keys * HEAD_DIM * HEADS
+    pk_tf, src = bf16_peak_tflops()
+    torch.cuda.synchronize()
+    return {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops": fl, "n_q": T_CHUNK, "n_keys": n_keys,
+            "peak_tflops": pk_tf, "peak_source": src, "frac": fl / ms / 1e9 / pk_tf,
+            "dev_status": int(status.item())}
+
+
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rates of the part
+
+
+def bf16_peak_tflops():
+    """Dense bf16 peak: the measured cuBLAS bf16 burst rate."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback bf16 burst"
 
 
 def fp4_peak_tflops():
@@ -874,6 +920,7 @@ def row_k_only_smooth_quant(nv, W, torch, dev, peak):
 
 ROWS = {"kv_write_30_layers": row_kv_write_30_layers, "kv_cache_read_dequant": row_kv_cache_read_dequant,
         "kv_cache_view_gather": row_kv_cache_view_gather, "kv_attention_decode": row_kv_attention_decode,
+        "kv_attention_prefill": row_kv_attention_prefill,
         "gemm_w4a4": row_gemm_w4a4,
         "weight_quant_2d": row_weight_quant_2d, "activation_quant_1d": row_activation_quant_1d,
         "k_only_smooth_quant": row_k_only_smooth_quant}

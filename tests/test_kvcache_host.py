@@ -234,3 +234,27 @@ def test_attention_argument_errors(lib):
     assert call(ws=None) == lib.NVFP4_EWORKSPACE and call(wsb=16) == lib.NVFP4_EWORKSPACE
     # 2 heads x 1 split x 1 query x (64 + 2) floats = 528 bytes, rounded up to 256-byte units
     assert lib.nvfp4_kv_attention_workspace_bytes(2, 16, 2, 64, 1) == 768
+
+
+def test_prefill_attention_argument_errors(lib):
+    """nvfp4_kv_attention_prefill's checks, all before any CUDA call (fake device addresses)."""
+    dev = 1 << 20
+    fr = np.array([0, 16], np.int64)
+    fm = np.array([0, 1], np.int32)
+
+    def call(n_q=200, D=128, fr_=fr, fm_=fm, n=None, pool_rows=64, n_meta=2, q=dev, codes=dev, out=dev):
+        n = len(fr_) if n is None else n
+        return lib.load().nvfp4_kv_attention_prefill(q, n_q, codes, dev, dev, dev, dev, dev, dev, pool_rows, n_meta,
+                                                     fr_.ctypes.data, fm_.ctypes.data, n, 16, 2, D, 0.125, out,
+                                                     None, None)
+
+    assert call(D=64) == lib.NVFP4_ESHAPE                               # head dimension 128 only
+    assert call(n_q=0) == lib.NVFP4_ESHAPE
+    assert call(n=0) == lib.NVFP4_ESHAPE
+    assert call(fr_=np.array([0, 49], np.int64)) == lib.NVFP4_ESHAPE  # frame past the pool
+    assert call(fm_=np.array([0, 2], np.int32)) == lib.NVFP4_ESHAPE   # slot past the metadata
+    many = np.arange(17)
+    assert call(fr_=(many * 16).astype(np.int64), fm_=many.astype(np.int32), pool_rows=17 * 16,
+                n_meta=17) == lib.NVFP4_ESHAPE                          # 17 distinct slots in one view
+    assert call(codes=None) == lib.NVFP4_EINVAL and call(out=None) == lib.NVFP4_EINVAL
+    assert call(q=dev + 8) == lib.NVFP4_EALIGN and call(out=dev + 4) == lib.NVFP4_EALIGN

@@ -71,7 +71,9 @@ def queries(n_q, H, D, seed, sd=1.0):
     return bits, (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-def run_and_check(nv, cache, pk, pv, qbits, qf, scale, heads=None):
+def run_and_check(nv, cache, pk, pv, qbits, qf, scale, heads=None, rows_q=None):
+    """Runs all queries on the GPU; compares the oracle on `heads` (all by default) and on the
+    query rows `rows_q` (all by default)."""
     from oracle import attention as oa
 
     fi, fr, fs = cache.view()
@@ -79,6 +81,8 @@ def run_and_check(nv, cache, pk, pv, qbits, qf, scale, heads=None):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = host(nv.kv_attention_prefill(dev(qbits), pk, pv, fr, fs, L, scale, status=status))
     assert int(host(status)[0]) == 0
+    if rows_q is not None:
+        out, qf = out[rows_q], qf[rows_q]
     heads = list(range(qf.shape[1])) if heads is None else heads
     rows = np.concatenate([np.arange(r, r + L) for r in fr])
     slot_of = np.repeat(fs, L)
@@ -121,3 +125,14 @@ def test_prefill_cache_read_view(nv):
     assert len(cache.view()[1]) == 21
     qbits, qf = queries(130, 24, 128, 9, sd=0.5)
     run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[0, 11, 23])
+
+
+def test_prefill_whole_chunk_sampled(nv):
+    """The row's shape: a whole chunk of 7040 queries x 24 heads over the 21-frame view in one call;
+    48 sampled query rows (both halves of many CTAs, the last ragged CTA included) of heads 5 and 17
+    against the oracle."""
+    cache, pk, pv = fill_cache(nv, F=8, L=880, H=24, D=128, S_g=3, S_s=3, W=18, n_chunks=5, seed0=1500)
+    qbits, qf = queries(7040, 24, 128, 11, sd=0.5)
+    rows_q = np.sort(np.concatenate([np.random.default_rng(12).choice(7040, 44, replace=False),
+                                     np.array([0, 255, 256, 7039])]))
+    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[5, 17], rows_q=rows_q)

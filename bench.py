@@ -208,6 +208,68 @@ def cpu_oracle_threads_run(tokens: int, threads: int):
     return elems * QUANT_BYTES_PER_ELEM / dt / 1e9, dt, elems
 
 
+def cpu_oracle_rows(threads: int) -> dict:
+    """The oracle on configs 3-5 with the rows' byte accounting, each on a stated sample scaled up by
+    bytes (so the default run stays within about half a minute of CPU time).  The KV quantizer runs
+    on `threads` host threads (the threaded driver, bit-identical); dequant and the weight quantizer
+    have single-threaded statements only."""
+    import numpy as np
+
+    import oracle
+    from nvfp4_block_quantization_gb300 import workloads as W
+
+    oracle.build()
+    rows = {}
+    # config 3: 30 layers of K (smoothed) and V with their per-layer seeds; layers 0 and 29 timed
+    secs = 0.0
+    for layer in (0, 29):
+        sk, sv = W.layer_seeds(layer)
+        K = W.to_bf16_bits(W.chunk_k(sk))
+        V = W.to_bf16_bits(W.chunk_v(sv))
+        t0 = time.perf_counter()
+        oracle.kv_smooth_quant_threads(K, True, threads)
+        oracle.kv_smooth_quant_threads(V, False, threads)
+        secs += time.perf_counter() - t0
+    per_layer = 2 * K.size * QUANT_BYTES_PER_ELEM
+    rows["kv_write_30_layers"] = {"GB/s": 2 * per_layer / secs / 1e9, "threads": threads, "seconds_sample": secs,
+                                  "sample": "layers 0 and 29 of 30 (seeds 3000 + 2l, 3001 + 2l), scaled by bytes"}
+    # config 4: dequant of a 21-frame view (18,480 tokens) of K (mean re-added, per-frame groups) and V;
+    # the codes are the config-2 chunk's, repeated to the view's length
+    qk = oracle.kv_smooth_quant_threads(W.to_bf16_bits(W.chunk_k(2000)), True, threads)
+    qv = oracle.kv_smooth_quant_threads(W.to_bf16_bits(W.chunk_v(2001)), False, threads)
+    n_tok, L = 21 * 880, 880
+    rep = lambda a: np.ascontiguousarray(np.concatenate([a] * 3, axis=0)[:n_tok])
+    groups = n_tok // L
+    gk = np.full(groups, qk["g"], np.float32)
+    gv = np.full(groups, qv["g"], np.float32)
+    mk = np.ascontiguousarray(np.broadcast_to(qk["mean"][None], (groups,) + qk["mean"].shape), dtype=np.float32)
+    ck, sk_, cv, sv_ = rep(qk["codes"]), rep(qk["scales"]), rep(qv["codes"]), rep(qv["scales"])
+    t0 = time.perf_counter()
+    oracle.kv_dequant(ck, sk_, gk, mk, tokens_per_group=L)
+    oracle.kv_dequant(cv, sv_, gv, None, tokens_per_group=L)
+    secs = time.perf_counter() - t0
+    deq_bytes = 2 * n_tok * HEADS * HEAD_DIM * QUANT_BYTES_PER_ELEM
+    rows["kv_cache_read_dequant"] = {"GB/s": deq_bytes / secs / 1e9, "threads": 1, "seconds_sample": secs,
+                                     "sample": "K (mean) and V of one 21-frame view"}
+    # config 5: weights (one matrix of each shape timed, scaled by bytes to all six) and activations
+    secs, el = 0.0, 0
+    for i, (M, N) in ((0, W.WEIGHT_SHAPES[0]), (4, W.WEIGHT_SHAPES[4])):
+        w = W.to_bf16_bits(W.weight(i, M, N))
+        t0 = time.perf_counter()
+        oracle.weight_quant_2d(w)
+        secs += time.perf_counter() - t0
+        el += M * N
+    rows["weight_quant_2d"] = {"GB/s": el * (2 + 0.5 + 1.0 / 256) / secs / 1e9, "threads": 1, "seconds_sample": secs,
+                               "sample": "matrices 0 (3072x3072) and 4 (3072x14336) of six, scaled by bytes"}
+    x = W.to_bf16_bits(W.activations()).reshape(T_CHUNK, 1, 3072)
+    t0 = time.perf_counter()
+    oracle.kv_smooth_quant_threads(x, False, threads)
+    secs = time.perf_counter() - t0
+    rows["activation_quant_1d"] = {"GB/s": x.size * QUANT_BYTES_PER_ELEM / secs / 1e9, "threads": threads,
+                                   "seconds_sample": secs, "sample": "the whole 7040x3072 activation"}
+    return rows
+
+
 def cpu_model() -> str:
     """The host CPU's name from /proc/cpuinfo (x86: model name; Arm: implementer and part), or ''."""
     try:
@@ -504,7 +566,8 @@ def run_ours(args, ws, rank):
                                           f"{elems} elements, {secs:.1f} s single-threaded",
                                 "all_cores": {"value": tgbs, "unit": "GB/s", "cores": nthreads, "seconds": tsecs,
                                               "kind": "oracle, threaded driver (channel, element and block ranges "
-                                                      "split over the host's cores; bit-identical results)"}}
+                                                      "split over the host's cores; bit-identical results)"},
+                                "rows": cpu_oracle_rows(nthreads)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

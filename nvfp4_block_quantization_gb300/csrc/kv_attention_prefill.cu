@@ -25,13 +25,27 @@
 // P' is rounded (bf16, relative 2^-9); 2^x is the hardware approximation
 // (relative error below 2^-22).
 //
-// One CTA per (256 queries, head), 256 threads: all threads dequantize each
-// 128-key tile into shared memory once for both 128-query halves; thread 0
-// issues the MMAs of both halves (TMEM: S of half 0 and 1 in columns 0-255, O in
-// 256-511); warp w owns query rows 32 (w % 4) .. of half w / 4 (its TMEM lane
-// quadrant) for the softmax and the epilogue.  Operand tiles use the no-swizzle
-// K-major layout of 8-row x 16-byte core matrices; the transposed V' tile pads
-// its K stride to 144 bytes so that its stores spread over the banks.
+// One CTA per (256 queries, head), 13 warps in roles, every hand-off an mbarrier:
+//   warps 0-3, 4-7  softmax of query half 0 / 1: thread r owns query row r of its
+//                   half (TMEM lane r); two passes over the half's S (maximum,
+//                   then P'), 32 columns at a time; P' (bf16 pairs) is written
+//                   into TMEM over the half's S columns already read; O rescaled
+//                   when needed;
+//   warps 8-11      dequantization into double buffers: tile j's K' (with the
+//                   per-key factors, in one of three table buffers) as soon as
+//                   both S MMAs of tile j - 2 have read its buffer, and its V'^T
+//                   as soon as both P' V' MMAs of tile j - 2 have; the next
+//                   tile's codes are loaded into registers meanwhile;
+//   warp 12         one thread issues the MMAs, ping-ponging the halves:
+//                   P'_0 V'(j-1), S_0(j), P'_1 V'(j-1), S_1(j), P' read from TMEM
+//                   (the A operand) and S_h(j) issued once P'_h V'(j-1) has read
+//                   the columns it overwrites.
+// TMEM: S of half 0 and 1 in columns 0-255 (P' over their first 64), O in
+// 256-511.  Operand tiles in shared memory use the no-swizzle K-major layout of
+// 8-row x 16-byte core matrices; the transposed V' tile pads its K stride to
+// 144 bytes so that its stores spread over the banks.  Every wait is bounded; a
+// timeout is reported in the status word and the CTA drains its MMAs before
+// freeing TMEM.
 #include <cstring>
 
 #include "nvfp4.h"
@@ -43,17 +57,23 @@ namespace {
 
 constexpr int kPfTile = 128;           // queries per half, keys per tile
 constexpr int kPfHalves = 2;           // query halves per CTA sharing each K'/V' tile
+constexpr int kPfRows = 128 * kPfHalves;
 constexpr int kPfD = 128;              // head dimension
-constexpr int kPfThreads = 128 * kPfHalves;
+constexpr int kPfSoftmaxWarps = 4 * kPfHalves;
+constexpr int kPfDequantWarps = 4;
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDequantWarps;
+constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
 constexpr int kPfMaxSlots = 16;        // distinct pool slots in one view
 constexpr uint32_t kLboStd = 128, kSboStd = 2048;  // [128 rows][256 B]: core matrices 128 B apart along K
 constexpr uint32_t kLboV = 144, kSboV = 2304;      // the padded V' tile
 constexpr int kTileStd = 32768;
 constexpr int kTileV = 36864;
 constexpr float kRescaleStep = 8.0f;  // base-2 units the running maximum may lag behind
-// Q (2 halves), K', P' (2 halves), V'^T, q . mean per thread, key tables, barriers
-constexpr int kPfSmem = kPfHalves * kTileStd + kTileStd + kPfHalves * kTileStd + kTileV + kPfMaxSlots * kPfThreads * 4 +
-                        4 * kPfTile * 4 + 256;
+// Q (2 halves), K' (2 buffers), V'^T (2 buffers), q . mean per row and slot, key tables (3 buffers), slot
+// tables, barriers; P' lives in TMEM over its half's S
+constexpr int kPfKeyBufs = 3;
+constexpr int kPfSmem = kPfHalves * kTileStd + 2 * kTileStd + 2 * kTileV + kPfMaxSlots * kPfRows * 4 +
+                        kPfKeyBufs * 3 * kPfTile * 4 + 2 * kPfMaxSlots * 4 + 256;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 struct PfView {
@@ -140,6 +160,28 @@ __device__ __forceinline__ void pf_st32(uint32_t taddr, const float v[32]) {
       : "memory");
 }
 
+__device__ __forceinline__ void pf_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// O (+)= P' V'^T with P' (A, bf16 pairs: lane = query row, column c = keys 2c and 2c + 1) in TMEM.
+__device__ __forceinline__ void pf_mma_tile_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t b_lbo,
+                                               uint32_t b_sbo, uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // K = 128 keys in steps of 16 (8 TMEM columns of A, two core matrices of B)
+    const uint64_t db = pf_desc(b_smem + k * 2 * b_lbo, b_lbo, b_sbo);
+    const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem + 8 * k), "l"(db), "r"(idesc), "r"(acc) : "memory");
+  }
+}
+
 __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, uint32_t a_lbo, uint32_t a_sbo,
                                             uint32_t b_smem, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc,
                                             bool accumulate) {
@@ -155,103 +197,119 @@ __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, ui
   }
 }
 
-// The codes and scales of one thread's share of a key tile, loaded ahead of use:
-// four (key, block) units of K' and four keys x one block of V'.  x packs the
+// One dequantization thread's share of a key tile's codes, loaded ahead of use:
+// eight (key, block) units of K' or eight keys x one block of V'.  x packs the
 // scale byte (bits 0-7) and 1 + the key's view slot (bits 8-15; 0: past the view).
-struct PfCodes {
-  uint2 kc[4];
-  uint32_t kx[4];
-  uint2 vc[4];
-  uint32_t vx[4];
+struct PfCodes8 {
+  uint2 c[8];
+  uint32_t x[8];
 };
 
-__device__ __forceinline__ void pf_load_codes(const PfView& view, const PfArgs& a, int h, int64_t t0, int kr, int kb,
-                                              int kg, int vkg, int vb, int vh, PfCodes& c) {
+// Loads the units of keys t0 + keys[j] (0 <= keys[j] < 128).  The view has fewer than 2^31 keys, so one
+// 32-bit division finds the frame of t0; each key's frame then follows by subtraction (at most
+// 127 / L_f + 1 steps, one for frames of 128 tokens or more).
+__device__ __forceinline__ void pf_load8(const PfView& view, const PfArgs& a, int h, int64_t t0, const uint8_t* codes,
+                                         const uint8_t* scales, const int keys[8], int blk, PfCodes8& r) {
+  const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys, u0 = (uint32_t)t0;
+  const uint32_t f0 = u0 / L, r0 = u0 - f0 * L;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int64_t t = t0 + kr + 8 * (kg + 4 * j);
-    c.kc[j] = make_uint2(0u, 0u);
-    c.kx[j] = 0u;
-    if (t < a.n_keys) {
-      int64_t prow;
-      int vs;
-      key_location(view, a.L_f, t, prow, vs);
-      const int64_t base = prow * a.H + h;
-      c.kc[j] = *reinterpret_cast<const uint2*>(a.k_codes + base * (kPfD / 2) + kb * 8);
-      c.kx[j] = (uint32_t)a.k_scales[base * (kPfD / 16) + kb] | ((uint32_t)(vs + 1) << 8);
+  for (int j = 0; j < 8; ++j) {
+    r.c[j] = make_uint2(0u, 0u);
+    r.x[j] = 0u;
+    if (u0 + (uint32_t)keys[j] < n_keys) {
+      uint32_t f = f0, rr = r0 + (uint32_t)keys[j];
+      while (rr >= L) {
+        rr -= L;
+        ++f;
+      }
+      const int vs = view.vslot[f];
+      const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
+      r.c[j] = *reinterpret_cast<const uint2*>(codes + base * (kPfD / 2) + blk * 8);
+      r.x[j] = (uint32_t)scales[base * (kPfD / 16) + blk] | ((uint32_t)(vs + 1) << 8);
     }
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int64_t t = t0 + 8 * vkg + 4 * vh + j;
-    c.vc[j] = make_uint2(0u, 0u);
-    c.vx[j] = 0u;
-    if (t < a.n_keys) {
-      int64_t prow;
-      int vs;
-      key_location(view, a.L_f, t, prow, vs);
-      const int64_t base = prow * a.H + h;
-      c.vc[j] = *reinterpret_cast<const uint2*>(a.v_codes + base * (kPfD / 2) + vb * 8);
-      c.vx[j] = (uint32_t)a.v_scales[base * (kPfD / 16) + vb] | ((uint32_t)(vs + 1) << 8);
-    }
-  }
+}
+
+__device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__device__ __forceinline__ void pf_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __grid_constant__ PfView view,
                                                                      PfArgs a) {
   extern __shared__ __align__(128) uint8_t pf_smem[];
   uint8_t* Qs = pf_smem;                          // Q of both halves, bf16 [query][d]
-  uint8_t* Kb = Qs + kPfHalves * kTileStd;        // K' tile [key][d]
-  uint8_t* Pb = Kb + kTileStd;                    // P' of both halves [query][key]
-  uint8_t* Vt = Pb + kPfHalves * kTileStd;        // V'^T tile [d][key], padded
-  float* qm = reinterpret_cast<float*>(Vt + kTileV);  // [view slot][thread]: scale log2e q . mean
-  float* key_a = qm + kPfMaxSlots * kPfThreads;        // per key: scale log2e g_k
-  float* key_gv = key_a + kPfTile;                      // g_v / G (0 past the view)
-  int* key_qm = reinterpret_cast<int*>(key_gv + kPfTile);  // offset of the key's slot in qm, -1 past the view
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(key_qm + 2 * kPfTile);
-  uint64_t* bar_pv = bar_s + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
+  uint8_t* Kb = Qs + kPfHalves * kTileStd;        // K' tiles [buffer][key][d]
+  uint8_t* Vt = Kb + 2 * kTileStd;                // V'^T tiles [buffer][d][key], padded
+  float* qm = reinterpret_cast<float*>(Vt + 2 * kTileV);  // [view slot][row]: scale log2e q . mean
+  float* key_a = qm + kPfMaxSlots * kPfRows;              // [table buffer][key]: scale log2e g_k
+  float* key_gv = key_a + kPfKeyBufs * kPfTile;           // [table buffer][key]: g_v / G (0 past the view)
+  int* key_off = reinterpret_cast<int*>(key_gv + kPfKeyBufs * kPfTile);  // slot offset in qm, -1 past the view
+  float* slot_a = reinterpret_cast<float*>(key_off + kPfKeyBufs * kPfTile);
+  float* slot_gv = slot_a + kPfMaxSlots;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(slot_gv + kPfMaxSlots);
+  uint64_t* k_full = bar;        // [buffer] K'(j) and its key tables written  (4 dequant warps)
+  uint64_t* k_free = bar + 2;    // [buffer] both S(j) MMAs have read K'(j)     (commit)
+  uint64_t* v_full = bar + 4;    // [buffer] V'(j) written                      (4 dequant warps)
+  uint64_t* v_free = bar + 6;    // [buffer] both P' V'(j) MMAs have read V'(j) (commit)
+  uint64_t* s_full = bar + 8;    // [half] S(j) in TMEM                         (commit)
+  uint64_t* p_full = bar + 10;   // [half] P'(j) in TMEM, S(j) read             (4 softmax warps)
+  uint64_t* o_done = bar + 12;   // [half] P' V'(j) accumulated into O          (commit)
+  uint64_t* drain = bar + 14;    // every MMA issued has finished               (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
   float* Gs = reinterpret_cast<float*>(tmem_slot + 1);
   int* failed = reinterpret_cast<int*>(Gs + 1);
+  volatile int* vfailed = failed;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int half = warp >> 2, quad = warp & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
-  const int64_t rowq = (int64_t)blockIdx.x * (kPfTile * kPfHalves) + tid;  // this thread's query
-  const bool q_ok = rowq < a.n_q;
   const int H = a.H;
   const float slog2e = a.scale * 1.4426950408889634f;
+  const int n_tiles = (int)((a.n_keys + kPfTile - 1) / kPfTile);
 
   if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_pv, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], kPfDequantWarps);
+      mbar_init(&k_free[i], 1);
+      mbar_init(&v_full[i], kPfDequantWarps);
+      mbar_init(&v_free[i], 1);
+    }
+    for (int i = 0; i < kPfHalves; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(drain, 1);
     *failed = 0;
     float G = 0.0f;
     for (int s = 0; s < view.n_vslots; ++s) G = fmaxf(G, a.v_g[view.slot[s]]);
     *Gs = G;
+    for (int s = 0; s < view.n_vslots; ++s) {
+      slot_a[s] = __fmul_rn(slog2e, a.k_g[view.slot[s]]);
+      slot_gv[s] = G > 0.0f ? __fdiv_rn(a.v_g[view.slot[s]], G) : 0.0f;
+    }
     mbar_fence_init();
   }
-  if (warp == 0) {
+  if (warp == kPfMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // roles in the dequantization
-  const int kr = tid & 7, kb = (tid >> 3) & 7, kg = tid >> 6;    // K': key row, block, group (0..3)
-  const int vkg = tid & 15, vb = (tid >> 4) & 7, vh = tid >> 7;  // V'^T: key group of 8, block, half
-  PfCodes pre;
-  pf_load_codes(view, a, h, 0, kr, kb, kg, vkg, vb, vh, pre);  // the first tile, in flight during the prologue
-
-  // Q rows (zeros past n_q) and scale log2e q . mean per view slot
-  {
+  // softmax threads: their Q row (zeros past n_q) and scale log2e q . mean per view slot
+  const int64_t rowq = (int64_t)blockIdx.x * kPfRows + tid;
+  if (warp < kPfSoftmaxWarps) {
+    const bool q_ok = rowq < a.n_q;
     const uint4* src = reinterpret_cast<const uint4*>(a.q + (rowq * H + h) * kPfD);
-    uint8_t* qs = Qs + half * kTileStd;
-    const int r = tid & 127;
+    uint8_t* qs = Qs + (tid >> 7) * kTileStd;
     uint32_t qw[64];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const uint4 v = q_ok ? ld_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(qs + core_off(r, c, kLboStd, kSboStd)) = v;
+      *reinterpret_cast<uint4*>(qs + core_off(tid & 127, c, kLboStd, kSboStd)) = v;
       qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
     }
     for (int s = 0; s < view.n_vslots; ++s) {
@@ -267,181 +325,242 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
           acc = __fmaf_rn(bf16hi(qw[2 * c + 1]), mv.w, acc);
         }
       }
-      qm[s * kPfThreads + tid] = __fmul_rn(slog2e, acc);
+      qm[s * kPfRows + tid] = __fmul_rn(slog2e, acc);
     }
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q is an MMA operand
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-  const uint32_t t_S = tmem + half * 128 + lane_addr, t_O = tmem + 256 + half * 128 + lane_addr;
   const float G = *Gs;
-  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfTile >> 3) << 17) |
-                         ((uint32_t)(kPfTile >> 4) << 24);  // bf16 x bf16 -> fp32, K-major, M = N = 128
-  const int n_tiles = (int)((a.n_keys + kPfTile - 1) / kPfTile);
-  uint32_t ph_s = 0, ph_pv = 0;
-  uint8_t* Pmine = Pb + half * kTileStd;
 
-  // K' of the prefetched tile into Kb, with its per-key factors
-  auto decode_k = [&]() {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int key = kr + 8 * (kg + 4 * j);
-      const uint32_t x = pre.kx[j];
-      uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      if (x >> 8) decode_block_bf16(pre.kc[j], x & 0xFFu, w);
-      if (kb == 0) {
-        const int vs = (int)(x >> 8) - 1;
-        key_a[key] = vs >= 0 ? __fmul_rn(slog2e, a.k_g[view.slot[vs]]) : 0.0f;
-        key_qm[key] = vs >= 0 ? vs * kPfThreads : -1;
+  if (warp < kPfSoftmaxWarps) {
+    // ================= softmax of one query half =================
+    const int half = warp >> 2;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_S = tmem + half * 128 + lane_addr, t_O = tmem + 256 + half * 128 + lane_addr;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int tb = j % kPfKeyBufs;
+      const float* ka = key_a + tb * kPfTile;
+      const float* kgv = key_gv + tb * kPfTile;
+      const int* koff = key_off + tb * kPfTile;
+      // a tile whose 128 keys are all in the view and in one slot (with frames of at least 128
+      // tokens its first and last key decide it): the slot's factors are scalars
+      const int64_t t0 = (int64_t)j * kPfTile;
+      int uvs = -1;
+      if (a.L_f >= kPfTile && t0 + kPfTile <= a.n_keys) {
+        const uint32_t L = (uint32_t)a.L_f;
+        const int v0 = view.vslot[(uint32_t)t0 / L], v1 = view.vslot[((uint32_t)t0 + kPfTile - 1) / L];
+        if (v0 == v1) uvs = v0;
       }
-      *reinterpret_cast<uint4*>(Kb + core_off(key, 2 * kb, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(Kb + core_off(key, 2 * kb + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-  };
-  // V'^T of the prefetched tile into Vt, with the keys' g_v / G
-  auto decode_v = [&]() {
-    uint32_t w[4][8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t x = pre.vx[j];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[j][i] = 0u;
-      if (x >> 8) decode_block_bf16(pre.vc[j], x & 0xFFu, w[j]);
-      if (vb == 0) {
-        const int vs = (int)(x >> 8) - 1;
-        key_gv[8 * vkg + 4 * vh + j] = (vs >= 0 && G > 0.0f) ? __fdiv_rn(a.v_g[view.slot[vs]], G) : 0.0f;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {  // channel 16 vb + i of the four keys: 8 bytes of V'^T's row
-      uint32_t o[2];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const uint32_t lo = (i & 1) ? (w[2 * p][i >> 1] >> 16) : (w[2 * p][i >> 1] & 0xFFFFu);
-        const uint32_t hi = (i & 1) ? (w[2 * p + 1][i >> 1] >> 16) : (w[2 * p + 1][i >> 1] & 0xFFFFu);
-        o[p] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint2*>(Vt + core_off(16 * vb + i, vkg, kLboV, kSboV) + 8 * vh) = make_uint2(o[0], o[1]);
-    }
-  };
-  auto issue_s = [&]() {  // S = Q K'^T for both halves
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    for (int hh = 0; hh < kPfHalves; ++hh)
-      pf_mma_tile(tmem + hh * 128, smem_u32(Qs + hh * kTileStd), kLboStd, kSboStd, smem_u32(Kb), kLboStd, kSboStd,
-                  idesc, false);
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar_s))
-                 : "memory");
-  };
-
-  // tile 0
-  decode_k();
-  decode_v();
-  if (n_tiles > 1) pf_load_codes(view, a, h, kPfTile, kr, kb, kg, vkg, vb, vh, pre);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (tid == 0) issue_s();
-
-  float m = -INFINITY, l = 0.0f;
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const bool more = tile + 1 < n_tiles;
-    if (!mbar_wait(bar_s, ph_s)) atomicExch(failed, 1);
-    ph_s ^= 1u;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // ---- scores (base 2), running maximum, weights of this thread's query row ----
-    float t[kPfTile];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) pf_ld32(t_S + 32 * c, t + 32 * c);
-    float mt = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kPfTile; ++k) {
-      const int off = key_qm[k];
-      t[k] = off >= 0 ? __fmaf_rn(key_a[k], t[k], qm[off + tid]) : -INFINITY;
-      mt = fmaxf(mt, t[k]);
-    }
-    const bool grow = mt > m + kRescaleStep;
-    if (__any_sync(0xffffffffu, grow)) {
-      const float m_new = grow ? mt : m;
-      const float f = grow ? ex2_approx(m - m_new) : 1.0f;  // 0 for the first tile (m = -inf)
-      l = __fmul_rn(l, f);
-      m = m_new;
-      if (tile > 0) {  // O holds earlier tiles (their MMAs have finished): scale this row, warp-wide
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          pf_ld32(t_O + 32 * c, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], f);
-          pf_st32(t_O + 32 * c, o);
-        }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      }
-    }
-    float sum = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      uint32_t o[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int k = 8 * c + 2 * p;
-        const float p0 = ex2_approx(t[k] - m), p1 = ex2_approx(t[k + 1] - m);
-        sum = __fadd_rn(sum, __fadd_rn(p0, p1));
-        const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(p0, key_gv[k]), __fmul_rn(p1, key_gv[k + 1])));
-        o[p] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      *reinterpret_cast<uint4*>(Pmine + core_off(tid & 127, c, kLboStd, kSboStd)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    l = __fadd_rn(l, sum);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    // ---- O += P' V' for both halves; meanwhile the next K' ----
-    if (tid == 0) {
+      const float ua = uvs >= 0 ? slot_a[uvs] : 0.0f, ub = uvs >= 0 ? qm[uvs * kPfRows + tid] : 0.0f;
+      const float ugv = uvs >= 0 ? slot_gv[uvs] : 0.0f;
+      if (!pf_wait_warp(&s_full[half], j & 1)) { ok = false; break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      for (int hh = 0; hh < kPfHalves; ++hh)
-        pf_mma_tile(tmem + 256 + hh * 128, smem_u32(Pb + hh * kTileStd), kLboStd, kSboStd, smem_u32(Vt), kLboV, kSboV,
-                    idesc, tile > 0);
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar_pv))
-                   : "memory");
-    }
-    if (more) decode_k();  // K' is free: S of this tile has finished
-    if (!mbar_wait(bar_pv, ph_pv)) atomicExch(failed, 1);
-    ph_pv ^= 1u;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (more) {
-      decode_v();  // V'^T and P' are free: P' V' has finished
-      if (tile + 2 < n_tiles) pf_load_codes(view, a, h, (int64_t)(tile + 2) * kPfTile, kr, kb, kg, vkg, vb, vh, pre);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();  // every wait of this tile is over: all threads see the same flag below
-    if (*reinterpret_cast<volatile int*>(failed)) break;
-    if (more && tid == 0) issue_s();
-  }
-  // ---- out = G O / l ----
-  if (!*reinterpret_cast<volatile int*>(failed)) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const float f = n_tiles > 0 ? __fdiv_rn(G, l) : 0.0f;
+      // pass 1: the tile's maximum of t = (scale log2e) (g_k S + q . mean)
+      float mt = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float o[32];
-      pf_ld32(t_O + 32 * c, o);
-      if (q_ok) {
-        float4* dst = reinterpret_cast<float4*>(a.out + (rowq * H + h) * kPfD + 32 * c);
+      for (int c = 0; c < 4; ++c) {
+        float t[32];
+        pf_ld32(t_S + 32 * c, t);
+        if (uvs >= 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__fmul_rn(o[4 * i], f), __fmul_rn(o[4 * i + 1], f), __fmul_rn(o[4 * i + 2], f),
-                               __fmul_rn(o[4 * i + 3], f));
+          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __fmaf_rn(ua, t[i], ub));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int k = 32 * c + i, off = koff[k];
+            if (off >= 0) mt = fmaxf(mt, __fmaf_rn(ka[k], t[i], qm[off + tid]));
+          }
+        }
       }
+      const bool grow = mt > m + kRescaleStep;
+      if (j > 0 && !pf_wait_warp(&o_done[half], (j - 1) & 1)) { ok = false; break; }  // O current
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? mt : m;
+        const float f = grow ? ex2_approx(m - m_new) : 1.0f;  // 0 for the first tile (m = -inf)
+        l = __fmul_rn(l, f);
+        m = m_new;
+        if (j > 0) {  // O holds earlier tiles: scale this row (warp-wide TMEM access)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            pf_ld32(t_O + 32 * c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], f);
+            pf_st32(t_O + 32 * c, o);
+          }
+        }
+      }
+      // pass 2: P' = bf16(2^(t - m) g_v / G) into TMEM over S (columns already read), and l
+      float sum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float t[32];
+        pf_ld32(t_S + 32 * c, t);
+        uint32_t pw[16];
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+          const int i = 2 * p, k = 32 * c + i;
+          float p0, p1, g0, g1;
+          if (uvs >= 0) {
+            p0 = ex2_approx(__fmaf_rn(ua, t[i], ub) - m);
+            p1 = ex2_approx(__fmaf_rn(ua, t[i + 1], ub) - m);
+            g0 = ugv;
+            g1 = ugv;
+          } else {
+            const int o0 = koff[k], o1 = koff[k + 1];
+            p0 = o0 >= 0 ? ex2_approx(__fmaf_rn(ka[k], t[i], qm[o0 + tid]) - m) : 0.0f;
+            p1 = o1 >= 0 ? ex2_approx(__fmaf_rn(ka[k + 1], t[i + 1], qm[o1 + tid]) - m) : 0.0f;
+            g0 = kgv[k];
+            g1 = kgv[k + 1];
+          }
+          sum = __fadd_rn(sum, __fadd_rn(p0, p1));
+          const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(p0, g0), __fmul_rn(p1, g1)));
+          pw[p] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        pf_st16(t_S + 16 * c, pw);  // keys 32 c .. 32 c + 31: columns 16 c .. 16 c + 15, S there already read
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      l = __fadd_rn(l, sum);
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[half]);
+      if (__any_sync(0xffffffffu, *vfailed != 0)) { ok = false; break; }
     }
-  } else if (tid == 0 && a.dev_status) {
-    atomicOr(a.dev_status, NVFP4_DEV_TIMEOUT);
+    // ---- out = G O / l ----
+    if (ok && pf_wait_warp(&o_done[half], (n_tiles - 1) & 1)) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const float f = __fdiv_rn(G, l);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        pf_ld32(t_O + 32 * c, o);
+        if (rowq < a.n_q) {
+          float4* dst = reinterpret_cast<float4*>(a.out + (rowq * H + h) * kPfD + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__fmul_rn(o[4 * i], f), __fmul_rn(o[4 * i + 1], f), __fmul_rn(o[4 * i + 2], f),
+                                 __fmul_rn(o[4 * i + 3], f));
+        }
+      }
+    } else {
+      atomicExch(failed, 1);
+    }
+  } else if (warp < kPfMmaWarp) {
+    // ================= dequantization of the key tiles =================
+    const int dt = tid - 32 * kPfSoftmaxWarps;
+    const int kr = dt & 7, kb = (dt >> 3) & 7, kg2 = dt >> 6;  // K': key row, block, key-group parity
+    const int vkg = dt & 15, vb = dt >> 4;                     // V'^T: key group of 8, block
+    int kkeys[8], vkeys[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      kkeys[j] = kr + 8 * (kg2 + 2 * j);
+      vkeys[j] = 8 * vkg + j;
+    }
+    PfCodes8 kpre, vpre;
+    pf_load8(view, a, h, 0, a.k_codes, a.k_scales, kkeys, kb, kpre);
+    pf_load8(view, a, h, 0, a.v_codes, a.v_scales, vkeys, vb, vpre);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int64_t t_next = (int64_t)(j + 1) * kPfTile;
+      const int bf = j & 1, use = j >> 1, tb = j % kPfKeyBufs;
+      uint8_t* kbuf = Kb + bf * kTileStd;
+      uint8_t* vbuf = Vt + bf * kTileV;
+      // ---- K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it ----
+      if (j >= 2 && !pf_wait_warp(&k_free[bf], (use - 1) & 1)) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int key = kkeys[u];
+        const uint32_t x = kpre.x[u];
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (x >> 8) decode_block_bf16(kpre.c[u], x & 0xFFu, w);
+        if (kb == 0) {
+          const int vs = (int)(x >> 8) - 1;
+          key_a[tb * kPfTile + key] = vs >= 0 ? slot_a[vs] : 0.0f;
+          key_gv[tb * kPfTile + key] = vs >= 0 ? slot_gv[vs] : 0.0f;
+          key_off[tb * kPfTile + key] = vs >= 0 ? vs * kPfRows : -1;
+        }
+        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      if (j + 1 < n_tiles) pf_load8(view, a, h, t_next, a.k_codes, a.k_scales, kkeys, kb, kpre);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&k_full[bf]);
+      // ---- V'(j) into buffer j % 2, once both P' V'(j - 2) MMAs have read it ----
+      if (j >= 2 && !pf_wait_warp(&v_free[bf], (use - 1) & 1)) break;
+      {
+        uint32_t w[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t x = vpre.x[u];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+          if (x >> 8) decode_block_bf16(vpre.c[u], x & 0xFFu, w[u]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // channel 16 vb + i of keys 8 vkg .. 8 vkg + 7: one 16-byte chunk
+          uint32_t o[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t lo = (i & 1) ? (w[2 * p][i >> 1] >> 16) : (w[2 * p][i >> 1] & 0xFFFFu);
+            const uint32_t hi = (i & 1) ? (w[2 * p + 1][i >> 1] >> 16) : (w[2 * p + 1][i >> 1] & 0xFFFFu);
+            o[p] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(vbuf + core_off(16 * vb + i, vkg, kLboV, kSboV)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (j + 1 < n_tiles) pf_load8(view, a, h, t_next, a.v_codes, a.v_scales, vkeys, vb, vpre);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&v_full[bf]);
+      if (__any_sync(0xffffffffu, *vfailed != 0)) break;
+    }
+  } else if (lane == 0) {
+    // ================= MMA issue, ping-ponging the halves =================
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfTile >> 3) << 17) |
+                           ((uint32_t)(kPfTile >> 4) << 24);  // bf16 x bf16 -> fp32, K-major, M = N = 128
+    bool ok = true;
+    for (int j = 0; j <= n_tiles && ok; ++j) {
+      const bool prev = j > 0, cur = j < n_tiles;
+      const int pj = j - 1;
+      if (cur && !mbar_wait(&k_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+      if (prev && !mbar_wait(&v_full[pj & 1], (pj >> 1) & 1)) { ok = false; break; }
+      for (int hh = 0; hh < kPfHalves && ok; ++hh) {
+        if (prev) {  // O_hh (+)= P'_hh(j - 1) V'(j - 1)
+          if (!mbar_wait(&p_full[hh], pj & 1)) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          pf_mma_tile_ta(tmem + 256 + hh * 128, tmem + hh * 128, smem_u32(Vt + (pj & 1) * kTileV), kLboV, kSboV,
+                         idesc, pj > 0);
+          pf_commit(&o_done[hh]);
+          if (hh == kPfHalves - 1) pf_commit(&v_free[pj & 1]);
+        }
+        if (cur) {  // S_hh(j) = Q_hh K'(j)^T, over P'_hh(j - 1) once its MMAs have read it
+          if (prev && !mbar_wait(&o_done[hh], pj & 1)) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          pf_mma_tile(tmem + hh * 128, smem_u32(Qs + hh * kTileStd), kLboStd, kSboStd, smem_u32(Kb + (j & 1) * kTileStd),
+                      kLboStd, kSboStd, idesc, false);
+          pf_commit(&s_full[hh]);
+          if (hh == kPfHalves - 1) pf_commit(&k_free[j & 1]);
+        }
+      }
+      if (*vfailed) ok = false;
+    }
+    if (!ok) atomicExch(failed, 1);
+    pf_commit(drain);
+    if (!mbar_wait(drain, 0)) atomicExch(failed, 1);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  if (tid == 0 && *vfailed && a.dev_status) atomicOr(a.dev_status, NVFP4_DEV_TIMEOUT);
+  if (warp == kPfMmaWarp) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
 }
 
 bool pf_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -462,6 +581,7 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
   if (n_frames < 1 || n_frames > NVFP4_MAX_VIEW_FRAMES || tokens_per_frame < 1 || pool_rows < 1 || n_meta < 1)
     return NVFP4_ESHAPE;
   if (tokens_per_frame > ((int64_t)1 << 40) / NVFP4_MAX_VIEW_FRAMES) return NVFP4_ESHAPE;
+  if ((int64_t)n_frames * tokens_per_frame > INT32_MAX) return NVFP4_ESHAPE;  // key indices in 32 bits
   if ((int64_t)H * D > ((int64_t)1 << 46) / pool_rows || (int64_t)H * D > ((int64_t)1 << 46) / n_q)
     return NVFP4_ESHAPE;
   if (!q_bf16 || !k_codes || !k_scales || !k_g || !v_codes || !v_scales || !v_g || !frame_row || !frame_meta || !out)
@@ -503,7 +623,7 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
   if (cudaFuncSetAttribute(nvfp4::attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nvfp4::kPfSmem) !=
       cudaSuccess)
     return NVFP4_ECUDA;
-  const int64_t q_per_cta = nvfp4::kPfTile * nvfp4::kPfHalves;
+  const int64_t q_per_cta = nvfp4::kPfRows;
   const dim3 grid((unsigned)((n_q + q_per_cta - 1) / q_per_cta), (unsigned)H);
   nvfp4::attn_prefill_kernel<<<grid, nvfp4::kPfThreads, nvfp4::kPfSmem, static_cast<cudaStream_t>(stream)>>>(view, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;

@@ -123,16 +123,34 @@ __device__ __forceinline__ void pf_ld32(uint32_t taddr, float v[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // 16 values of one block (8 code bytes, E4M3 scale byte) as exact bf16 pairs:
-// w[j] holds channels 2j (low half) and 2j + 1.
+// w[j] holds channels 2j (low half) and 2j + 1.  No conversion instructions: the bf16 bytes of
+// the eight E2M1 magnitudes (0, 0.5, 1, 1.5, 2, 3, 4, 6 = 0x0000, 0x3F00, 0x3F80, 0x3FC0, 0x4000,
+// 0x4040, 0x4080, 0x40C0) are two 8-entry byte tables, read by one byte permute per four values;
+// the code's sign bit is or-ed into the high byte; one packed bf16 multiply by the block scale E
+// ends it.  |E2M1| has at most 2 significant bits and E4M3 at most 4, so the product is exact in
+// bf16 and lies in [2^-10, 2688], inside its normal range.
 __device__ __forceinline__ void decode_block_bf16(uint2 codes, uint32_t scale_byte, uint32_t w[8]) {
-  const float E = e4m3_value(scale_byte);
+  const uint32_t E2 = __byte_perm(__float_as_uint(e4m3_value(scale_byte)), 0u, 0x3232);  // E exact in bf16
   const uint32_t c[2] = {codes.x, codes.y};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t h2 = e2m1x2_to_f16x2((c[j >> 2] >> (8 * (j & 3))) & 0xFFu);
-    const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(f16lo(h2), E), __fmul_rn(f16hi(h2), E)));
-    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t mag = c[q] & 0x77777777u, s4 = c[q] << 4;  // s4: even codes' sign bits at bit 7 of a byte
+#pragma unroll
+    for (int hq = 0; hq < 2; ++hq) {  // codes 4 hq .. 4 hq + 3 of this word
+      const uint32_t sel = hq ? (mag >> 16) : mag;
+      const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
+      const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
+      const uint32_t hs = hi | (__byte_perm(s4, c[q], hq ? 0x7362 : 0x5140) & 0x80808080u);
+      w[4 * q + 2 * hq] = bf16x2_mul(__byte_perm(lo, hs, 0x5140), E2);
+      w[4 * q + 2 * hq + 1] = bf16x2_mul(__byte_perm(lo, hs, 0x7362), E2);
+    }
   }
 }
 
@@ -198,16 +216,28 @@ __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, ui
 }
 
 // One dequantization thread's share of a key tile's codes, loaded ahead of use:
-// eight (key, block) units of K' or eight keys x one block of V'.  x packs the
-// scale byte (bits 0-7) and 1 + the key's view slot (bits 8-15; 0: past the view).
+// eight (key, block) units of K' or eight keys x one block of V'.  Keys past the view keep zero
+// codes and a zero scale, which decode to zeros.  Nothing here reads a loaded value, so the loads
+// stay in flight until the tile is decoded.
 struct PfCodes8 {
   uint2 c[8];
-  uint32_t x[8];
+  uint32_t s[8];  // E4M3 scale byte
 };
 
-// Loads the units of keys t0 + keys[j] (0 <= keys[j] < 128).  The view has fewer than 2^31 keys, so one
-// 32-bit division finds the frame of t0; each key's frame then follows by subtraction (at most
-// 127 / L_f + 1 steps, one for frames of 128 tokens or more).
+// The frame holding key t0 + key and the key's offset in it, from t0's frame f0 and offset r0
+// (at most 127 / L_f + 1 subtractions, one for frames of 128 tokens or more).
+__device__ __forceinline__ uint32_t pf_walk(uint32_t f0, uint32_t r0, uint32_t key, uint32_t L, uint32_t& rr) {
+  uint32_t f = f0;
+  rr = r0 + key;
+  while (rr >= L) {
+    rr -= L;
+    ++f;
+  }
+  return f;
+}
+
+// Loads the units of keys t0 + keys[j] (0 <= keys[j] < 128).  The view has fewer than 2^31 keys,
+// so one 32-bit division finds the frame of t0.
 __device__ __forceinline__ void pf_load8(const PfView& view, const PfArgs& a, int h, int64_t t0, const uint8_t* codes,
                                          const uint8_t* scales, const int keys[8], int blk, PfCodes8& r) {
   const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys, u0 = (uint32_t)t0;
@@ -215,17 +245,13 @@ __device__ __forceinline__ void pf_load8(const PfView& view, const PfArgs& a, in
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     r.c[j] = make_uint2(0u, 0u);
-    r.x[j] = 0u;
+    r.s[j] = 0u;
     if (u0 + (uint32_t)keys[j] < n_keys) {
-      uint32_t f = f0, rr = r0 + (uint32_t)keys[j];
-      while (rr >= L) {
-        rr -= L;
-        ++f;
-      }
-      const int vs = view.vslot[f];
+      uint32_t rr;
+      const uint32_t f = pf_walk(f0, r0, (uint32_t)keys[j], L, rr);
       const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
       r.c[j] = *reinterpret_cast<const uint2*>(codes + base * (kPfD / 2) + blk * 8);
-      r.x[j] = (uint32_t)scales[base * (kPfD / 16) + blk] | ((uint32_t)(vs + 1) << 8);
+      r.s[j] = scales[base * (kPfD / 16) + blk];
     }
   }
 }
@@ -472,14 +498,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       uint8_t* vbuf = Vt + bf * kTileV;
       // ---- K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it ----
       if (j >= 2 && !pf_wait_warp(&k_free[bf], (use - 1) & 1)) break;
+      const uint32_t L = (uint32_t)a.L_f, u0 = (uint32_t)(j * kPfTile);
+      const uint32_t f0 = u0 / L, r0 = u0 - f0 * L;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int key = kkeys[u];
-        const uint32_t x = kpre.x[u];
-        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (x >> 8) decode_block_bf16(kpre.c[u], x & 0xFFu, w);
-        if (kb == 0) {
-          const int vs = (int)(x >> 8) - 1;
+        uint32_t w[8];
+        decode_block_bf16(kpre.c[u], kpre.s[u], w);
+        if (kb == 0) {  // the key's factors: its view slot, -1 past the view
+          int vs = -1;
+          if (u0 + (uint32_t)key < (uint32_t)a.n_keys) {
+            uint32_t rr;
+            vs = view.vslot[pf_walk(f0, r0, (uint32_t)key, L, rr)];
+          }
           key_a[tb * kPfTile + key] = vs >= 0 ? slot_a[vs] : 0.0f;
           key_gv[tb * kPfTile + key] = vs >= 0 ? slot_gv[vs] : 0.0f;
           key_off[tb * kPfTile + key] = vs >= 0 ? vs * kPfRows : -1;
@@ -496,12 +527,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       {
         uint32_t w[8][8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t x = vpre.x[u];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w[u][i] = 0u;
-          if (x >> 8) decode_block_bf16(vpre.c[u], x & 0xFFu, w[u]);
-        }
+        for (int u = 0; u < 8; ++u) decode_block_bf16(vpre.c[u], vpre.s[u], w[u]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {  // channel 16 vb + i of keys 8 vkg .. 8 vkg + 7: one 16-byte chunk
           uint32_t o[4];

@@ -60,7 +60,8 @@ constexpr int kPfHalves = 2;           // query halves per CTA sharing each K'/V
 constexpr int kPfRows = 128 * kPfHalves;
 constexpr int kPfD = 128;              // head dimension
 constexpr int kPfSoftmaxWarps = 4 * kPfHalves;
-constexpr int kPfDequantWarps = 4;
+constexpr int kPfDequantWarps = 8;  // 4 for K', 4 for V'
+constexpr int kPfKWarps = 4;
 constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDequantWarps;
 constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
 constexpr int kPfMaxSlots = 16;        // distinct pool slots in one view
@@ -129,28 +130,64 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Issues a 32-column TMEM load without waiting for it (pf_wait_ld32 completes it).
+__device__ __forceinline__ void pf_ld32_issue(uint32_t taddr, uint32_t r[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Marks 32 registers as written here, so that no use of them moves above a preceding wait::ld.
+__device__ __forceinline__ void pf_tie32(uint32_t r[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                 "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),
+                 "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
+__device__ __forceinline__ void pf_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 16 values of one block (8 code bytes, E4M3 scale byte) as exact bf16 pairs:
 // w[j] holds channels 2j (low half) and 2j + 1.  No conversion instructions: the bf16 bytes of
 // the eight E2M1 magnitudes (0, 0.5, 1, 1.5, 2, 3, 4, 6 = 0x0000, 0x3F00, 0x3F80, 0x3FC0, 0x4000,
 // 0x4040, 0x4080, 0x40C0) are two 8-entry byte tables, read by one byte permute per four values;
 // the code's sign bit is or-ed into the high byte; one packed bf16 multiply by the block scale E
 // ends it.  |E2M1| has at most 2 significant bits and E4M3 at most 4, so the product is exact in
-// bf16 and lies in [2^-10, 2688], inside its normal range.
-__device__ __forceinline__ void decode_block_bf16(uint2 codes, uint32_t scale_byte, uint32_t w[8]) {
-  const uint32_t E2 = __byte_perm(__float_as_uint(e4m3_value(scale_byte)), 0u, 0x3232);  // E exact in bf16
-  const uint32_t c[2] = {codes.x, codes.y};
+// bf16 and lies in [2^-10, 2688], inside its normal range.  A block is two words.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t scale_byte) {  // E in both halves, exact in bf16
+  return __byte_perm(__float_as_uint(e4m3_value(scale_byte)), 0u, 0x3232);
+}
+
+// Eight codes (one 32-bit word, code 2j + k in bits 8j + 4k .. + 3) times E2 -> w[0..3].
+__device__ __forceinline__ void decode_word_bf16(uint32_t cw, uint32_t E2, uint32_t w[4]) {
+  const uint32_t mag = cw & 0x77777777u, s4 = cw << 4;  // s4: even codes' sign bits at bit 7 of a byte
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint32_t mag = c[q] & 0x77777777u, s4 = c[q] << 4;  // s4: even codes' sign bits at bit 7 of a byte
-#pragma unroll
-    for (int hq = 0; hq < 2; ++hq) {  // codes 4 hq .. 4 hq + 3 of this word
-      const uint32_t sel = hq ? (mag >> 16) : mag;
-      const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
-      const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
-      const uint32_t hs = hi | (__byte_perm(s4, c[q], hq ? 0x7362 : 0x5140) & 0x80808080u);
-      w[4 * q + 2 * hq] = bf16x2_mul(__byte_perm(lo, hs, 0x5140), E2);
-      w[4 * q + 2 * hq + 1] = bf16x2_mul(__byte_perm(lo, hs, 0x7362), E2);
-    }
+  for (int hq = 0; hq < 2; ++hq) {  // codes 4 hq .. 4 hq + 3
+    const uint32_t sel = hq ? (mag >> 16) : mag;
+    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
+    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
+    const uint32_t hs = hi | (__byte_perm(s4, cw, hq ? 0x7362 : 0x5140) & 0x80808080u);
+    w[2 * hq] = bf16x2_mul(__byte_perm(lo, hs, 0x5140), E2);
+    w[2 * hq + 1] = bf16x2_mul(__byte_perm(lo, hs, 0x7362), E2);
   }
 }
 
@@ -299,9 +336,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], kPfDequantWarps);
+      mbar_init(&k_full[i], kPfKWarps);
       mbar_init(&k_free[i], 1);
-      mbar_init(&v_full[i], kPfDequantWarps);
+      mbar_init(&v_full[i], kPfDequantWarps - kPfKWarps);
       mbar_init(&v_free[i], 1);
     }
     for (int i = 0; i < kPfHalves; ++i) {
@@ -388,14 +425,48 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // pass 1: the tile's maximum of t = (scale log2e) (g_k S + q . mean)
       float mt = -INFINITY;
+      if (uvs >= 0) {
+        // one slot: t = fmaf(ua, S, ub) is monotonic in S (non-decreasing for ua >= 0), so the
+        // maximum is fmaf(ua, S*, ub) with S* the largest S (the smallest for ua < 0)
+        const bool up = ua >= 0.0f;
+        float e0 = up ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float t[32];
-        pf_ld32(t_S + 32 * c, t);
-        if (uvs >= 0) {
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t r0[32], r1[32];
+          pf_ld32_issue(t_S + 32 * c, r0);
+          pf_ld32_issue(t_S + 32 * c + 32, r1);
+          pf_wait_ld();
+          pf_tie32(r0);
+          pf_tie32(r1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __fmaf_rn(ua, t[i], ub));
-        } else {
+          for (int i = 0; i < 32; i += 8) {
+            if (up) {
+              e0 = fmax3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+              e1 = fmax3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+              e2 = fmax3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
+              e3 = fmax3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
+              e0 = fmax3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+              e1 = fmax3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+              e2 = fmax3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
+              e3 = fmax3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
+            } else {
+              e0 = fmin3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+              e1 = fmin3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+              e2 = fmin3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
+              e3 = fmin3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
+              e0 = fmin3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+              e1 = fmin3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+              e2 = fmin3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
+              e3 = fmin3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
+            }
+          }
+        }
+        mt = __fmaf_rn(ua, up ? fmax3(e0, e1, fmaxf(e2, e3)) : fmin3(e0, e1, fminf(e2, e3)), ub);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float t[32];
+          pf_ld32(t_S + 32 * c, t);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int k = 32 * c + i, off = koff[k];
@@ -423,34 +494,46 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
       }
       // pass 2: P' = bf16(2^(t - m) g_v / G) into TMEM over S (columns already read), and l
-      float sum = 0.0f;
+      float2 sa = make_float2(0.0f, 0.0f), sb = sa;
+      if (uvs >= 0) {  // pairs of keys in packed fp32x2 arithmetic; t - m = fmaf(ua, S, ub - m)
+        const float2 ua2 = make_float2(ua, ua), c2 = make_float2(__fsub_rn(ub, m), __fsub_rn(ub, m));
+        const float2 g2 = make_float2(ugv, ugv);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float t[32];
-        pf_ld32(t_S + 32 * c, t);
-        uint32_t pw[16];
+        for (int c = 0; c < 4; ++c) {
+          float t[32];
+          pf_ld32(t_S + 32 * c, t);
+          uint32_t pw[16];
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          const int i = 2 * p, k = 32 * c + i;
-          float p0, p1, g0, g1;
-          if (uvs >= 0) {
-            p0 = ex2_approx(__fmaf_rn(ua, t[i], ub) - m);
-            p1 = ex2_approx(__fmaf_rn(ua, t[i + 1], ub) - m);
-            g0 = ugv;
-            g1 = ugv;
-          } else {
-            const int o0 = koff[k], o1 = koff[k + 1];
-            p0 = o0 >= 0 ? ex2_approx(__fmaf_rn(ka[k], t[i], qm[o0 + tid]) - m) : 0.0f;
-            p1 = o1 >= 0 ? ex2_approx(__fmaf_rn(ka[k + 1], t[i + 1], qm[o1 + tid]) - m) : 0.0f;
-            g0 = kgv[k];
-            g1 = kgv[k + 1];
+          for (int p = 0; p < 16; ++p) {
+            const float2 x = __ffma2_rn(make_float2(t[2 * p], t[2 * p + 1]), ua2, c2);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (p & 1) sb = __fadd2_rn(sb, e); else sa = __fadd2_rn(sa, e);
+            const float2 q = __fmul2_rn(e, g2);
+            const __nv_bfloat162 b = __float22bfloat162_rn(q);
+            pw[p] = *reinterpret_cast<const uint32_t*>(&b);
           }
-          sum = __fadd_rn(sum, __fadd_rn(p0, p1));
-          const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(p0, g0), __fmul_rn(p1, g1)));
-          pw[p] = *reinterpret_cast<const uint32_t*>(&b);
+          pf_st16(t_S + 16 * c, pw);  // keys 32 c .. 32 c + 31: columns 16 c .. 16 c + 15, S there already read
         }
-        pf_st16(t_S + 16 * c, pw);  // keys 32 c .. 32 c + 31: columns 16 c .. 16 c + 15, S there already read
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float t[32];
+          pf_ld32(t_S + 32 * c, t);
+          uint32_t pw[16];
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const int i = 2 * p, k = 32 * c + i;
+            const int o0 = koff[k], o1 = koff[k + 1];
+            const float p0 = o0 >= 0 ? ex2_approx(__fmaf_rn(ka[k], t[i], qm[o0 + tid]) - m) : 0.0f;
+            const float p1 = o1 >= 0 ? ex2_approx(__fmaf_rn(ka[k + 1], t[i + 1], qm[o1 + tid]) - m) : 0.0f;
+            if (p & 1) sb = __fadd2_rn(sb, make_float2(p0, p1)); else sa = __fadd2_rn(sa, make_float2(p0, p1));
+            const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(p0, kgv[k]), __fmul_rn(p1, kgv[k + 1])));
+            pw[p] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          pf_st16(t_S + 16 * c, pw);
+        }
       }
+      const float sum = __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sb.x, sb.y));
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l = __fadd_rn(l, sum);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -477,26 +560,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     } else {
       atomicExch(failed, 1);
     }
-  } else if (warp < kPfMmaWarp) {
-    // ================= dequantization of the key tiles =================
+  } else if (warp < kPfSoftmaxWarps + kPfKWarps) {
+    // ================= K' tiles, with the per-key factors =================
     const int dt = tid - 32 * kPfSoftmaxWarps;
-    const int kr = dt & 7, kb = (dt >> 3) & 7, kg2 = dt >> 6;  // K': key row, block, key-group parity
-    const int vkg = dt & 15, vb = dt >> 4;                     // V'^T: key group of 8, block
-    int kkeys[8], vkeys[8];
+    const int kr = dt & 7, kb = (dt >> 3) & 7, kg2 = dt >> 6;  // key row, block, key-group parity
+    int kkeys[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      kkeys[j] = kr + 8 * (kg2 + 2 * j);
-      vkeys[j] = 8 * vkg + j;
-    }
-    PfCodes8 kpre, vpre;
+    for (int j = 0; j < 8; ++j) kkeys[j] = kr + 8 * (kg2 + 2 * j);
+    PfCodes8 kpre;
     pf_load8(view, a, h, 0, a.k_codes, a.k_scales, kkeys, kb, kpre);
-    pf_load8(view, a, h, 0, a.v_codes, a.v_scales, vkeys, vb, vpre);
     for (int j = 0; j < n_tiles; ++j) {
-      const int64_t t_next = (int64_t)(j + 1) * kPfTile;
       const int bf = j & 1, use = j >> 1, tb = j % kPfKeyBufs;
       uint8_t* kbuf = Kb + bf * kTileStd;
-      uint8_t* vbuf = Vt + bf * kTileV;
-      // ---- K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it ----
+      // K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it
       if (j >= 2 && !pf_wait_warp(&k_free[bf], (use - 1) & 1)) break;
       const uint32_t L = (uint32_t)a.L_f, u0 = (uint32_t)(j * kPfTile);
       const uint32_t f0 = u0 / L, r0 = u0 - f0 * L;
@@ -504,7 +580,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       for (int u = 0; u < 8; ++u) {
         const int key = kkeys[u];
         uint32_t w[8];
-        decode_block_bf16(kpre.c[u], kpre.s[u], w);
+        const uint32_t E2 = scale_bf16x2(kpre.s[u]);
+        decode_word_bf16(kpre.c[u].x, E2, w);
+        decode_word_bf16(kpre.c[u].y, E2, w + 4);
         if (kb == 0) {  // the key's factors: its view slot, -1 past the view
           int vs = -1;
           if (u0 + (uint32_t)key < (uint32_t)a.n_keys) {
@@ -518,29 +596,40 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (j + 1 < n_tiles) pf_load8(view, a, h, t_next, a.k_codes, a.k_scales, kkeys, kb, kpre);
+      if (j + 1 < n_tiles) pf_load8(view, a, h, (int64_t)(j + 1) * kPfTile, a.k_codes, a.k_scales, kkeys, kb, kpre);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&k_full[bf]);
-      // ---- V'(j) into buffer j % 2, once both P' V'(j - 2) MMAs have read it ----
+      if (__any_sync(0xffffffffu, *vfailed != 0)) break;
+    }
+  } else if (warp < kPfMmaWarp) {
+    // ================= V'^T tiles =================
+    const int dt = tid - 32 * (kPfSoftmaxWarps + kPfKWarps);
+    const int vkg = dt & 15, vb = dt >> 4;  // key group of 8, block
+    int vkeys[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) vkeys[j] = 8 * vkg + j;
+    PfCodes8 vpre;
+    pf_load8(view, a, h, 0, a.v_codes, a.v_scales, vkeys, vb, vpre);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int bf = j & 1, use = j >> 1;
+      uint8_t* vbuf = Vt + bf * kTileV;
+      // V'(j) into buffer j % 2, once both P' V'(j - 2) MMAs have read it
       if (j >= 2 && !pf_wait_warp(&v_free[bf], (use - 1) & 1)) break;
-      {
-        uint32_t w[8][8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) decode_block_bf16(vpre.c[u], vpre.s[u], w[u]);
+      for (int q = 0; q < 2; ++q) {  // channels 16 vb + 8 q .. + 7 of the eight keys
+        uint32_t w[8][4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {  // channel 16 vb + i of keys 8 vkg .. 8 vkg + 7: one 16-byte chunk
+        for (int u = 0; u < 8; ++u) decode_word_bf16(q ? vpre.c[u].y : vpre.c[u].x, scale_bf16x2(vpre.s[u]), w[u]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // channel 16 vb + 8 q + i of keys 8 vkg .. 8 vkg + 7: one 16-byte chunk
           uint32_t o[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t lo = (i & 1) ? (w[2 * p][i >> 1] >> 16) : (w[2 * p][i >> 1] & 0xFFFFu);
-            const uint32_t hi = (i & 1) ? (w[2 * p + 1][i >> 1] >> 16) : (w[2 * p + 1][i >> 1] & 0xFFFFu);
-            o[p] = lo | (hi << 16);
-          }
-          *reinterpret_cast<uint4*>(vbuf + core_off(16 * vb + i, vkg, kLboV, kSboV)) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int p = 0; p < 4; ++p) o[p] = __byte_perm(w[2 * p][i >> 1], w[2 * p + 1][i >> 1], (i & 1) ? 0x7632 : 0x5410);
+          *reinterpret_cast<uint4*>(vbuf + core_off(16 * vb + 8 * q + i, vkg, kLboV, kSboV)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      if (j + 1 < n_tiles) pf_load8(view, a, h, t_next, a.v_codes, a.v_scales, vkeys, vb, vpre);
+      if (j + 1 < n_tiles) pf_load8(view, a, h, (int64_t)(j + 1) * kPfTile, a.v_codes, a.v_scales, vkeys, vb, vpre);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&v_full[bf]);

@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         // maximum is fmaf(ua, S*, ub) with S* the largest S (the smallest for ua < 0)
         const bool up = ua >= 0.0f;
         float e0 = up ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; c += 2) {
           uint32_t r0[32], r1[32];
           pf_ld32_issue(t_S + 32 * c, r0);
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
         mt = __fmaf_rn(ua, up ? fmax3(e0, e1, fmaxf(e2, e3)) : fmin3(e0, e1, fminf(e2, e3)), ub);
       } else {
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         l = __fmul_rn(l, f);
         m = m_new;
         if (j > 0) {  // O holds earlier tiles: scale this row (warp-wide TMEM access)
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
             pf_ld32(t_O + 32 * c, o);
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       if (uvs >= 0) {  // pairs of keys in packed fp32x2 arithmetic; t - m = fmaf(ua, S, ub - m)
         const float2 ua2 = make_float2(ua, ua), c2 = make_float2(__fsub_rn(ub, m), __fsub_rn(ub, m));
         const float2 g2 = make_float2(ugv, ugv);
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
           pf_st16(t_S + 16 * c, pw);  // keys 32 c .. 32 c + 31: columns 16 c .. 16 c + 15, S there already read
         }
       } else {
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     if (ok && pf_wait_warp(&o_done[half], (n_tiles - 1) & 1)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const float f = __fdiv_rn(G, l);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
         pf_ld32(t_O + 32 * c, o);
@@ -560,43 +560,58 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     } else {
       atomicExch(failed, 1);
     }
-  } else if (warp < kPfSoftmaxWarps + kPfKWarps) {
+  } else if (warp < kPfMmaWarp && ((warp - kPfSoftmaxWarps) & 2) == 0) {
     // ================= K' tiles, with the per-key factors =================
-    const int dt = tid - 32 * kPfSoftmaxWarps;
-    const int kr = dt & 7, kb = (dt >> 3) & 7, kg2 = dt >> 6;  // key row, block, key-group parity
-    int kkeys[8];
+    // Thread `key` owns key `key` of every tile: its 64 code bytes and 8 scale bytes, loaded one
+    // tile ahead (nothing reads them until the tile is decoded), and its factors in the tables.
+    const int dq = warp - kPfSoftmaxWarps;  // 0, 1, 4, 5: warps 8, 9, 12, 13 (sub-partitions 0 and 1)
+    const int key = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
+    const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
+    uint32_t f = (uint32_t)key / L, rr = (uint32_t)key - f * L;  // frame and offset of the key in tile 0
+    uint4 kc[4];
+    uint2 ks;
+    int kvs;  // view slot of the loaded key, -1 past the view
+    auto load_key = [&](uint32_t t) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) kkeys[j] = kr + 8 * (kg2 + 2 * j);
-    PfCodes8 kpre;
-    pf_load8(view, a, h, 0, a.k_codes, a.k_scales, kkeys, kb, kpre);
+      for (int i = 0; i < 4; ++i) kc[i] = make_uint4(0u, 0u, 0u, 0u);
+      ks = make_uint2(0u, 0u);
+      kvs = -1;
+      if (t < n_keys) {
+        const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
+        const uint4* src = reinterpret_cast<const uint4*>(a.k_codes + base * (kPfD / 2));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kc[i] = src[i];
+        ks = *reinterpret_cast<const uint2*>(a.k_scales + base * (kPfD / 16));
+        kvs = view.vslot[f];
+      }
+    };
+    load_key((uint32_t)key);
     for (int j = 0; j < n_tiles; ++j) {
       const int bf = j & 1, use = j >> 1, tb = j % kPfKeyBufs;
       uint8_t* kbuf = Kb + bf * kTileStd;
       // K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it
       if (j >= 2 && !pf_wait_warp(&k_free[bf], (use - 1) & 1)) break;
-      const uint32_t L = (uint32_t)a.L_f, u0 = (uint32_t)(j * kPfTile);
-      const uint32_t f0 = u0 / L, r0 = u0 - f0 * L;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int key = kkeys[u];
+      for (int b = 0; b < 8; ++b) {  // block b: code bytes 8 b .. 8 b + 7, scale byte b
+        const uint4 c4 = kc[b >> 1];
+        const uint32_t E2 = scale_bf16x2(((b < 4 ? ks.x : ks.y) >> (8 * (b & 3))) & 0xFFu);
         uint32_t w[8];
-        const uint32_t E2 = scale_bf16x2(kpre.s[u]);
-        decode_word_bf16(kpre.c[u].x, E2, w);
-        decode_word_bf16(kpre.c[u].y, E2, w + 4);
-        if (kb == 0) {  // the key's factors: its view slot, -1 past the view
-          int vs = -1;
-          if (u0 + (uint32_t)key < (uint32_t)a.n_keys) {
-            uint32_t rr;
-            vs = view.vslot[pf_walk(f0, r0, (uint32_t)key, L, rr)];
-          }
-          key_a[tb * kPfTile + key] = vs >= 0 ? slot_a[vs] : 0.0f;
-          key_gv[tb * kPfTile + key] = vs >= 0 ? slot_gv[vs] : 0.0f;
-          key_off[tb * kPfTile + key] = vs >= 0 ? vs * kPfRows : -1;
-        }
-        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * kb + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
+        decode_word_bf16((b & 1) ? c4.z : c4.x, E2, w);
+        decode_word_bf16((b & 1) ? c4.w : c4.y, E2, w + 4);
+        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * b, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * b + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (j + 1 < n_tiles) pf_load8(view, a, h, (int64_t)(j + 1) * kPfTile, a.k_codes, a.k_scales, kkeys, kb, kpre);
+      key_a[tb * kPfTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
+      key_gv[tb * kPfTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
+      key_off[tb * kPfTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
+      if (j + 1 < n_tiles) {
+        rr += kPfTile;
+        while (rr >= L) {
+          rr -= L;
+          ++f;
+        }
+        load_key((uint32_t)((j + 1) * kPfTile + key));
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&k_full[bf]);
@@ -604,7 +619,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     }
   } else if (warp < kPfMmaWarp) {
     // ================= V'^T tiles =================
-    const int dt = tid - 32 * (kPfSoftmaxWarps + kPfKWarps);
+    const int dq = warp - kPfSoftmaxWarps;  // 2, 3, 6, 7: warps 10, 11, 14, 15 (sub-partitions 2 and 3)
+    const int dt = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
     const int vkg = dt & 15, vb = dt >> 4;  // key group of 8, block
     int vkeys[8];
 #pragma unroll
@@ -701,7 +717,7 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
     return NVFP4_ESHAPE;
   if (!q_bf16 || !k_codes || !k_scales || !k_g || !v_codes || !v_scales || !v_g || !frame_row || !frame_meta || !out)
     return NVFP4_EINVAL;
-  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(k_codes, 8) || !nvfp4::pf_aligned(v_codes, 8) ||
+  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(k_codes, 16) || !nvfp4::pf_aligned(k_scales, 8) || !nvfp4::pf_aligned(v_codes, 8) ||
       !nvfp4::pf_aligned(k_g, 4) || !nvfp4::pf_aligned(v_g, 4) || !nvfp4::pf_aligned(out, 16) ||
       !nvfp4::pf_aligned(k_mean, 4) || !nvfp4::pf_aligned(dev_status, 4))
     return NVFP4_EALIGN;

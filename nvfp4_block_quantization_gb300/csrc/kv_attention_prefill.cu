@@ -252,10 +252,9 @@ __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, ui
   }
 }
 
-// One dequantization thread's share of a key tile's codes, loaded ahead of use:
-// eight (key, block) units of K' or eight keys x one block of V'.  Keys past the view keep zero
-// codes and a zero scale, which decode to zeros.  Nothing here reads a loaded value, so the loads
-// stay in flight until the tile is decoded.
+// One V' thread's share of a key tile's codes, loaded ahead of use: eight keys x one block.
+// Keys past the view keep zero codes and a zero scale, which decode to zeros.  Nothing reads a
+// loaded value before the tile is decoded, so the loads stay in flight meanwhile.
 struct PfCodes8 {
   uint2 c[8];
   uint32_t s[8];  // E4M3 scale byte
@@ -271,26 +270,6 @@ __device__ __forceinline__ uint32_t pf_walk(uint32_t f0, uint32_t r0, uint32_t k
     ++f;
   }
   return f;
-}
-
-// Loads the units of keys t0 + keys[j] (0 <= keys[j] < 128).  The view has fewer than 2^31 keys,
-// so one 32-bit division finds the frame of t0.
-__device__ __forceinline__ void pf_load8(const PfView& view, const PfArgs& a, int h, int64_t t0, const uint8_t* codes,
-                                         const uint8_t* scales, const int keys[8], int blk, PfCodes8& r) {
-  const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys, u0 = (uint32_t)t0;
-  const uint32_t f0 = u0 / L, r0 = u0 - f0 * L;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    r.c[j] = make_uint2(0u, 0u);
-    r.s[j] = 0u;
-    if (u0 + (uint32_t)keys[j] < n_keys) {
-      uint32_t rr;
-      const uint32_t f = pf_walk(f0, r0, (uint32_t)keys[j], L, rr);
-      const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
-      r.c[j] = *reinterpret_cast<const uint2*>(codes + base * (kPfD / 2) + blk * 8);
-      r.s[j] = scales[base * (kPfD / 16) + blk];
-    }
-  }
 }
 
 __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity) {
@@ -621,12 +600,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     // ================= V'^T tiles =================
     const int dq = warp - kPfSoftmaxWarps;  // 2, 3, 6, 7: warps 10, 11, 14, 15 (sub-partitions 2 and 3)
     const int dt = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
-    const int vkg = dt & 15, vb = dt >> 4;  // key group of 8, block
-    int vkeys[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) vkeys[j] = 8 * vkg + j;
+    const int vkg = dt & 15, vb = dt >> 4;  // keys 8 vkg .. 8 vkg + 7 of a tile, block vb
+    const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
+    uint32_t f = (uint32_t)(8 * vkg) / L, rr = (uint32_t)(8 * vkg) - f * L;  // frame and offset of key 8 vkg
+    const int64_t code_stride = (int64_t)a.H * (kPfD / 2), scale_stride = (int64_t)a.H * (kPfD / 16);
     PfCodes8 vpre;
-    pf_load8(view, a, h, 0, a.v_codes, a.v_scales, vkeys, vb, vpre);
+    // the eight keys from t0 on: consecutive pool rows unless the group crosses a frame
+    auto load_group = [&](uint32_t t0) {
+      const int64_t row0 = t0 < n_keys ? view.row[f] + (int64_t)rr : 0;
+      const uint8_t* cp = a.v_codes + (row0 * a.H + h) * (kPfD / 2) + vb * 8;
+      const uint8_t* sp = a.v_scales + (row0 * a.H + h) * (kPfD / 16) + vb;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        vpre.c[i] = make_uint2(0u, 0u);
+        vpre.s[i] = 0u;
+        if (t0 + i < n_keys) {
+          if (rr + i < L) {
+            vpre.c[i] = *reinterpret_cast<const uint2*>(cp + i * code_stride);
+            vpre.s[i] = sp[i * scale_stride];
+          } else {
+            uint32_t ri;
+            const int64_t base = (view.row[pf_walk(f, rr, (uint32_t)i, L, ri)] + (int64_t)ri) * a.H + h;
+            vpre.c[i] = *reinterpret_cast<const uint2*>(a.v_codes + base * (kPfD / 2) + vb * 8);
+            vpre.s[i] = a.v_scales[base * (kPfD / 16) + vb];
+          }
+        }
+      }
+    };
+    load_group((uint32_t)(8 * vkg));
     for (int j = 0; j < n_tiles; ++j) {
       const int bf = j & 1, use = j >> 1;
       uint8_t* vbuf = Vt + bf * kTileV;
@@ -645,7 +646,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
           *reinterpret_cast<uint4*>(vbuf + core_off(16 * vb + 8 * q + i, vkg, kLboV, kSboV)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      if (j + 1 < n_tiles) pf_load8(view, a, h, (int64_t)(j + 1) * kPfTile, a.v_codes, a.v_scales, vkeys, vb, vpre);
+      if (j + 1 < n_tiles) {
+        rr += kPfTile;
+        while (rr >= L) {
+          rr -= L;
+          ++f;
+        }
+        load_group((uint32_t)((j + 1) * kPfTile + 8 * vkg));
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&v_full[bf]);

@@ -66,14 +66,15 @@ constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDequantWarps;
 constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
 constexpr int kPfMaxSlots = 16;        // distinct pool slots in one view
 constexpr uint32_t kLboStd = 128, kSboStd = 2048;  // [128 rows][256 B]: core matrices 128 B apart along K
-constexpr uint32_t kLboV = 144, kSboV = 2304;      // the padded V' tile
+// V' [key][d] as an MN-major B operand: LBO = 2048 between groups of 8 keys (the K direction),
+// SBO = 128 between groups of 8 channels (the N direction).
+constexpr uint32_t kLboV = 2048, kSboV = 128;
 constexpr int kTileStd = 32768;
-constexpr int kTileV = 36864;
 constexpr float kRescaleStep = 8.0f;  // base-2 units the running maximum may lag behind
 // Q (2 halves), K' (2 buffers), V'^T (2 buffers), q . mean per row and slot, key tables (3 buffers), slot
 // tables, barriers; P' lives in TMEM over its half's S
 constexpr int kPfKeyBufs = 3;
-constexpr int kPfSmem = kPfHalves * kTileStd + 2 * kTileStd + 2 * kTileV + kPfMaxSlots * kPfRows * 4 +
+constexpr int kPfSmem = kPfHalves * kTileStd + 2 * kTileStd + 2 * kTileStd + kPfMaxSlots * kPfRows * 4 +
                         kPfKeyBufs * 3 * kPfTile * 4 + 2 * kPfMaxSlots * 4 + 256;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
@@ -191,13 +192,6 @@ __device__ __forceinline__ void decode_word_bf16(uint32_t cw, uint32_t E2, uint3
   }
 }
 
-// The view token of key t: its pool row and the view-slot index of its chunk.
-__device__ __forceinline__ void key_location(const PfView& view, int64_t L_f, int64_t t, int64_t& row, int& vs) {
-  const int64_t f = t / L_f;
-  row = view.row[f] + (t - f * L_f);
-  vs = view.vslot[f];
-}
-
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -252,26 +246,6 @@ __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, ui
   }
 }
 
-// One V' thread's share of a key tile's codes, loaded ahead of use: eight keys x one block.
-// Keys past the view keep zero codes and a zero scale, which decode to zeros.  Nothing reads a
-// loaded value before the tile is decoded, so the loads stay in flight meanwhile.
-struct PfCodes8 {
-  uint2 c[8];
-  uint32_t s[8];  // E4M3 scale byte
-};
-
-// The frame holding key t0 + key and the key's offset in it, from t0's frame f0 and offset r0
-// (at most 127 / L_f + 1 subtractions, one for frames of 128 tokens or more).
-__device__ __forceinline__ uint32_t pf_walk(uint32_t f0, uint32_t r0, uint32_t key, uint32_t L, uint32_t& rr) {
-  uint32_t f = f0;
-  rr = r0 + key;
-  while (rr >= L) {
-    rr -= L;
-    ++f;
-  }
-  return f;
-}
-
 __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
@@ -286,8 +260,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   extern __shared__ __align__(128) uint8_t pf_smem[];
   uint8_t* Qs = pf_smem;                          // Q of both halves, bf16 [query][d]
   uint8_t* Kb = Qs + kPfHalves * kTileStd;        // K' tiles [buffer][key][d]
-  uint8_t* Vt = Kb + 2 * kTileStd;                // V'^T tiles [buffer][d][key], padded
-  float* qm = reinterpret_cast<float*>(Vt + 2 * kTileV);  // [view slot][row]: scale log2e q . mean
+  uint8_t* Vt = Kb + 2 * kTileStd;                // V' tiles [buffer][key][d]
+  float* qm = reinterpret_cast<float*>(Vt + 2 * kTileStd);  // [view slot][row]: scale log2e q . mean
   float* key_a = qm + kPfMaxSlots * kPfRows;              // [table buffer][key]: scale log2e g_k
   float* key_gv = key_a + kPfKeyBufs * kPfTile;           // [table buffer][key]: g_v / G (0 past the view)
   int* key_off = reinterpret_cast<int*>(key_gv + kPfKeyBufs * kPfTile);  // slot offset in qm, -1 past the view
@@ -539,12 +513,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     } else {
       atomicExch(failed, 1);
     }
-  } else if (warp < kPfMmaWarp && ((warp - kPfSoftmaxWarps) & 2) == 0) {
-    // ================= K' tiles, with the per-key factors =================
-    // Thread `key` owns key `key` of every tile: its 64 code bytes and 8 scale bytes, loaded one
-    // tile ahead (nothing reads them until the tile is decoded), and its factors in the tables.
-    const int dq = warp - kPfSoftmaxWarps;  // 0, 1, 4, 5: warps 8, 9, 12, 13 (sub-partitions 0 and 1)
+  } else if (warp < kPfMmaWarp) {
+    // ================= K' and V' tiles, one key per thread =================
+    // Warps 8, 9, 12, 13 (sub-partitions 0 and 1) decode K' and write the key factors; warps
+    // 10, 11, 14, 15 (sub-partitions 2 and 3) decode V'.  Thread `key` owns key `key` of every
+    // tile: its 64 code bytes and 8 scale bytes are loaded one tile ahead (nothing reads them
+    // until the tile is decoded) and its 128 bf16 channels stored as 16 chunks of 16 bytes, the
+    // same [key][d] core-matrix layout for both (K-major for S = Q K'^T, MN-major for P' V').
+    const int dq = warp - kPfSoftmaxWarps;
+    const bool is_k = (dq & 2) == 0;
     const int key = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
+    const uint8_t* codes = is_k ? a.k_codes : a.v_codes;
+    const uint8_t* scales = is_k ? a.k_scales : a.v_scales;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* free_ = is_k ? k_free : v_free;
+    uint8_t* tiles = is_k ? Kb : Vt;
     const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
     uint32_t f = (uint32_t)key / L, rr = (uint32_t)key - f * L;  // frame and offset of the key in tile 0
     uint4 kc[4];
@@ -557,19 +540,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       kvs = -1;
       if (t < n_keys) {
         const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
-        const uint4* src = reinterpret_cast<const uint4*>(a.k_codes + base * (kPfD / 2));
+        const uint4* src = reinterpret_cast<const uint4*>(codes + base * (kPfD / 2));
 #pragma unroll
         for (int i = 0; i < 4; ++i) kc[i] = src[i];
-        ks = *reinterpret_cast<const uint2*>(a.k_scales + base * (kPfD / 16));
+        ks = *reinterpret_cast<const uint2*>(scales + base * (kPfD / 16));
         kvs = view.vslot[f];
       }
     };
     load_key((uint32_t)key);
     for (int j = 0; j < n_tiles; ++j) {
       const int bf = j & 1, use = j >> 1, tb = j % kPfKeyBufs;
-      uint8_t* kbuf = Kb + bf * kTileStd;
-      // K'(j) into buffer j % 2, once both S(j - 2) MMAs have read it
-      if (j >= 2 && !pf_wait_warp(&k_free[bf], (use - 1) & 1)) break;
+      uint8_t* buf = tiles + bf * kTileStd;
+      // tile j into buffer j % 2, once both MMAs of tile j - 2 have read it
+      if (j >= 2 && !pf_wait_warp(&free_[bf], (use - 1) & 1)) break;
 #pragma unroll
       for (int b = 0; b < 8; ++b) {  // block b: code bytes 8 b .. 8 b + 7, scale byte b
         const uint4 c4 = kc[b >> 1];
@@ -577,12 +560,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         uint32_t w[8];
         decode_word_bf16((b & 1) ? c4.z : c4.x, E2, w);
         decode_word_bf16((b & 1) ? c4.w : c4.y, E2, w + 4);
-        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * b, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(kbuf + core_off(key, 2 * b + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
+        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * b, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * b + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      key_a[tb * kPfTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
-      key_gv[tb * kPfTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
-      key_off[tb * kPfTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
+      if (is_k) {
+        key_a[tb * kPfTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
+        key_gv[tb * kPfTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
+        key_off[tb * kPfTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
+      }
       if (j + 1 < n_tiles) {
         rr += kPfTile;
         while (rr >= L) {
@@ -593,70 +578,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&k_full[bf]);
-      if (__any_sync(0xffffffffu, *vfailed != 0)) break;
-    }
-  } else if (warp < kPfMmaWarp) {
-    // ================= V'^T tiles =================
-    const int dq = warp - kPfSoftmaxWarps;  // 2, 3, 6, 7: warps 10, 11, 14, 15 (sub-partitions 2 and 3)
-    const int dt = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
-    const int vkg = dt & 15, vb = dt >> 4;  // keys 8 vkg .. 8 vkg + 7 of a tile, block vb
-    const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
-    uint32_t f = (uint32_t)(8 * vkg) / L, rr = (uint32_t)(8 * vkg) - f * L;  // frame and offset of key 8 vkg
-    const int64_t code_stride = (int64_t)a.H * (kPfD / 2), scale_stride = (int64_t)a.H * (kPfD / 16);
-    PfCodes8 vpre;
-    // the eight keys from t0 on: consecutive pool rows unless the group crosses a frame
-    auto load_group = [&](uint32_t t0) {
-      const int64_t row0 = t0 < n_keys ? view.row[f] + (int64_t)rr : 0;
-      const uint8_t* cp = a.v_codes + (row0 * a.H + h) * (kPfD / 2) + vb * 8;
-      const uint8_t* sp = a.v_scales + (row0 * a.H + h) * (kPfD / 16) + vb;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        vpre.c[i] = make_uint2(0u, 0u);
-        vpre.s[i] = 0u;
-        if (t0 + i < n_keys) {
-          if (rr + i < L) {
-            vpre.c[i] = *reinterpret_cast<const uint2*>(cp + i * code_stride);
-            vpre.s[i] = sp[i * scale_stride];
-          } else {
-            uint32_t ri;
-            const int64_t base = (view.row[pf_walk(f, rr, (uint32_t)i, L, ri)] + (int64_t)ri) * a.H + h;
-            vpre.c[i] = *reinterpret_cast<const uint2*>(a.v_codes + base * (kPfD / 2) + vb * 8);
-            vpre.s[i] = a.v_scales[base * (kPfD / 16) + vb];
-          }
-        }
-      }
-    };
-    load_group((uint32_t)(8 * vkg));
-    for (int j = 0; j < n_tiles; ++j) {
-      const int bf = j & 1, use = j >> 1;
-      uint8_t* vbuf = Vt + bf * kTileV;
-      // V'(j) into buffer j % 2, once both P' V'(j - 2) MMAs have read it
-      if (j >= 2 && !pf_wait_warp(&v_free[bf], (use - 1) & 1)) break;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {  // channels 16 vb + 8 q .. + 7 of the eight keys
-        uint32_t w[8][4];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) decode_word_bf16(q ? vpre.c[u].y : vpre.c[u].x, scale_bf16x2(vpre.s[u]), w[u]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {  // channel 16 vb + 8 q + i of keys 8 vkg .. 8 vkg + 7: one 16-byte chunk
-          uint32_t o[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) o[p] = __byte_perm(w[2 * p][i >> 1], w[2 * p + 1][i >> 1], (i & 1) ? 0x7632 : 0x5410);
-          *reinterpret_cast<uint4*>(vbuf + core_off(16 * vb + 8 * q + i, vkg, kLboV, kSboV)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      if (j + 1 < n_tiles) {
-        rr += kPfTile;
-        while (rr >= L) {
-          rr -= L;
-          ++f;
-        }
-        load_group((uint32_t)((j + 1) * kPfTile + 8 * vkg));
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&v_full[bf]);
+      if (lane == 0) mbar_arrive(&full[bf]);
       if (__any_sync(0xffffffffu, *vfailed != 0)) break;
     }
   } else if (lane == 0) {
@@ -673,8 +595,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         if (prev) {  // O_hh (+)= P'_hh(j - 1) V'(j - 1)
           if (!mbar_wait(&p_full[hh], pj & 1)) { ok = false; break; }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          pf_mma_tile_ta(tmem + 256 + hh * 128, tmem + hh * 128, smem_u32(Vt + (pj & 1) * kTileV), kLboV, kSboV,
-                         idesc, pj > 0);
+          pf_mma_tile_ta(tmem + 256 + hh * 128, tmem + hh * 128, smem_u32(Vt + (pj & 1) * kTileStd), kLboV, kSboV,
+                         idesc | (1u << 16), pj > 0);  // B = V' MN-major
           pf_commit(&o_done[hh]);
           if (hh == kPfHalves - 1) pf_commit(&v_free[pj & 1]);
         }

@@ -55,27 +55,29 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kPfTile = 128;           // queries per half, keys per tile
+constexpr int kPfQTile = 128;          // queries per half: the TMEM lanes
+constexpr int kPfKTile = 64;           // keys per tile
 constexpr int kPfHalves = 2;           // query halves per CTA sharing each K'/V' tile
-constexpr int kPfRows = 128 * kPfHalves;
+constexpr int kPfRows = kPfQTile * kPfHalves;
 constexpr int kPfD = 128;              // head dimension
 constexpr int kPfSoftmaxWarps = 4 * kPfHalves;
-constexpr int kPfDequantWarps = 8;  // 4 for K', 4 for V'
-constexpr int kPfKWarps = 4;
-constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDequantWarps;
-constexpr int kPfThreads = 32 * (kPfMmaWarp + 1);
+constexpr int kPfDecodeWarps = 8;      // K' on sub-partitions 0 and 1, V' on 2 and 3
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDecodeWarps;
+constexpr int kPfThreads = 32 * (kPfMmaWarp + kPfHalves);  // one MMA-issuing warp per half
 constexpr int kPfMaxSlots = 16;        // distinct pool slots in one view
-constexpr uint32_t kLboStd = 128, kSboStd = 2048;  // [128 rows][256 B]: core matrices 128 B apart along K
+constexpr int kPfBufs = 4;             // K' and V' tile buffers each
+constexpr int kPfKeyBufs = 8;          // key-factor table buffers
+constexpr uint32_t kLboStd = 128, kSboStd = 2048;  // [rows][256 B]: core matrices 128 B apart along d
 // V' [key][d] as an MN-major B operand: LBO = 2048 between groups of 8 keys (the K direction),
 // SBO = 128 between groups of 8 channels (the N direction).
 constexpr uint32_t kLboV = 2048, kSboV = 128;
-constexpr int kTileStd = 32768;
+constexpr int kTileQ = kPfQTile * kPfD * 2;   // one half's Q, bf16
+constexpr int kTileKV = kPfKTile * kPfD * 2;  // one K' or V' tile, bf16
 constexpr float kRescaleStep = 8.0f;  // base-2 units the running maximum may lag behind
-// Q (2 halves), K' (2 buffers), V'^T (2 buffers), q . mean per row and slot, key tables (3 buffers), slot
-// tables, barriers; P' lives in TMEM over its half's S
-constexpr int kPfKeyBufs = 3;
-constexpr int kPfSmem = kPfHalves * kTileStd + 2 * kTileStd + 2 * kTileStd + kPfMaxSlots * kPfRows * 4 +
-                        kPfKeyBufs * 3 * kPfTile * 4 + 2 * kPfMaxSlots * 4 + 256;
+// Q (2 halves), K' and V' (4 buffers each), q . mean per row and slot, key tables, slot tables,
+// barriers; P' lives in TMEM over the S it was computed from
+constexpr int kPfSmem = kPfHalves * kTileQ + 2 * kPfBufs * kTileKV + kPfMaxSlots * kPfRows * 4 +
+                        kPfKeyBufs * 3 * kPfKTile * 4 + 2 * kPfMaxSlots * 4 + 512;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 struct PfView {
@@ -221,7 +223,7 @@ __device__ __forceinline__ void pf_st16(uint32_t taddr, const uint32_t v[16]) {
 __device__ __forceinline__ void pf_mma_tile_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t b_lbo,
                                                uint32_t b_sbo, uint32_t idesc, bool accumulate) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // K = 128 keys in steps of 16 (8 TMEM columns of A, two core matrices of B)
+  for (int k = 0; k < kPfKTile / 16; ++k) {  // K = the tile's keys in steps of 16 (8 TMEM columns of A, two core matrices of B)
     const uint64_t db = pf_desc(b_smem + k * 2 * b_lbo, b_lbo, b_sbo);
     const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
     asm volatile(
@@ -235,7 +237,7 @@ __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, ui
                                             uint32_t b_smem, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc,
                                             bool accumulate) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // K = 128 in steps of 16 (two core matrices along K)
+  for (int k = 0; k < kPfD / 16; ++k) {  // K = d = 128 in steps of 16 (two core matrices along K)
     const uint64_t da = pf_desc(a_smem + k * 2 * a_lbo, a_lbo, a_sbo);
     const uint64_t db = pf_desc(b_smem + k * 2 * b_lbo, b_lbo, b_sbo);
     const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
@@ -259,24 +261,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
                                                                      PfArgs a) {
   extern __shared__ __align__(128) uint8_t pf_smem[];
   uint8_t* Qs = pf_smem;                          // Q of both halves, bf16 [query][d]
-  uint8_t* Kb = Qs + kPfHalves * kTileStd;        // K' tiles [buffer][key][d]
-  uint8_t* Vt = Kb + 2 * kTileStd;                // V' tiles [buffer][key][d]
-  float* qm = reinterpret_cast<float*>(Vt + 2 * kTileStd);  // [view slot][row]: scale log2e q . mean
-  float* key_a = qm + kPfMaxSlots * kPfRows;              // [table buffer][key]: scale log2e g_k
-  float* key_gv = key_a + kPfKeyBufs * kPfTile;           // [table buffer][key]: g_v / G (0 past the view)
-  int* key_off = reinterpret_cast<int*>(key_gv + kPfKeyBufs * kPfTile);  // slot offset in qm, -1 past the view
-  float* slot_a = reinterpret_cast<float*>(key_off + kPfKeyBufs * kPfTile);
+  uint8_t* Kb = Qs + kPfHalves * kTileQ;          // K' tiles [buffer][key][d]
+  uint8_t* Vb = Kb + kPfBufs * kTileKV;           // V' tiles [buffer][key][d]
+  float* qm = reinterpret_cast<float*>(Vb + kPfBufs * kTileKV);  // [view slot][row]: scale log2e q . mean
+  float* key_a = qm + kPfMaxSlots * kPfRows;               // [table buffer][key]: scale log2e g_k
+  float* key_gv = key_a + kPfKeyBufs * kPfKTile;           // [table buffer][key]: g_v / G (0 past the view)
+  int* key_off = reinterpret_cast<int*>(key_gv + kPfKeyBufs * kPfKTile);  // slot offset in qm, -1 past the view
+  float* slot_a = reinterpret_cast<float*>(key_off + kPfKeyBufs * kPfKTile);
   float* slot_gv = slot_a + kPfMaxSlots;
+  // Tile j uses K'/V' buffer j % 4 and, in each half, S buffer j % 2.  A barrier completes one phase
+  // per use of its buffer, and every wait names the phase it needs by its parity.
   uint64_t* bar = reinterpret_cast<uint64_t*>(slot_gv + kPfMaxSlots);
-  uint64_t* k_full = bar;        // [buffer] K'(j) and its key tables written  (4 dequant warps)
-  uint64_t* k_free = bar + 2;    // [buffer] both S(j) MMAs have read K'(j)     (commit)
-  uint64_t* v_full = bar + 4;    // [buffer] V'(j) written                      (4 dequant warps)
-  uint64_t* v_free = bar + 6;    // [buffer] both P' V'(j) MMAs have read V'(j) (commit)
-  uint64_t* s_full = bar + 8;    // [half] S(j) in TMEM                         (commit)
-  uint64_t* p_full = bar + 10;   // [half] P'(j) in TMEM, S(j) read             (4 softmax warps)
-  uint64_t* o_done = bar + 12;   // [half] P' V'(j) accumulated into O          (commit)
-  uint64_t* drain = bar + 14;    // every MMA issued has finished               (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* k_full = bar;        // [buffer] K'(j) and its key tables written   (2 decode warps)
+  uint64_t* k_free = bar + 4;    // [buffer] both S(j) MMAs have read K'(j)      (a commit per half)
+  uint64_t* v_full = bar + 8;    // [buffer] V'(j) written                       (2 decode warps)
+  uint64_t* v_free = bar + 12;   // [buffer] both P' V'(j) MMAs have read V'(j)  (a commit per half)
+  uint64_t* s_full = bar + 16;   // [half][S buffer] S(j) in TMEM                (commit)
+  uint64_t* p_full = bar + 20;   // [half][S buffer] P'(j) in TMEM               (4 softmax warps)
+  uint64_t* o_done = bar + 24;   // [half][S buffer] P' V'(j) added to O         (commit)
+  uint64_t* drain = bar + 28;    // every MMA issued has finished                (a commit per half)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 29);
   float* Gs = reinterpret_cast<float*>(tmem_slot + 1);
   int* failed = reinterpret_cast<int*>(Gs + 1);
   volatile int* vfailed = failed;
@@ -285,21 +289,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   const int h = blockIdx.y;
   const int H = a.H;
   const float slog2e = a.scale * 1.4426950408889634f;
-  const int n_tiles = (int)((a.n_keys + kPfTile - 1) / kPfTile);
+  const int n_tiles = (int)((a.n_keys + kPfKTile - 1) / kPfKTile);
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], kPfKWarps);
-      mbar_init(&k_free[i], 1);
-      mbar_init(&v_full[i], kPfDequantWarps - kPfKWarps);
-      mbar_init(&v_free[i], 1);
+    for (int i = 0; i < kPfBufs; ++i) {
+      mbar_init(&k_full[i], 2);
+      mbar_init(&k_free[i], kPfHalves);
+      mbar_init(&v_full[i], 2);
+      mbar_init(&v_free[i], kPfHalves);
     }
-    for (int i = 0; i < kPfHalves; ++i) {
+    for (int i = 0; i < 2 * kPfHalves; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, kPfHalves);
     *failed = 0;
     float G = 0.0f;
     for (int s = 0; s < view.n_vslots; ++s) G = fmaxf(G, a.v_g[view.slot[s]]);
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   if (warp < kPfSoftmaxWarps) {
     const bool q_ok = rowq < a.n_q;
     const uint4* src = reinterpret_cast<const uint4*>(a.q + (rowq * H + h) * kPfD);
-    uint8_t* qs = Qs + (tid >> 7) * kTileStd;
+    uint8_t* qs = Qs + (tid >> 7) * kTileQ;
     uint32_t qw[64];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -355,26 +359,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     // ================= softmax of one query half =================
     const int half = warp >> 2;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_S = tmem + half * 128 + lane_addr, t_O = tmem + 256 + half * 128 + lane_addr;
+    const uint32_t t_half = tmem + half * 256 + lane_addr, t_O = t_half + 128;  // S buffers at +0, +64; O at +128
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      const int tb = j % kPfKeyBufs;
-      const float* ka = key_a + tb * kPfTile;
-      const float* kgv = key_gv + tb * kPfTile;
-      const int* koff = key_off + tb * kPfTile;
-      // a tile whose 128 keys are all in the view and in one slot (with frames of at least 128
-      // tokens its first and last key decide it): the slot's factors are scalars
-      const int64_t t0 = (int64_t)j * kPfTile;
+      const int sb = j & 1, tb = j % kPfKeyBufs;
+      const uint32_t t_S = t_half + 64 * sb;
+      const float* ka = key_a + tb * kPfKTile;
+      const float* kgv = key_gv + tb * kPfKTile;
+      const int* koff = key_off + tb * kPfKTile;
+      // a tile whose keys are all in the view and in one slot (with frames of at least 64 tokens
+      // its first and last key decide it): the slot's factors are scalars
+      const int64_t t0 = (int64_t)j * kPfKTile;
       int uvs = -1;
-      if (a.L_f >= kPfTile && t0 + kPfTile <= a.n_keys) {
+      if (a.L_f >= kPfKTile && t0 + kPfKTile <= a.n_keys) {
         const uint32_t L = (uint32_t)a.L_f;
-        const int v0 = view.vslot[(uint32_t)t0 / L], v1 = view.vslot[((uint32_t)t0 + kPfTile - 1) / L];
+        const int v0 = view.vslot[(uint32_t)t0 / L], v1 = view.vslot[((uint32_t)t0 + kPfKTile - 1) / L];
         if (v0 == v1) uvs = v0;
       }
       const float ua = uvs >= 0 ? slot_a[uvs] : 0.0f, ub = uvs >= 0 ? qm[uvs * kPfRows + tid] : 0.0f;
       const float ugv = uvs >= 0 ? slot_gv[uvs] : 0.0f;
-      if (!pf_wait_warp(&s_full[half], j & 1)) { ok = false; break; }
+      if (!pf_wait_warp(&s_full[2 * half + sb], (j >> 1) & 1)) { ok = false; break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // pass 1: the tile's maximum of t = (scale log2e) (g_k S + q . mean)
       float mt = -INFINITY;
@@ -383,41 +388,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         // maximum is fmaf(ua, S*, ub) with S* the largest S (the smallest for ua < 0)
         const bool up = ua >= 0.0f;
         float e0 = up ? -INFINITY : INFINITY, e1 = e0, e2 = e0, e3 = e0;
-#pragma unroll 1
-        for (int c = 0; c < 4; c += 2) {
-          uint32_t r0[32], r1[32];
-          pf_ld32_issue(t_S + 32 * c, r0);
-          pf_ld32_issue(t_S + 32 * c + 32, r1);
-          pf_wait_ld();
-          pf_tie32(r0);
-          pf_tie32(r1);
+        uint32_t r0[32], r1[32];
+        pf_ld32_issue(t_S, r0);
+        pf_ld32_issue(t_S + 32, r1);
+        pf_wait_ld();
+        pf_tie32(r0);
+        pf_tie32(r1);
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            if (up) {
-              e0 = fmax3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-              e1 = fmax3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
-              e2 = fmax3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
-              e3 = fmax3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
-              e0 = fmax3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
-              e1 = fmax3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
-              e2 = fmax3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
-              e3 = fmax3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
-            } else {
-              e0 = fmin3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-              e1 = fmin3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
-              e2 = fmin3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
-              e3 = fmin3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
-              e0 = fmin3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
-              e1 = fmin3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
-              e2 = fmin3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
-              e3 = fmin3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
-            }
+        for (int i = 0; i < 32; i += 8) {
+          if (up) {
+            e0 = fmax3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+            e1 = fmax3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+            e2 = fmax3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
+            e3 = fmax3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
+            e0 = fmax3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+            e1 = fmax3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+            e2 = fmax3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
+            e3 = fmax3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
+          } else {
+            e0 = fmin3(e0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+            e1 = fmin3(e1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+            e2 = fmin3(e2, __uint_as_float(r0[i + 4]), __uint_as_float(r0[i + 5]));
+            e3 = fmin3(e3, __uint_as_float(r0[i + 6]), __uint_as_float(r0[i + 7]));
+            e0 = fmin3(e0, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+            e1 = fmin3(e1, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+            e2 = fmin3(e2, __uint_as_float(r1[i + 4]), __uint_as_float(r1[i + 5]));
+            e3 = fmin3(e3, __uint_as_float(r1[i + 6]), __uint_as_float(r1[i + 7]));
           }
         }
         mt = __fmaf_rn(ua, up ? fmax3(e0, e1, fmaxf(e2, e3)) : fmin3(e0, e1, fminf(e2, e3)), ub);
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kPfKTile / 32; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
 #pragma unroll
@@ -428,14 +430,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
       }
       const bool grow = mt > m + kRescaleStep;
-      if (j > 0 && !pf_wait_warp(&o_done[half], (j - 1) & 1)) { ok = false; break; }  // O current
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (__any_sync(0xffffffffu, grow)) {
         const float m_new = grow ? mt : m;
         const float f = grow ? ex2_approx(m - m_new) : 1.0f;  // 0 for the first tile (m = -inf)
         l = __fmul_rn(l, f);
         m = m_new;
-        if (j > 0) {  // O holds earlier tiles: scale this row (warp-wide TMEM access)
+        if (j > 0) {  // O holds tiles up to j - 1: once P' V'(j - 1) is in, scale this row
+          if (!pf_wait_warp(&o_done[2 * half + (sb ^ 1)], ((j - 1) >> 1) & 1)) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
@@ -447,12 +449,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
       }
       // pass 2: P' = bf16(2^(t - m) g_v / G) into TMEM over S (columns already read), and l
-      float2 sa = make_float2(0.0f, 0.0f), sb = sa;
+      float2 sa = make_float2(0.0f, 0.0f), sc = sa;
       if (uvs >= 0) {  // pairs of keys in packed fp32x2 arithmetic; t - m = fmaf(ua, S, ub - m)
         const float2 ua2 = make_float2(ua, ua), c2 = make_float2(__fsub_rn(ub, m), __fsub_rn(ub, m));
         const float2 g2 = make_float2(ugv, ugv);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kPfKTile / 32; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
           uint32_t pw[16];
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
           for (int p = 0; p < 16; ++p) {
             const float2 x = __ffma2_rn(make_float2(t[2 * p], t[2 * p + 1]), ua2, c2);
             const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (p & 1) sb = __fadd2_rn(sb, e); else sa = __fadd2_rn(sa, e);
+            if (p & 1) sc = __fadd2_rn(sc, e); else sa = __fadd2_rn(sa, e);
             const float2 q = __fmul2_rn(e, g2);
             const __nv_bfloat162 b = __float22bfloat162_rn(q);
             pw[p] = *reinterpret_cast<const uint32_t*>(&b);
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kPfKTile / 32; ++c) {
           float t[32];
           pf_ld32(t_S + 32 * c, t);
           uint32_t pw[16];
@@ -479,23 +481,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
             const int o0 = koff[k], o1 = koff[k + 1];
             const float p0 = o0 >= 0 ? ex2_approx(__fmaf_rn(ka[k], t[i], qm[o0 + tid]) - m) : 0.0f;
             const float p1 = o1 >= 0 ? ex2_approx(__fmaf_rn(ka[k + 1], t[i + 1], qm[o1 + tid]) - m) : 0.0f;
-            if (p & 1) sb = __fadd2_rn(sb, make_float2(p0, p1)); else sa = __fadd2_rn(sa, make_float2(p0, p1));
+            if (p & 1) sc = __fadd2_rn(sc, make_float2(p0, p1)); else sa = __fadd2_rn(sa, make_float2(p0, p1));
             const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(__fmul_rn(p0, kgv[k]), __fmul_rn(p1, kgv[k + 1])));
             pw[p] = *reinterpret_cast<const uint32_t*>(&b);
           }
           pf_st16(t_S + 16 * c, pw);
         }
       }
-      const float sum = __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sb.x, sb.y));
+      const float sum = __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sc.x, sc.y));
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l = __fadd_rn(l, sum);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[half]);
+      if (lane == 0) mbar_arrive(&p_full[2 * half + sb]);
       if (__any_sync(0xffffffffu, *vfailed != 0)) { ok = false; break; }
     }
-    // ---- out = G O / l ----
-    if (ok && pf_wait_warp(&o_done[half], (n_tiles - 1) & 1)) {
+    // ---- out = G O / l, once the last P' V' is in (its commit covers every earlier MMA) ----
+    const int jl = n_tiles - 1;
+    if (ok && pf_wait_warp(&o_done[2 * half + (jl & 1)], (jl >> 1) & 1)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const float f = __fdiv_rn(G, l);
 #pragma unroll 1
@@ -515,21 +518,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     }
   } else if (warp < kPfMmaWarp) {
     // ================= K' and V' tiles, one key per thread =================
-    // Warps 8, 9, 12, 13 (sub-partitions 0 and 1) decode K' and write the key factors; warps
-    // 10, 11, 14, 15 (sub-partitions 2 and 3) decode V'.  Thread `key` owns key `key` of every
-    // tile: its 64 code bytes and 8 scale bytes are loaded one tile ahead (nothing reads them
-    // until the tile is decoded) and its 128 bf16 channels stored as 16 chunks of 16 bytes, the
-    // same [key][d] core-matrix layout for both (K-major for S = Q K'^T, MN-major for P' V').
+    // Warps 8, 9 and 12, 13 (sub-partitions 0 and 1) decode K' and write the key factors; warps
+    // 10, 11 and 14, 15 (sub-partitions 2 and 3) decode V'.  Warps 8, 9 / 10, 11 take the even
+    // tiles, 12, 13 / 14, 15 the odd ones.  Thread `key` owns key `key` of its tiles: the key's 64
+    // code bytes and 8 scale bytes are loaded a tile ahead (nothing reads them until the tile is
+    // decoded), and its 128 bf16 channels stored as 16 chunks of 16 bytes in the same [key][d]
+    // core-matrix layout for both (K-major for S = Q K'^T, MN-major for P' V').
     const int dq = warp - kPfSoftmaxWarps;
     const bool is_k = (dq & 2) == 0;
-    const int key = 32 * ((dq & 1) | (dq >> 2 << 1)) + lane;
+    const int grp = dq >> 2, key = 32 * (dq & 1) + lane;
     const uint8_t* codes = is_k ? a.k_codes : a.v_codes;
     const uint8_t* scales = is_k ? a.k_scales : a.v_scales;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* free_ = is_k ? k_free : v_free;
-    uint8_t* tiles = is_k ? Kb : Vt;
+    uint8_t* tiles = is_k ? Kb : Vb;
     const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
-    uint32_t f = (uint32_t)key / L, rr = (uint32_t)key - f * L;  // frame and offset of the key in tile 0
+    const uint32_t t_first = (uint32_t)(grp * kPfKTile + key);
+    uint32_t f = t_first / L, rr = t_first - f * L;  // frame and offset of the key in the group's first tile
     uint4 kc[4];
     uint2 ks;
     int kvs;  // view slot of the loaded key, -1 past the view
@@ -547,68 +552,72 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         kvs = view.vslot[f];
       }
     };
-    load_key((uint32_t)key);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int bf = j & 1, use = j >> 1, tb = j % kPfKeyBufs;
-      uint8_t* buf = tiles + bf * kTileStd;
-      // tile j into buffer j % 2, once both MMAs of tile j - 2 have read it
-      if (j >= 2 && !pf_wait_warp(&free_[bf], (use - 1) & 1)) break;
+    load_key(t_first);
+    for (int j = grp; j < n_tiles; j += 2) {
+      const int b = j % kPfBufs, use = j / kPfBufs, tb = j % kPfKeyBufs;
+      uint8_t* buf = tiles + b * kTileKV;
+      // tile j into buffer j % 4, once the MMAs of tile j - 4 have read it
+      if (j >= kPfBufs && !pf_wait_warp(&free_[b], (use - 1) & 1)) break;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {  // block b: code bytes 8 b .. 8 b + 7, scale byte b
-        const uint4 c4 = kc[b >> 1];
-        const uint32_t E2 = scale_bf16x2(((b < 4 ? ks.x : ks.y) >> (8 * (b & 3))) & 0xFFu);
+      for (int k = 0; k < 8; ++k) {  // block k: code bytes 8 k .. 8 k + 7, scale byte k
+        const uint4 c4 = kc[k >> 1];
+        const uint32_t E2 = scale_bf16x2(((k < 4 ? ks.x : ks.y) >> (8 * (k & 3))) & 0xFFu);
         uint32_t w[8];
-        decode_word_bf16((b & 1) ? c4.z : c4.x, E2, w);
-        decode_word_bf16((b & 1) ? c4.w : c4.y, E2, w + 4);
-        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * b, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * b + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
+        decode_word_bf16((k & 1) ? c4.z : c4.x, E2, w);
+        decode_word_bf16((k & 1) ? c4.w : c4.y, E2, w + 4);
+        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * k, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(buf + core_off(key, 2 * k + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
       if (is_k) {
-        key_a[tb * kPfTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
-        key_gv[tb * kPfTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
-        key_off[tb * kPfTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
+        key_a[tb * kPfKTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
+        key_gv[tb * kPfKTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
+        key_off[tb * kPfKTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
       }
-      if (j + 1 < n_tiles) {
-        rr += kPfTile;
+      if (j + 2 < n_tiles) {  // the same key of tile j + 2
+        rr += 2 * kPfKTile;
         while (rr >= L) {
           rr -= L;
           ++f;
         }
-        load_key((uint32_t)((j + 1) * kPfTile + key));
+        load_key((uint32_t)((j + 2) * kPfKTile + key));
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[bf]);
+      if (lane == 0) mbar_arrive(&full[b]);
       if (__any_sync(0xffffffffu, *vfailed != 0)) break;
     }
   } else if (lane == 0) {
-    // ================= MMA issue, ping-ponging the halves =================
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfTile >> 3) << 17) |
-                           ((uint32_t)(kPfTile >> 4) << 24);  // bf16 x bf16 -> fp32, K-major, M = N = 128
+    // ================= MMA issue, one thread per half =================
+    // S is one tile ahead: S_hh(j + 2) goes into S buffer j % 2 as soon as P'_hh(j) V'(j) has
+    // read P'_hh(j) from it, so the softmax finds S_hh(j + 1) ready.
+    const int hh = warp - kPfMmaWarp;
+    const uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfKTile >> 3) << 17) |
+                             ((uint32_t)(kPfQTile >> 4) << 24);  // bf16 x bf16 -> fp32, K-major, N = 64 keys
+    const uint32_t idesc_o = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kPfD >> 3) << 17) |
+                             ((uint32_t)(kPfQTile >> 4) << 24);  // B = V' MN-major, N = d = 128
+    const uint32_t t_half = tmem + hh * 256, q_smem = smem_u32(Qs + hh * kTileQ);
     bool ok = true;
-    for (int j = 0; j <= n_tiles && ok; ++j) {
-      const bool prev = j > 0, cur = j < n_tiles;
-      const int pj = j - 1;
-      if (cur && !mbar_wait(&k_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
-      if (prev && !mbar_wait(&v_full[pj & 1], (pj >> 1) & 1)) { ok = false; break; }
-      for (int hh = 0; hh < kPfHalves && ok; ++hh) {
-        if (prev) {  // O_hh (+)= P'_hh(j - 1) V'(j - 1)
-          if (!mbar_wait(&p_full[hh], pj & 1)) { ok = false; break; }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          pf_mma_tile_ta(tmem + 256 + hh * 128, tmem + hh * 128, smem_u32(Vt + (pj & 1) * kTileStd), kLboV, kSboV,
-                         idesc | (1u << 16), pj > 0);  // B = V' MN-major
-          pf_commit(&o_done[hh]);
-          if (hh == kPfHalves - 1) pf_commit(&v_free[pj & 1]);
-        }
-        if (cur) {  // S_hh(j) = Q_hh K'(j)^T, over P'_hh(j - 1) once its MMAs have read it
-          if (prev && !mbar_wait(&o_done[hh], pj & 1)) { ok = false; break; }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          pf_mma_tile(tmem + hh * 128, smem_u32(Qs + hh * kTileStd), kLboStd, kSboStd, smem_u32(Kb + (j & 1) * kTileStd),
-                      kLboStd, kSboStd, idesc, false);
-          pf_commit(&s_full[hh]);
-          if (hh == kPfHalves - 1) pf_commit(&k_free[j & 1]);
-        }
-      }
+    auto issue_s = [&](int j) {  // S_hh(j) = Q_hh K'(j)^T into S buffer j % 2
+      const int b = j % kPfBufs;
+      if (!mbar_wait(&k_full[b], (j / kPfBufs) & 1)) return false;
+      if (j >= 2 && !mbar_wait(&o_done[2 * hh + (j & 1)], ((j - 2) >> 1) & 1)) return false;  // P'_hh(j - 2) read
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      pf_mma_tile(t_half + 64 * (j & 1), q_smem, kLboStd, kSboStd, smem_u32(Kb + b * kTileKV), kLboStd, kSboStd,
+                  idesc_s, false);
+      pf_commit(&s_full[2 * hh + (j & 1)]);
+      pf_commit(&k_free[b]);
+      return true;
+    };
+    for (int j = 0; j < 2 && j < n_tiles && ok; ++j) ok = issue_s(j);
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int b = j % kPfBufs;
+      if (!mbar_wait(&v_full[b], (j / kPfBufs) & 1)) { ok = false; break; }
+      if (!mbar_wait(&p_full[2 * hh + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      pf_mma_tile_ta(t_half + 128, t_half + 64 * (j & 1), smem_u32(Vb + b * kTileKV), kLboV, kSboV, idesc_o, j > 0);
+      pf_commit(&o_done[2 * hh + (j & 1)]);  // O_hh (+)= P'_hh(j) V'(j)
+      pf_commit(&v_free[b]);
+      if (j + 2 < n_tiles) ok = issue_s(j + 2);
       if (*vfailed) ok = false;
     }
     if (!ok) atomicExch(failed, 1);
@@ -638,7 +647,7 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
                                         const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
                                         float scale, float* out, int* dev_status, void* stream) {
   if (D != nvfp4::kPfD || H < 1 || H > 65535) return NVFP4_ESHAPE;
-  if (n_q < 1 || n_q > ((int64_t)1 << 30) * nvfp4::kPfTile) return NVFP4_ESHAPE;
+  if (n_q < 1 || n_q > ((int64_t)1 << 30) * nvfp4::kPfRows) return NVFP4_ESHAPE;
   if (n_frames < 1 || n_frames > NVFP4_MAX_VIEW_FRAMES || tokens_per_frame < 1 || pool_rows < 1 || n_meta < 1)
     return NVFP4_ESHAPE;
   if (tokens_per_frame > ((int64_t)1 << 40) / NVFP4_MAX_VIEW_FRAMES) return NVFP4_ESHAPE;
@@ -647,7 +656,8 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
     return NVFP4_ESHAPE;
   if (!q_bf16 || !k_codes || !k_scales || !k_g || !v_codes || !v_scales || !v_g || !frame_row || !frame_meta || !out)
     return NVFP4_EINVAL;
-  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(k_codes, 16) || !nvfp4::pf_aligned(k_scales, 8) || !nvfp4::pf_aligned(v_codes, 8) ||
+  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(k_codes, 16) || !nvfp4::pf_aligned(k_scales, 8) ||
+      !nvfp4::pf_aligned(v_codes, 16) || !nvfp4::pf_aligned(v_scales, 8) ||
       !nvfp4::pf_aligned(k_g, 4) || !nvfp4::pf_aligned(v_g, 4) || !nvfp4::pf_aligned(out, 16) ||
       !nvfp4::pf_aligned(k_mean, 4) || !nvfp4::pf_aligned(dev_status, 4))
     return NVFP4_EALIGN;

@@ -77,7 +77,7 @@ constexpr float kRescaleStep = 8.0f;  // base-2 units the running maximum may la
 // Q (2 halves), K' and V' (4 buffers each), q . mean per row and slot, key tables, slot tables,
 // barriers; P' lives in TMEM over the S it was computed from
 constexpr int kPfSmem = kPfHalves * kTileQ + 2 * kPfBufs * kTileKV + kPfMaxSlots * kPfRows * 4 +
-                        kPfKeyBufs * 3 * kPfKTile * 4 + 2 * kPfMaxSlots * 4 + 512;
+                        kPfKeyBufs * 3 * kPfKTile * 4 + 2 * kPfMaxSlots * 4 + 512;  // barriers etc. in the last 512 B
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 struct PfView {
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   uint64_t* p_full = bar + 20;   // [half][S buffer] P'(j) in TMEM               (4 softmax warps)
   uint64_t* o_done = bar + 24;   // [half][S buffer] P' V'(j) added to O         (commit)
   uint64_t* drain = bar + 28;    // every MMA issued has finished                (a commit per half)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 29);
+  uint64_t* key_ready = bar + 29;  // [table buffer] key factors of tile j written (2 decode warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 29 + kPfKeyBufs);
   float* Gs = reinterpret_cast<float*>(tmem_slot + 1);
   int* failed = reinterpret_cast<int*>(Gs + 1);
   volatile int* vfailed = failed;
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, kPfHalves);
+    for (int i = 0; i < kPfKeyBufs; ++i) mbar_init(&key_ready[i], 2);
     *failed = 0;
     float G = 0.0f;
     for (int s = 0; s < view.n_vslots; ++s) G = fmaxf(G, a.v_g[view.slot[s]]);
@@ -370,13 +372,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       const int* koff = key_off + tb * kPfKTile;
       // a tile whose keys are all in the view and in one slot (with frames of at least 64 tokens
       // its first and last key decide it): the slot's factors are scalars
-      const int64_t t0 = (int64_t)j * kPfKTile;
-      int uvs = -1;
-      if (a.L_f >= kPfKTile && t0 + kPfKTile <= a.n_keys) {
-        const uint32_t L = (uint32_t)a.L_f;
-        const int v0 = view.vslot[(uint32_t)t0 / L], v1 = view.vslot[((uint32_t)t0 + kPfKTile - 1) / L];
-        if (v0 == v1) uvs = v0;
-      }
+      if (!pf_wait_warp(&key_ready[tb], (j / kPfKeyBufs) & 1)) { ok = false; break; }
+      const int o_first = koff[0], o_last = koff[kPfKTile - 1];
+      const int uvs = (a.L_f >= kPfKTile && o_first == o_last && o_first >= 0) ? o_first / kPfRows : -1;
       const float ua = uvs >= 0 ? slot_a[uvs] : 0.0f, ub = uvs >= 0 ? qm[uvs * kPfRows + tid] : 0.0f;
       const float ugv = uvs >= 0 ? slot_gv[uvs] : 0.0f;
       if (!pf_wait_warp(&s_full[2 * half + sb], (j >> 1) & 1)) { ok = false; break; }
@@ -568,10 +566,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
         *reinterpret_cast<uint4*>(buf + core_off(key, 2 * k, kLboStd, kSboStd)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(buf + core_off(key, 2 * k + 1, kLboStd, kSboStd)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (is_k) {
+      if (is_k) {  // the key's factors, for the softmax
         key_a[tb * kPfKTile + key] = kvs >= 0 ? slot_a[kvs] : 0.0f;
         key_gv[tb * kPfKTile + key] = kvs >= 0 ? slot_gv[kvs] : 0.0f;
         key_off[tb * kPfKTile + key] = kvs >= 0 ? kvs * kPfRows : -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&key_ready[tb]);
       }
       if (j + 2 < n_tiles) {  // the same key of tile j + 2
         rr += 2 * kPfKTile;

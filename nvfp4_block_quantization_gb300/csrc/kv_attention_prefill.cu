@@ -219,33 +219,42 @@ __device__ __forceinline__ void pf_st16(uint32_t taddr, const uint32_t v[16]) {
       : "memory");
 }
 
-// O (+)= P' V'^T with P' (A, bf16 pairs: lane = query row, column c = keys 2c and 2c + 1) in TMEM.
+// One tcgen05.mma of kind f16; `acc` 0 overwrites D.  An operand given as a 64-bit value is a
+// shared-memory descriptor; as a 32-bit value, a TMEM address.
+__device__ __forceinline__ void pf_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void pf_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+
+// The descriptors of one K step follow from the first by adding the step's byte offset / 16 to
+// the address field (bits 0-13): shared-memory addresses stay below 2^18, so it cannot carry.
+
+// O (+)= P' V' with P' (A, bf16 pairs: lane = query row, column c = keys 2c and 2c + 1) in TMEM.
 __device__ __forceinline__ void pf_mma_tile_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t b_lbo,
                                                uint32_t b_sbo, uint32_t idesc, bool accumulate) {
+  const uint64_t db = pf_desc(b_smem, b_lbo, b_sbo);
 #pragma unroll
-  for (int k = 0; k < kPfKTile / 16; ++k) {  // K = the tile's keys in steps of 16 (8 TMEM columns of A, two core matrices of B)
-    const uint64_t db = pf_desc(b_smem + k * 2 * b_lbo, b_lbo, b_sbo);
-    const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem + 8 * k), "l"(db), "r"(idesc), "r"(acc) : "memory");
-  }
+  for (int k = 0; k < kPfKTile / 16; ++k)  // K = the tile's keys in steps of 16 (8 TMEM columns of A, two core matrices of B)
+    pf_mma_ta(d_tmem, a_tmem + 8 * k, db + (uint64_t)((k * 2 * b_lbo) >> 4), idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void pf_mma_tile(uint32_t d_tmem, uint32_t a_smem, uint32_t a_lbo, uint32_t a_sbo,
                                             uint32_t b_smem, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc,
                                             bool accumulate) {
+  const uint64_t da = pf_desc(a_smem, a_lbo, a_sbo), db = pf_desc(b_smem, b_lbo, b_sbo);
 #pragma unroll
-  for (int k = 0; k < kPfD / 16; ++k) {  // K = d = 128 in steps of 16 (two core matrices along K)
-    const uint64_t da = pf_desc(a_smem + k * 2 * a_lbo, a_lbo, a_sbo);
-    const uint64_t db = pf_desc(b_smem + k * 2 * b_lbo, b_lbo, b_sbo);
-    const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(da), "l"(db), "r"(idesc), "r"(acc) : "memory");
-  }
+  for (int k = 0; k < kPfD / 16; ++k)  // K = d = 128 in steps of 16 (two core matrices along K)
+    pf_mma(d_tmem, da + (uint64_t)((k * 2 * a_lbo) >> 4), db + (uint64_t)((k * 2 * b_lbo) >> 4), idesc,
+           (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity) {

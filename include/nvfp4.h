@@ -374,20 +374,23 @@ nvfp4_status nvfp4_kv_attention_decode(const float* q, int n_q, const uint8_t* k
  *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t.
  * Computed as: K' = Q E_k and V' = Q E_v, exact in bf16, in shared memory;
  * s = scale * (g_k (q . K') + q . mean) with q . K' summed in fp32 by
- * tcgen05.mma and q . mean in fp32; a first pass finds each row's max m and
- * l = sum exp(s - m); a second accumulates P' V' in fp32 on the tensor cores
- * with P' = bf16(exp(s - m) g_v / G), G the largest g_v of the view, and
- * writes out = G O / l in fp32.  P' is the only value rounded below fp32
- * (relative 2^-9).
+ * tcgen05.mma and q . mean in fp32; one pass over the view in tiles of 64
+ * keys with a running maximum m that moves when a tile exceeds it by more
+ * than 8 (base 2; O and l are then rescaled); P' = bf16(2^(s log2 e - m)
+ * g_v / G), G the largest g_v of the view, accumulated as O += P' V' in fp32
+ * on the tensor cores, l = sum 2^(s log2 e - m) in fp32; out = G O / l in
+ * fp32.  P' is the only value rounded below fp32 (relative 2^-9); 2^x is the
+ * hardware approximation (relative error below 2^-22).
  *   q_bf16     device [n_q][H][D] bf16, 16-byte aligned; D = 128
- *   k_*, v_*   the pools of nvfp4_kv_gather_dequant (codes 8-byte aligned)
+ *   k_*, v_*   the pools of nvfp4_kv_gather_dequant: codes 16-byte aligned,
+ *              scales 8-byte aligned, k_mean 4-byte aligned (NVFP4_EALIGN)
  *   frame_row, frame_meta  HOST arrays of n_frames (<= NVFP4_MAX_VIEW_FRAMES)
  *              entries, validated before anything is enqueued; at most 16
  *              distinct slots in one view (NVFP4_ESHAPE otherwise)
  *   out        device [n_q][H][D] fp32, 16-byte aligned
  *   dev_status device int or NULL: NVFP4_DEV_TIMEOUT is OR-ed in when a
  *              bounded wait for the tensor cores gave up (out then incomplete)
- * One CTA per 128 queries and head; no workspace. */
+ * One CTA per 256 queries and head; no workspace. */
 nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const uint8_t* k_codes,
                                         const uint8_t* k_scales, const float* k_g, const float* k_mean,
                                         const uint8_t* v_codes, const uint8_t* v_scales, const float* v_g,

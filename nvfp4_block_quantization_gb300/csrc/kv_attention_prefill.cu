@@ -25,27 +25,26 @@
 // P' is rounded (bf16, relative 2^-9); 2^x is the hardware approximation
 // (relative error below 2^-22).
 //
-// One CTA per (256 queries, head), 13 warps in roles, every hand-off an mbarrier:
-//   warps 0-3, 4-7  softmax of query half 0 / 1: thread r owns query row r of its
-//                   half (TMEM lane r); two passes over the half's S (maximum,
-//                   then P'), 32 columns at a time; P' (bf16 pairs) is written
-//                   into TMEM over the half's S columns already read; O rescaled
-//                   when needed;
-//   warps 8-11      dequantization into double buffers: tile j's K' (with the
-//                   per-key factors, in one of three table buffers) as soon as
-//                   both S MMAs of tile j - 2 have read its buffer, and its V'^T
-//                   as soon as both P' V' MMAs of tile j - 2 have; the next
-//                   tile's codes are loaded into registers meanwhile;
-//   warp 12         one thread issues the MMAs, ping-ponging the halves:
-//                   P'_0 V'(j-1), S_0(j), P'_1 V'(j-1), S_1(j), P' read from TMEM
-//                   (the A operand) and S_h(j) issued once P'_h V'(j-1) has read
-//                   the columns it overwrites.
-// TMEM: S of half 0 and 1 in columns 0-255 (P' over their first 64), O in
-// 256-511.  Operand tiles in shared memory use the no-swizzle K-major layout of
-// 8-row x 16-byte core matrices; the transposed V' tile pads its K stride to
-// 144 bytes so that its stores spread over the banks.  Every wait is bounded; a
-// timeout is reported in the status word and the CTA drains its MMAs before
-// freeing TMEM.
+// One CTA per (256 queries, head), 18 warps in roles, every hand-off an mbarrier; keys in
+// tiles of 64:
+//   warps 0-3, 4-7    softmax of query half 0 / 1: thread r owns query row r of its half (TMEM
+//                     lane r); per tile, the maximum of its 64 scores, then P' (bf16 pairs)
+//                     written into TMEM over the S columns already read; O rescaled when needed.
+//                     A tile whose keys share one view slot (most of them) takes the slot's
+//                     factors as scalars and the extreme raw S with 3-input max, and forms P'
+//                     in packed fp32x2 arithmetic;
+//   warps 8, 9, 12, 13  K' decoders (sub-partitions 0 and 1), warps 10, 11, 14, 15 V'
+//                     decoders (2 and 3): thread k owns key k of every other tile, loads its
+//                     72 code and scale bytes a tile ahead, and writes its 128 bf16 channels,
+//                     E2M1 magnitudes taken from byte-permute tables and multiplied by the block
+//                     scale in bf16x2 (exact); the K' decoders also write each key's factors;
+//   warps 16, 17      one thread per half issues that half's MMAs: S_h(j + 2) = Q_h K'(j + 2)^T
+//                     into the S buffer that P'_h(j) V'(j) has just read, so S stays one tile
+//                     ahead of the softmax.
+// TMEM per half: two 64-column S buffers (P' over the first 32 columns of each) and a
+// 128-column O.  K' and V' share one [key][d] layout of 8-row x 16-byte core matrices, four
+// buffers each: K-major for S = Q K'^T, MN-major for P' V'.  Every wait is bounded; a timeout is
+// reported in the status word and the CTA drains its MMAs before freeing TMEM.
 #include <cstring>
 
 #include "nvfp4.h"

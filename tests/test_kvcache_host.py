@@ -242,11 +242,12 @@ def test_prefill_attention_argument_errors(lib):
     fr = np.array([0, 16], np.int64)
     fm = np.array([0, 1], np.int32)
 
-    def call(n_q=200, D=128, fr_=fr, fm_=fm, n=None, pool_rows=64, n_meta=2, q=dev, codes=dev, out=dev):
+    def call(n_q=200, D=128, fr_=fr, fm_=fm, n=None, pool_rows=64, n_meta=2, q=dev, codes=dev, out=dev,
+             k_scales=dev, v_codes=dev, v_scales=dev):
         n = len(fr_) if n is None else n
-        return lib.load().nvfp4_kv_attention_prefill(q, n_q, codes, dev, dev, dev, dev, dev, dev, pool_rows, n_meta,
-                                                     fr_.ctypes.data, fm_.ctypes.data, n, 16, 2, D, 0.125, out,
-                                                     None, None)
+        return lib.load().nvfp4_kv_attention_prefill(q, n_q, codes, k_scales, dev, dev, v_codes, v_scales, dev,
+                                                     pool_rows, n_meta, fr_.ctypes.data, fm_.ctypes.data, n, 16, 2,
+                                                     D, 0.125, out, None, None)
 
     assert call(D=64) == lib.NVFP4_ESHAPE                               # head dimension 128 only
     assert call(n_q=0) == lib.NVFP4_ESHAPE
@@ -258,3 +259,6 @@ def test_prefill_attention_argument_errors(lib):
                 n_meta=17) == lib.NVFP4_ESHAPE                          # 17 distinct slots in one view
     assert call(codes=None) == lib.NVFP4_EINVAL and call(out=None) == lib.NVFP4_EINVAL
     assert call(q=dev + 8) == lib.NVFP4_EALIGN and call(out=dev + 4) == lib.NVFP4_EALIGN
+    # a key's 64 code bytes are read as four 16-byte words and its 8 scale bytes as one word
+    assert call(codes=dev + 8) == lib.NVFP4_EALIGN and call(v_codes=dev + 8) == lib.NVFP4_EALIGN
+    assert call(k_scales=dev + 4) == lib.NVFP4_EALIGN and call(v_scales=dev + 4) == lib.NVFP4_EALIGN

@@ -699,9 +699,8 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
   a.L_f = tokens_per_frame;
   a.H = H;
   a.scale = scale;
-  if (cudaFuncSetAttribute(nvfp4::attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nvfp4::kPfSmem) !=
-      cudaSuccess)
-    return NVFP4_ECUDA;
+  static std::atomic<unsigned long long> smem_set{0};
+  if (nvfp4::smem_limit_once(nvfp4::attn_prefill_kernel, nvfp4::kPfSmem, smem_set) != cudaSuccess) return NVFP4_ECUDA;
   const int64_t q_per_cta = nvfp4::kPfRows;
   const dim3 grid((unsigned)((n_q + q_per_cta - 1) / q_per_cta), (unsigned)H);
   nvfp4::attn_prefill_kernel<<<grid, nvfp4::kPfThreads, nvfp4::kPfSmem, static_cast<cudaStream_t>(stream)>>>(view, a);

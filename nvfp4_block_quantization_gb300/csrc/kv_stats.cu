@@ -404,8 +404,9 @@ __global__ void __maxnreg__(80) kv_stats_kernel(const __grid_constant__ KvBatch 
 
 cudaError_t launch_kv_stats(const KvBatch& b, const KvGeom& g, bool bf16, cudaStream_t s) {
   const size_t smem = (size_t)kStatsStages * kStatsStageBytes + sizeof(StatsSmem);
-  cudaError_t e = bf16 ? cudaFuncSetAttribute(kv_stats_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                       : cudaFuncSetAttribute(kv_stats_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> set_bf16{0}, set_f32{0};  // the limit is raised once per device
+  cudaError_t e = bf16 ? smem_limit_once(kv_stats_kernel<true>, (int)smem, set_bf16)
+                       : smem_limit_once(kv_stats_kernel<false>, (int)smem, set_f32);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.P);

@@ -787,16 +787,24 @@ def row_kv_attention_prefill(nv, W, torch, dev, peak):
     q = (torch.randn((T_CHUNK, HEADS, HEAD_DIM), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
     o = torch.empty((T_CHUNK, HEADS, HEAD_DIM), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the last, partial wave of (query tile, head) units runs split along the keys, in this workspace
+    ws_bytes = nv._lib.nvfp4_kv_attention_prefill_workspace_bytes(T_CHUNK, HEADS, len(fr), Lf)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def call(i):
-        nv.kv_attention_prefill(q, pk, pv, fr, fs, Lf, HEAD_DIM ** -0.5, out=o, status=status)
+        nv.kv_attention_prefill(q, pk, pv, fr, fs, Lf, HEAD_DIM ** -0.5, out=o, status=status, workspace=ws)
+
+    def call_whole(i):
+        nv.kv_attention_prefill(q, pk, pv, fr, fs, Lf, HEAD_DIM ** -0.5, out=o, status=status, split=False)
 
     ms = _time_graph(torch, call, 2, 5)
+    ms_whole = _time_graph(torch, call_whole, 2, 5)
     fl = 4.0 * T_CHUNK * n_keys * HEAD_DIM * HEADS
     pk_tf, src = bf16_peak_tflops()
     torch.cuda.synchronize()
     return {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops": fl, "n_q": T_CHUNK, "n_keys": n_keys,
             "peak_tflops": pk_tf, "peak_source": src, "frac": fl / ms / 1e9 / pk_tf,
+            "split_units": ws_bytes // (2 * (256 * 128 + 512) * 4), "ms_without_key_split": ms_whole,
             "dev_status": int(status.item())}
 
 

@@ -388,15 +388,28 @@ nvfp4_status nvfp4_kv_attention_decode(const float* q, int n_q, const uint8_t* k
  *              entries, validated before anything is enqueued; at most 16
  *              distinct slots in one view (NVFP4_ESHAPE otherwise)
  *   out        device [n_q][H][D] fp32, 16-byte aligned
+ *   workspace  device scratch, 16-byte aligned, or NULL: with at least
+ *              nvfp4_kv_attention_prefill_workspace_bytes(...) bytes (else
+ *              NVFP4_EINVAL) the (query tile, head) units of the last, partial
+ *              wave of CTAs run as two CTAs over the two halves of the view's
+ *              keys each, merged by a second kernel on the same stream:
+ *              out = (o_0 w_0 + o_1 w_1) / (w_0 + w_1), o_i = G O_i / l_i of
+ *              half i, w_i = l_i 2^(m_i - max(m_0, m_1)).  NULL: every unit runs
+ *              whole.  Owned by the caller, free again once the call's work on
+ *              `stream` is done.
  *   dev_status device int or NULL: NVFP4_DEV_TIMEOUT is OR-ed in when a
  *              bounded wait for the tensor cores gave up (out then incomplete)
- * One CTA per 256 queries and head; no workspace. */
+ * One CTA per 256 queries and head (a split unit: two). */
+/* Workspace bytes for nvfp4_kv_attention_prefill on the current device: 0
+ * when no unit would be split (or the shape is invalid). */
+size_t nvfp4_kv_attention_prefill_workspace_bytes(int64_t n_q, int H, int n_frames, int64_t tokens_per_frame);
 nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const uint8_t* k_codes,
                                         const uint8_t* k_scales, const float* k_g, const float* k_mean,
                                         const uint8_t* v_codes, const uint8_t* v_scales, const float* v_g,
                                         int64_t pool_rows, int n_meta, const int64_t* frame_row,
                                         const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
-                                        float scale, float* out, int* dev_status, void* stream);
+                                        float scale, float* out, void* workspace, size_t workspace_bytes,
+                                        int* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Weights with 16x16 2-D blocks (LongLive-2.0 summary page, training        */

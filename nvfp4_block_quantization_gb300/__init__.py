@@ -375,11 +375,13 @@ def kv_gather_dequant(pool: KvCachePool, frame_row, frame_slot, tokens_per_frame
 
 
 def kv_attention_prefill(q, k_pool: KvCachePool, v_pool: KvCachePool, frame_row, frame_slot, tokens_per_frame: int,
-                         scale: float, out=None, status=None, stream=None):
+                         scale: float, out=None, status=None, stream=None, workspace=None, split: bool = True):
     """Attention of a block of queries q [n_q, H, 128] (bf16) over a cache view read straight from the
     NVFP4 pools, on the tensor cores (``nvfp4_kv_attention_prefill``); K's means are re-added when its
     pool has them.  Returns fp32 [n_q, H, 128]; ``status`` (int32 [1], optional) collects
-    NVFP4_DEV_TIMEOUT."""
+    NVFP4_DEV_TIMEOUT.  With ``split`` the last, partial wave of CTAs is split along the keys, in
+    ``workspace`` (uint8 on the device, allocated here when None); ``split=False`` runs every unit
+    whole."""
     import numpy as np
 
     torch = _torch()
@@ -391,11 +393,19 @@ def kv_attention_prefill(q, k_pool: KvCachePool, v_pool: KvCachePool, frame_row,
     fs = np.ascontiguousarray(frame_slot, dtype=np.int32)
     if out is None:
         out = torch.empty((n_q, H, D), dtype=torch.float32, device=q.device)
+    ws_bytes = 0
+    if split:
+        need = _lib.nvfp4_kv_attention_prefill_workspace_bytes(n_q, H, int(fr.shape[0]), tokens_per_frame)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    else:
+        workspace = None
     st = _lib.nvfp4_kv_attention_prefill(_ptr(q), n_q, _ptr(k_pool.codes), _ptr(k_pool.scales), _ptr(k_pool.g),
                                          _ptr(k_pool.mean), _ptr(v_pool.codes), _ptr(v_pool.scales), _ptr(v_pool.g),
                                          k_pool.codes.shape[0], int(k_pool.g.numel()), fr.ctypes.data,
                                          fs.ctypes.data, int(fr.shape[0]), tokens_per_frame, H, D, float(scale),
-                                         _ptr(out), _ptr(status), _stream(stream))
+                                         _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _lib.check(st, "nvfp4_kv_attention_prefill")
     return out
 

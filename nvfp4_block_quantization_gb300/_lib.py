@@ -41,6 +41,7 @@ EXPORTS = (
     "nvfp4_kv_gather_dequant",
     "nvfp4_kv_attention_workspace_bytes",
     "nvfp4_kv_attention_decode",
+    "nvfp4_kv_attention_prefill_workspace_bytes",
     "nvfp4_kv_attention_prefill",
     "nvfp4_mma_scales_bytes",
     "nvfp4_scales_to_mma",
@@ -166,8 +167,10 @@ def load(path: str | None = None):
     lib.nvfp4_kv_attention_decode.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32,
                                               i32, ctypes.c_float, vp, vp, sz, vp]
     lib.nvfp4_kv_attention_decode.restype = i32
+    lib.nvfp4_kv_attention_prefill_workspace_bytes.argtypes = [i64, i32, i32, i64]
+    lib.nvfp4_kv_attention_prefill_workspace_bytes.restype = sz
     lib.nvfp4_kv_attention_prefill.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, i64, i32,
-                                               i32, ctypes.c_float, vp, vp, vp]
+                                               i32, ctypes.c_float, vp, vp, sz, vp, vp]
     lib.nvfp4_kv_attention_prefill.restype = i32
     lib.nvfp4_mma_scales_bytes.argtypes = [i64, i64]
     lib.nvfp4_mma_scales_bytes.restype = i64
@@ -310,12 +313,16 @@ def nvfp4_kv_attention_decode(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v
                                             H, D, scale, out, workspace, workspace_bytes, stream)
 
 
+def nvfp4_kv_attention_prefill_workspace_bytes(n_q, H, n_frames, tokens_per_frame):
+    return load().nvfp4_kv_attention_prefill_workspace_bytes(n_q, H, n_frames, tokens_per_frame)
+
+
 def nvfp4_kv_attention_prefill(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g, pool_rows, n_meta,
-                               frame_row, frame_meta, n_frames, tokens_per_frame, H, D, scale, out, dev_status,
-                               stream):
+                               frame_row, frame_meta, n_frames, tokens_per_frame, H, D, scale, out, workspace,
+                               workspace_bytes, dev_status, stream):
     return load().nvfp4_kv_attention_prefill(q, n_q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g,
                                              pool_rows, n_meta, frame_row, frame_meta, n_frames, tokens_per_frame,
-                                             H, D, scale, out, dev_status, stream)
+                                             H, D, scale, out, workspace, workspace_bytes, dev_status, stream)
 
 
 def nvfp4_mma_scales_bytes(rows, K):

@@ -100,7 +100,15 @@ struct PfArgs {
   int64_t n_q, n_keys, L_f;
   int H;
   float scale;
+  // Key split of the last wave: units (head h, query tile qt) are numbered h * q_tiles + qt.
+  // Units below n_full run whole; each later unit runs as two CTAs over keys [0, t_mid) and
+  // [t_mid, n_keys), which write G O / l, m and l of their rows to `part` for the merge kernel.
+  float* part;
+  int64_t q_tiles, n_full, t_mid;
 };
+
+// One split half's rows in the workspace: out [256][128] fp32, then m [256] and l [256].
+constexpr int64_t kPfPartFloats = (int64_t)kPfRows * kPfD + 2 * kPfRows;
 
 __device__ __forceinline__ uint32_t core_off(uint32_t r, uint32_t chunk, uint32_t lbo, uint32_t sbo) {
   return (r >> 3) * sbo + chunk * lbo + (r & 7) * 16;
@@ -295,10 +303,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   volatile int* vfailed = failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y;
+  const int64_t bid = blockIdx.x;
+  const int64_t unit = bid < a.n_full ? bid : a.n_full + (bid - a.n_full) / 2;
+  const int part = bid < a.n_full ? -1 : (int)((bid - a.n_full) & 1);  // -1: the whole view
+  const int h = (int)(unit / a.q_tiles);
+  const int64_t qt = unit - (int64_t)h * a.q_tiles;
+  const int64_t t_begin = part == 1 ? a.t_mid : 0, t_end = part == 0 ? a.t_mid : a.n_keys;  // this CTA's keys
   const int H = a.H;
   const float slog2e = a.scale * 1.4426950408889634f;
-  const int n_tiles = (int)((a.n_keys + kPfKTile - 1) / kPfKTile);
+  const int n_tiles = (int)((t_end - t_begin + kPfKTile - 1) / kPfKTile);
 
   if (tid == 0) {
     for (int i = 0; i < kPfBufs; ++i) {
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // softmax threads: their Q row (zeros past n_q) and scale log2e q . mean per view slot
-  const int64_t rowq = (int64_t)blockIdx.x * kPfRows + tid;
+  const int64_t rowq = qt * kPfRows + tid;
   if (warp < kPfSoftmaxWarps) {
     const bool q_ok = rowq < a.n_q;
     const uint4* src = reinterpret_cast<const uint4*>(a.q + (rowq * H + h) * kPfD);
@@ -507,12 +520,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     if (ok && pf_wait_warp(&o_done[2 * half + (jl & 1)], (jl >> 1) & 1)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const float f = __fdiv_rn(G, l);
+      float* P = part < 0 ? nullptr : a.part + ((unit - a.n_full) * 2 + part) * kPfPartFloats;
+      if (P) {  // a split half: its rows' m and l beside its G O / l
+        P[kPfRows * kPfD + tid] = m;
+        P[kPfRows * kPfD + kPfRows + tid] = l;
+      }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
         pf_ld32(t_O + 32 * c, o);
         if (rowq < a.n_q) {
-          float4* dst = reinterpret_cast<float4*>(a.out + (rowq * H + h) * kPfD + 32 * c);
+          float4* dst = reinterpret_cast<float4*>(P ? P + (int64_t)tid * kPfD + 32 * c : a.out + (rowq * H + h) * kPfD + 32 * c);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__fmul_rn(o[4 * i], f), __fmul_rn(o[4 * i + 1], f), __fmul_rn(o[4 * i + 2], f),
@@ -538,8 +556,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* free_ = is_k ? k_free : v_free;
     uint8_t* tiles = is_k ? Kb : Vb;
-    const uint32_t L = (uint32_t)a.L_f, n_keys = (uint32_t)a.n_keys;
-    const uint32_t t_first = (uint32_t)(grp * kPfKTile + key);
+    const uint32_t L = (uint32_t)a.L_f, t_stop = (uint32_t)t_end;
+    const uint32_t t_first = (uint32_t)(t_begin + grp * kPfKTile + key);
     uint32_t f = t_first / L, rr = t_first - f * L;  // frame and offset of the key in the group's first tile
     uint4 kc[4];
     uint2 ks;
@@ -549,7 +567,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
       for (int i = 0; i < 4; ++i) kc[i] = make_uint4(0u, 0u, 0u, 0u);
       ks = make_uint2(0u, 0u);
       kvs = -1;
-      if (t < n_keys) {
+      if (t < t_stop) {
         const int64_t base = (view.row[f] + (int64_t)rr) * a.H + h;
         const uint4* src = reinterpret_cast<const uint4*>(codes + base * (kPfD / 2));
 #pragma unroll
@@ -587,7 +605,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
           rr -= L;
           ++f;
         }
-        load_key((uint32_t)((j + 2) * kPfKTile + key));
+        load_key((uint32_t)(t_begin + (j + 2) * kPfKTile + key));
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -641,21 +659,77 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
   }
 }
 
+// The two halves of each split unit: out = (o_0 w_0 + o_1 w_1) / (w_0 + w_1) with
+// w_i = l_i 2^(m_i - max(m_0, m_1)) (o_i = G O_i / l_i over the half's keys).  One thread per
+// row and 4 channels.
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const float* __restrict__ part, float* __restrict__ out,
+                                                            int64_t n_split, int64_t n_full, int64_t q_tiles,
+                                                            int64_t n_q, int H) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_split * kPfRows * (kPfD / 4)) return;
+  const int c4 = (int)(i % (kPfD / 4));
+  const int r = (int)((i / (kPfD / 4)) % kPfRows);
+  const int64_t s = i / ((int64_t)kPfRows * (kPfD / 4));
+  const int64_t unit = n_full + s;
+  const int h = (int)(unit / q_tiles);
+  const int64_t row = (unit - (int64_t)h * q_tiles) * kPfRows + r;
+  if (row >= n_q) return;
+  const float* P0 = part + 2 * s * kPfPartFloats;
+  const float* P1 = P0 + kPfPartFloats;
+  const float m0 = P0[kPfRows * kPfD + r], m1 = P1[kPfRows * kPfD + r];
+  const float l0 = P0[kPfRows * kPfD + kPfRows + r], l1 = P1[kPfRows * kPfD + kPfRows + r];
+  const float mm = fmaxf(m0, m1);
+  const float w0 = __fmul_rn(l0, ex2_approx(m0 - mm)), w1 = __fmul_rn(l1, ex2_approx(m1 - mm));
+  const float inv = __frcp_rn(__fadd_rn(w0, w1));
+  const float4 o0 = reinterpret_cast<const float4*>(P0 + (int64_t)r * kPfD)[c4];
+  const float4 o1 = reinterpret_cast<const float4*>(P1 + (int64_t)r * kPfD)[c4];
+  float4 v;
+  v.x = __fmul_rn(__fmaf_rn(o0.x, w0, __fmul_rn(o1.x, w1)), inv);
+  v.y = __fmul_rn(__fmaf_rn(o0.y, w0, __fmul_rn(o1.y, w1)), inv);
+  v.z = __fmul_rn(__fmaf_rn(o0.z, w0, __fmul_rn(o1.z, w1)), inv);
+  v.w = __fmul_rn(__fmaf_rn(o0.w, w0, __fmul_rn(o1.w, w1)), inv);
+  reinterpret_cast<float4*>(out + (row * H + h) * kPfD)[c4] = v;
+}
+
 bool pf_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int pf_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
+// The units of the last, partial wave of CTAs are split along keys when they fill at most half
+// of the SMs (the wave then ends after about half a unit's time): how many.
+int64_t pf_split_units(int64_t n_q, int H, int64_t n_keys, int sms) {
+  const int64_t units = (n_q + kPfRows - 1) / kPfRows * H;
+  const int64_t r = sms > 0 ? units % sms : 0;
+  return ((n_keys + kPfKTile - 1) / kPfKTile >= 2 && r > 0 && 2 * r <= sms) ? r : 0;
+}
 
 }  // namespace
 }  // namespace nvfp4
 
 extern "C" {
 
+size_t nvfp4_kv_attention_prefill_workspace_bytes(int64_t n_q, int H, int n_frames, int64_t tokens_per_frame) {
+  if (n_q < 1 || H < 1 || n_frames < 1 || tokens_per_frame < 1 || n_frames > NVFP4_MAX_VIEW_FRAMES ||
+      tokens_per_frame > ((int64_t)1 << 40) / NVFP4_MAX_VIEW_FRAMES)
+    return 0;
+  const int64_t split = nvfp4::pf_split_units(n_q, H, (int64_t)n_frames * tokens_per_frame, nvfp4::pf_sm_count());
+  return (size_t)split * 2 * nvfp4::kPfPartFloats * sizeof(float);
+}
+
 nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const uint8_t* k_codes,
                                         const uint8_t* k_scales, const float* k_g, const float* k_mean,
                                         const uint8_t* v_codes, const uint8_t* v_scales, const float* v_g,
                                         int64_t pool_rows, int n_meta, const int64_t* frame_row,
                                         const int* frame_meta, int n_frames, int64_t tokens_per_frame, int H, int D,
-                                        float scale, float* out, int* dev_status, void* stream) {
+                                        float scale, float* out, void* workspace, size_t workspace_bytes,
+                                        int* dev_status, void* stream) {
   if (D != nvfp4::kPfD || H < 1 || H > 65535) return NVFP4_ESHAPE;
-  if (n_q < 1 || n_q > ((int64_t)1 << 30) * nvfp4::kPfRows) return NVFP4_ESHAPE;
+  if (n_q < 1 || (n_q + nvfp4::kPfRows - 1) / nvfp4::kPfRows * H > ((int64_t)1 << 30)) return NVFP4_ESHAPE;
   if (n_frames < 1 || n_frames > NVFP4_MAX_VIEW_FRAMES || tokens_per_frame < 1 || pool_rows < 1 || n_meta < 1)
     return NVFP4_ESHAPE;
   if (tokens_per_frame > ((int64_t)1 << 40) / NVFP4_MAX_VIEW_FRAMES) return NVFP4_ESHAPE;
@@ -664,7 +738,7 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
     return NVFP4_ESHAPE;
   if (!q_bf16 || !k_codes || !k_scales || !k_g || !v_codes || !v_scales || !v_g || !frame_row || !frame_meta || !out)
     return NVFP4_EINVAL;
-  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(k_codes, 16) || !nvfp4::pf_aligned(k_scales, 8) ||
+  if (!nvfp4::pf_aligned(q_bf16, 16) || !nvfp4::pf_aligned(workspace, 16) || !nvfp4::pf_aligned(k_codes, 16) || !nvfp4::pf_aligned(k_scales, 8) ||
       !nvfp4::pf_aligned(v_codes, 16) || !nvfp4::pf_aligned(v_scales, 8) ||
       !nvfp4::pf_aligned(k_g, 4) || !nvfp4::pf_aligned(v_g, 4) || !nvfp4::pf_aligned(out, 16) ||
       !nvfp4::pf_aligned(k_mean, 4) || !nvfp4::pf_aligned(dev_status, 4))
@@ -701,9 +775,23 @@ nvfp4_status nvfp4_kv_attention_prefill(const void* q_bf16, int64_t n_q, const u
   a.scale = scale;
   static std::atomic<unsigned long long> smem_set{0};
   if (nvfp4::smem_limit_once(nvfp4::attn_prefill_kernel, nvfp4::kPfSmem, smem_set) != cudaSuccess) return NVFP4_ECUDA;
-  const int64_t q_per_cta = nvfp4::kPfRows;
-  const dim3 grid((unsigned)((n_q + q_per_cta - 1) / q_per_cta), (unsigned)H);
-  nvfp4::attn_prefill_kernel<<<grid, nvfp4::kPfThreads, nvfp4::kPfSmem, static_cast<cudaStream_t>(stream)>>>(view, a);
+  a.q_tiles = (n_q + nvfp4::kPfRows - 1) / nvfp4::kPfRows;
+  const int64_t units = a.q_tiles * H;
+  int64_t split = 0;
+  if (workspace) {
+    split = nvfp4::pf_split_units(n_q, H, a.n_keys, nvfp4::pf_sm_count());
+    if (workspace_bytes < (size_t)split * 2 * nvfp4::kPfPartFloats * sizeof(float)) return NVFP4_EINVAL;
+  }
+  a.part = static_cast<float*>(workspace);
+  a.n_full = units - split;
+  a.t_mid = (a.n_keys + nvfp4::kPfKTile - 1) / nvfp4::kPfKTile / 2 * nvfp4::kPfKTile;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  nvfp4::attn_prefill_kernel<<<(unsigned)(units + split), nvfp4::kPfThreads, nvfp4::kPfSmem, st>>>(view, a);
+  if (split > 0) {
+    const int64_t threads = split * nvfp4::kPfRows * (nvfp4::kPfD / 4);
+    nvfp4::prefill_merge_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(a.part, out, split, a.n_full,
+                                                                                   a.q_tiles, n_q, H);
+  }
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 

@@ -71,15 +71,16 @@ def queries(n_q, H, D, seed, sd=1.0):
     return bits, (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-def run_and_check(nv, cache, pk, pv, qbits, qf, scale, heads=None, rows_q=None):
-    """Runs all queries on the GPU; compares the oracle on `heads` (all by default) and on the
-    query rows `rows_q` (all by default)."""
+def run_and_check(nv, cache, pk, pv, qbits, qf, scale, heads=None, rows_q=None, split=True):
+    """Runs all queries on the GPU (with the last wave's units split along the keys when
+    `split`); compares the oracle on `heads` (all by default) and on the query rows `rows_q`
+    (all by default)."""
     from oracle import attention as oa
 
     fi, fr, fs = cache.view()
     L = cache.state.tokens_per_frame
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = host(nv.kv_attention_prefill(dev(qbits), pk, pv, fr, fs, L, scale, status=status))
+    out = host(nv.kv_attention_prefill(dev(qbits), pk, pv, fr, fs, L, scale, status=status, split=split))
     assert int(host(status)[0]) == 0
     if rows_q is not None:
         out, qf = out[rows_q], qf[rows_q]
@@ -118,21 +119,23 @@ def test_prefill_one_query_and_one_frame(nv):
     run_and_check(nv, cache, pk, pv, qbits, qf, 0.3)
 
 
-def test_prefill_cache_read_view(nv):
+@pytest.mark.parametrize("split", [True, False])
+def test_prefill_cache_read_view(nv, split):
     """The cache-read workload's view: 3 sink + 18 rolling frames of 880 tokens, 24 heads x 128,
-    130 queries (two tiles); heads 0, 11 and 23 against the oracle."""
+    130 queries (one 256-query unit per head, so all 24 units form the last wave and are split along
+    the keys unless `split` is off); heads 0, 11 and 23 against the oracle."""
     cache, pk, pv = fill_cache(nv, F=8, L=880, H=24, D=128, S_g=3, S_s=3, W=18, n_chunks=5)
     assert len(cache.view()[1]) == 21
     qbits, qf = queries(130, 24, 128, 9, sd=0.5)
-    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[0, 11, 23])
+    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[0, 11, 23], split=split)
 
 
 def test_prefill_whole_chunk_sampled(nv):
     """The row's shape: a whole chunk of 7040 queries x 24 heads over the 21-frame view in one call;
-    48 sampled query rows (both halves of many CTAs, the last ragged CTA included) of heads 5 and 17
-    against the oracle."""
+    48 sampled query rows (both halves of many CTAs, the last ragged CTA included) of heads 5, 17
+    and 23 against the oracle (on 152 SMs the last 64 of the 672 units, heads 21-23, run split)."""
     cache, pk, pv = fill_cache(nv, F=8, L=880, H=24, D=128, S_g=3, S_s=3, W=18, n_chunks=5, seed0=1500)
     qbits, qf = queries(7040, 24, 128, 11, sd=0.5)
     rows_q = np.sort(np.concatenate([np.random.default_rng(12).choice(7040, 44, replace=False),
                                      np.array([0, 255, 256, 7039])]))
-    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[5, 17], rows_q=rows_q)
+    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[5, 17, 23], rows_q=rows_q)

@@ -243,11 +243,11 @@ def test_prefill_attention_argument_errors(lib):
     fm = np.array([0, 1], np.int32)
 
     def call(n_q=200, D=128, fr_=fr, fm_=fm, n=None, pool_rows=64, n_meta=2, q=dev, codes=dev, out=dev,
-             k_scales=dev, v_codes=dev, v_scales=dev):
+             k_scales=dev, v_codes=dev, v_scales=dev, ws=None):
         n = len(fr_) if n is None else n
         return lib.load().nvfp4_kv_attention_prefill(q, n_q, codes, k_scales, dev, dev, v_codes, v_scales, dev,
                                                      pool_rows, n_meta, fr_.ctypes.data, fm_.ctypes.data, n, 16, 2,
-                                                     D, 0.125, out, None, None)
+                                                     D, 0.125, out, ws, 1 << 30, None, None)
 
     assert call(D=64) == lib.NVFP4_ESHAPE                               # head dimension 128 only
     assert call(n_q=0) == lib.NVFP4_ESHAPE
@@ -262,3 +262,4 @@ def test_prefill_attention_argument_errors(lib):
     # a key's 64 code bytes are read as four 16-byte words and its 8 scale bytes as one word
     assert call(codes=dev + 8) == lib.NVFP4_EALIGN and call(v_codes=dev + 8) == lib.NVFP4_EALIGN
     assert call(k_scales=dev + 4) == lib.NVFP4_EALIGN and call(v_scales=dev + 4) == lib.NVFP4_EALIGN
+    assert call(ws=dev + 8) == lib.NVFP4_EALIGN                        # the key-split workspace

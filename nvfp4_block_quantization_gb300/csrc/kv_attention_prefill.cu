@@ -33,12 +33,13 @@
 //                     A tile whose keys share one view slot (most of them) takes the slot's
 //                     factors as scalars and the extreme raw S with 3-input max, and forms P'
 //                     in packed fp32x2 arithmetic;
-//   warps 8, 9, 12, 13  K' decoders (sub-partitions 0 and 1), warps 10, 11, 14, 15 V'
-//                     decoders (2 and 3): thread k owns key k of every other tile, loads its
+//   warps 8, 9, 12, 13  K' decoders (sub-partitions 0 and 1), warps 10, 11, 16, 17 V'
+//                     decoders: thread k owns key k of every other tile, loads its
 //                     72 code and scale bytes a tile ahead, and writes its 128 bf16 channels,
 //                     E2M1 magnitudes taken from byte-permute tables and multiplied by the block
 //                     scale in bf16x2 (exact); the K' decoders also write each key's factors;
-//   warps 16, 17      one thread per half issues that half's MMAs: S_h(j + 2) = Q_h K'(j + 2)^T
+//   warps 14, 15      one thread per half (sub-partitions 2 and 3, beside the lighter V'
+//                     decoders) issues that half's MMAs: S_h(j + 2) = Q_h K'(j + 2)^T
 //                     into the S buffer that P'_h(j) V'(j) has just read, so S stays one tile
 //                     ahead of the softmax.
 // TMEM per half: two 64-column S buffers (P' over the first 32 columns of each) and a
@@ -61,8 +62,8 @@ constexpr int kPfRows = kPfQTile * kPfHalves;
 constexpr int kPfD = 128;              // head dimension
 constexpr int kPfSoftmaxWarps = 4 * kPfHalves;
 constexpr int kPfDecodeWarps = 8;      // K' on sub-partitions 0 and 1, V' on 2 and 3
-constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDecodeWarps;
-constexpr int kPfThreads = 32 * (kPfMmaWarp + kPfHalves);  // one MMA-issuing warp per half
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDecodeWarps;  // the warp that allocates TMEM
+constexpr int kPfThreads = 32 * (kPfMmaWarp + kPfHalves);  // plus one MMA-issuing warp per half
 constexpr int kPfMaxSlots = 16;        // distinct pool slots in one view
 constexpr int kPfBufs = 4;             // K' and V' tile buffers each
 constexpr int kPfKeyBufs = 8;          // key-factor table buffers
@@ -540,15 +541,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     } else {
       atomicExch(failed, 1);
     }
-  } else if (warp < kPfMmaWarp) {
+  } else if (warp != 14 && warp != 15) {
     // ================= K' and V' tiles, one key per thread =================
     // Warps 8, 9 and 12, 13 (sub-partitions 0 and 1) decode K' and write the key factors; warps
-    // 10, 11 and 14, 15 (sub-partitions 2 and 3) decode V'.  Warps 8, 9 / 10, 11 take the even
-    // tiles, 12, 13 / 14, 15 the odd ones.  Thread `key` owns key `key` of its tiles: the key's 64
+    // 10, 11 and 16, 17 decode V'.  Warps 8, 9 / 10, 11 take the even tiles, 12, 13 / 16, 17 the
+    // odd ones.  Thread `key` owns key `key` of its tiles: the key's 64
     // code bytes and 8 scale bytes are loaded a tile ahead (nothing reads them until the tile is
     // decoded), and its 128 bf16 channels stored as 16 chunks of 16 bytes in the same [key][d]
     // core-matrix layout for both (K-major for S = Q K'^T, MN-major for P' V').
-    const int dq = warp - kPfSoftmaxWarps;
+    const int dq = warp < 14 ? warp - kPfSoftmaxWarps : warp - 10;  // warps 8-13, 16, 17 -> 0..7
     const bool is_k = (dq & 2) == 0;
     const int grp = dq >> 2, key = 32 * (dq & 1) + lane;
     const uint8_t* codes = is_k ? a.k_codes : a.v_codes;
@@ -616,7 +617,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(const __gri
     // ================= MMA issue, one thread per half =================
     // S is one tile ahead: S_hh(j + 2) goes into S buffer j % 2 as soon as P'_hh(j) V'(j) has
     // read P'_hh(j) from it, so the softmax finds S_hh(j + 1) ready.
-    const int hh = warp - kPfMmaWarp;
+    const int hh = warp - 14;  // warps 14, 15: sub-partitions 2 and 3
     const uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfKTile >> 3) << 17) |
                              ((uint32_t)(kPfQTile >> 4) << 24);  // bf16 x bf16 -> fp32, K-major, N = 64 keys
     const uint32_t idesc_o = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kPfD >> 3) << 17) |

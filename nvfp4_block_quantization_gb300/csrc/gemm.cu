@@ -12,8 +12,9 @@
 // scale per 16 elements of K on each operand, fp32 accumulation in TMEM), in a
 // persistent kernel, one CTA per SM walking 128 x 256 tiles of Y:
 //   - a TMA thread streams 128-byte-swizzled K slices of 256 elements of X and
-//     W codes, with the matching scale tiles (plain bulk copies), into a
-//     4-stage shared-memory ring that runs on across tiles;
+//     W codes, with the matching scale tiles (plain bulk copies, issued first on
+//     a barrier of their own), into a 4-stage shared-memory ring that runs on
+//     across tiles;
 //   - four scale warps move each slice's scales from shared memory into TMEM
 //     (tcgen05.st), so the tensor-pipe queue holds MMAs only;
 //   - one MMA thread issues the slice's four 128 x 256 x 64 MMAs;
@@ -215,7 +216,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
   uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + kEpiWarps * kEpiStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* sf_ready = empty + kStages;
-  uint64_t* acc_full = sf_ready + kStages;
+  uint64_t* sf_full = sf_ready + kStages;  // a stage's scale bytes landed (ahead of its codes)
+  uint64_t* acc_full = sf_full + kStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], kScaleWarps);
+      mbar_init(&sf_full[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiWarps);
@@ -262,18 +265,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
           uint8_t* st = smem + s * kStageBytes;
           const int kt0 = kb * (kBK / kMmaK);
           const int nkt = min(kBK / kMmaK, a.kbt - kt0);
-          mbar_expect_tx(&full[s], kABytes + kBBytes + 512u * nkt * (1 + n_rt));
-          tma_load_2d(st, &map_x, kb * (kBK / 2), m0, &full[s]);
-          tma_load_2d(st + kABytes, &map_w, kb * (kBK / 2), n0, &full[s]);
-          bulk_load(st + kABytes + kBBytes, a.sfa + ((size_t)(m0 / 128) * a.kbt + kt0) * 512, 512u * nkt, &full[s]);
+          // the scales first, on their own barrier: the scale warps move them into TMEM while the
+          // codes are still landing
+          mbar_expect_tx(&sf_full[s], 512u * nkt * (1 + n_rt));
+          bulk_load(st + kABytes + kBBytes, a.sfa + ((size_t)(m0 / 128) * a.kbt + kt0) * 512, 512u * nkt, &sf_full[s]);
           for (int rt = 0; rt < n_rt; ++rt)
             bulk_load(st + kABytes + kBBytes + kSfaBytes + rt * (kSfbBytes / 2),
-                      a.sfb + ((size_t)(n0 / 128 + rt) * a.kbt + kt0) * 512, 512u * nkt, &full[s]);
+                      a.sfb + ((size_t)(n0 / 128 + rt) * a.kbt + kt0) * 512, 512u * nkt, &sf_full[s]);
+          mbar_expect_tx(&full[s], kABytes + kBBytes);
+          tma_load_2d(st, &map_x, kb * (kBK / 2), m0, &full[s]);
+          tma_load_2d(st + kABytes, &map_w, kb * (kBK / 2), n0, &full[s]);
         }
       }
       // copies still in flight land before the CTA leaves
       for (uint32_t q = g > (uint32_t)kStages ? g - kStages : 0; q < g; ++q)
-        if (!mbar_wait(&full[q % kStages], (q / kStages) & 1)) atomicExch(failed, 1);
+        if (!mbar_wait(&full[q % kStages], (q / kStages) & 1) || !mbar_wait(&sf_full[q % kStages], (q / kStages) & 1))
+          atomicExch(failed, 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -289,7 +296,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int s = g % kStages;
-          if (!mbar_wait(&sf_ready[s], (g / kStages) & 1)) { ok = false; break; }
+          if (!mbar_wait(&sf_ready[s], (g / kStages) & 1) || !mbar_wait(&full[s], (g / kStages) & 1)) {
+            ok = false;
+            break;
+          }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t st = smem_u32(smem + s * kStageBytes);
           const int nkt = min(kBK / kMmaK, a.kbt - kb * (kBK / kMmaK));
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         const int s = g % kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (g / kStages) & 1));  // warp-uniform: tcgen05.st is .aligned
+        ok = __all_sync(0xffffffffu, mbar_wait(&sf_full[s], (g / kStages) & 1));  // warp-uniform: tcgen05.st is .aligned
         if (!ok) break;
         const uint8_t* sf = smem + s * kStageBytes + kABytes + kBBytes;
         const int nkt = min(kBK / kMmaK, a.kbt - kb * (kBK / kMmaK));

@@ -136,7 +136,7 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint3
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
 }
-constexpr uint32_t kLayoutNone = 0, kLayoutSw128 = 2;
+constexpr uint32_t kLayoutSw128 = 2;
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -172,13 +172,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t r[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
+__device__ __forceinline__ void tmem_st12(uint32_t taddr, const uint32_t r[12]) {  // columns 0-7 and 8-11
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr + 8), "r"(r[8]),
+               "r"(r[9]), "r"(r[10]), "r"(r[11])
+               : "memory");
 }
+
 
 // Persistent: one CTA per SM walks the 128 x 256 tiles of Y (tile t = blockIdx.x
 // + i gridDim.x, W tiles fastest).  Fourteen warps:
@@ -188,9 +190,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t r[16]) 
 //                      TMEM; waits for the epilogue to hand the accumulator back
 //                      before a new tile's first MMA;
 //   warps 2..5         scales: warp w writes TMEM lane quadrant w % 4 with
-//                      tcgen05.st -- for K step j of stage s, the 16 columns at
+//                      tcgen05.st -- for K step j of stage s, the columns at
 //                      256 + 64 s + 16 j hold W's row tiles 0 and 1 (4 columns
-//                      each) and X's tile (4 columns), lane l of every quadrant
+//                      each) and X's tile (4 columns, then 4 unused), lane l of every quadrant
 //                      holding rows l, l + 32, l + 64, l + 96 of a tile in
 //                      consecutive columns; the tensor-pipe queue then carries
 //                      MMAs only;
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
         const uint8_t* sf = smem + s * kStageBytes + kABytes + kBBytes;
         const int nkt = min(kBK / kMmaK, a.kbt - kb * (kBK / kMmaK));
         for (int j = 0; j < nkt; ++j) {
-          uint32_t r[16];
+          uint32_t r[12];
           const uint4 b0 = *reinterpret_cast<const uint4*>(sf + kSfaBytes + j * 512 + lane * 16);
           const uint4 b1 = n_rt == 2 ? *reinterpret_cast<const uint4*>(sf + kSfaBytes + kSfbBytes / 2 + j * 512 + lane * 16)
                                      : make_uint4(0u, 0u, 0u, 0u);
@@ -344,8 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
           r[0] = b0.x; r[1] = b0.y; r[2] = b0.z; r[3] = b0.w;
           r[4] = b1.x; r[5] = b1.y; r[6] = b1.z; r[7] = b1.w;
           r[8] = a0.x; r[9] = a0.y; r[10] = a0.z; r[11] = a0.w;
-          r[12] = 0u; r[13] = 0u; r[14] = 0u; r[15] = 0u;
-          tmem_st16(lane_base + kTmemSf + s * kSfColsPerStage + j * kSfColsPerMma, r);
+          tmem_st12(lane_base + kTmemSf + s * kSfColsPerStage + j * kSfColsPerMma, r);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

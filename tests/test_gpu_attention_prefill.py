@@ -45,7 +45,7 @@ def host(t):
     return t.detach().cpu().numpy()
 
 
-def fill_cache(nv, F, L, H, D, S_g, S_s, W, n_chunks, shot_after=None, seed0=1400):
+def fill_cache(nv, F, L, H, D, S_g, S_s, W, n_chunks, shot_after=None, seed0=1400, k_gains=None):
     from nvfp4_block_quantization_gb300 import workloads as Wl
 
     cache = nv.KvCache(F, L, S_g, S_s, W)
@@ -55,7 +55,8 @@ def fill_cache(nv, F, L, H, D, S_g, S_s, W, n_chunks, shot_after=None, seed0=140
         if shot_after is not None and c == shot_after:
             cache.new_shot()
         slot = cache.append()
-        K = dev(Wl.to_bf16_bits(Wl.chunk_k(seed0 + 2 * c, T=F * L, H=H, D=D)))
+        gain = 1.0 if k_gains is None else k_gains[c]
+        K = dev(Wl.to_bf16_bits(Wl.chunk_k(seed0 + 2 * c, T=F * L, H=H, D=D) * np.float32(gain)))
         V = dev(Wl.to_bf16_bits(Wl.chunk_v(seed0 + 2 * c + 1, T=F * L, H=H, D=D)))
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         nv.kv_smooth_quant_batched([K, V], [True, False],
@@ -139,3 +140,16 @@ def test_prefill_whole_chunk_sampled(nv):
     rows_q = np.sort(np.concatenate([np.random.default_rng(12).choice(7040, 44, replace=False),
                                      np.array([0, 255, 256, 7039])]))
     run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, heads=[5, 17, 23], rows_q=rows_q)
+
+
+@pytest.mark.parametrize("split", [True, False])
+def test_prefill_rising_scores(nv, split):
+    """K of later chunks scaled up (gains 1/4, 1, 4, 16, 64): the scores jump by far more than the
+    lazy-rescale step at chunk boundaries, so the running maximum moves mid-view and O is rescaled
+    in TMEM; with the key split the two halves' maxima differ by orders of magnitude, so the merge
+    weights are near 0 and 1.  16 frames of 64 tokens, 2 heads, 300 queries."""
+    cache, pk, pv = fill_cache(nv, F=4, L=64, H=2, D=128, S_g=2, S_s=2, W=12, n_chunks=5,
+                               k_gains=[0.25, 1.0, 4.0, 16.0, 64.0])
+    qbits, qf = queries(300, 2, 128, 21)
+    run_and_check(nv, cache, pk, pv, qbits, qf, 128 ** -0.5, split=split)
+

@@ -46,6 +46,8 @@
 // 128-column O.  K' and V' share one [key][d] layout of 8-row x 16-byte core matrices, four
 // buffers each: K-major for S = Q K'^T, MN-major for P' V'.  Every wait is bounded; a timeout is
 // reported in the status word and the CTA drains its MMAs before freeing TMEM.
+// With a workspace, the units of the last, partial wave of CTAs run as two CTAs over the two
+// halves of the keys; prefill_merge_kernel combines them.
 #include <cstring>
 
 #include "nvfp4.h"
@@ -141,7 +143,7 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Issues a 32-column TMEM load without waiting for it (pf_wait_ld32 completes it).
+// Issues a 32-column TMEM load without waiting for it (pf_wait_ld completes it).
 __device__ __forceinline__ void pf_ld32_issue(uint32_t taddr, uint32_t r[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "

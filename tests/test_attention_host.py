@@ -4,7 +4,7 @@
   for bit: two independent statements of the same formula.
 - Closed forms of softmax attention: identical keys give the plain mean of V; one key
   far ahead of the others gives that token's V; adding a constant to every score
-  changes nothing.
+  changes nothing; two keys with score gap ln 3 / scale weigh 1/4 and 3/4 (also the bound's B).
 """
 import numpy as np
 
@@ -90,3 +90,23 @@ def test_two_keys_weighted_by_the_scaled_score_gap():
     assert np.allclose(out[0], want, rtol=0, atol=1e-12)
     assert np.allclose(A[0], [scale * c, scale * c], rtol=1e-15, atol=0)
     assert np.array_equal(Vmax, [8.0, 12.0])
+
+
+def test_weighted_abs_of_two_keys():
+    """attention_weighted_abs on the same two-key case: weights exactly 1/4 and 3/4, so
+    out = v0 / 4 + 3 v1 / 4 and B = |v0| / 4 + 3 |v1| / 4 per channel (B bounds how far a
+    relative error in every weight can move the output).  Values of both signs, so a
+    missing absolute value changes B."""
+    D = 16
+    q = np.zeros((1, 1, D))
+    q[0, 0, :] = 1.0
+    c = 8.0
+    scale = np.log(3.0) / c
+    k = np.zeros((2, 1, D))
+    k[1, 0, :] = c / D
+    v = np.zeros((2, 1, D))
+    v[0, 0, :] = np.arange(D) - 7.5
+    v[1, 0, :] = 3.0 - 0.5 * np.arange(D)
+    out, B = oa.attention_weighted_abs(q, k, v, scale)
+    assert np.allclose(out[0, 0], 0.25 * v[0, 0] + 0.75 * v[1, 0], rtol=0, atol=1e-12)
+    assert np.allclose(B[0, 0], 0.25 * np.abs(v[0, 0]) + 0.75 * np.abs(v[1, 0]), rtol=0, atol=1e-12)

@@ -263,3 +263,14 @@ def test_prefill_attention_argument_errors(lib):
     assert call(codes=dev + 8) == lib.NVFP4_EALIGN and call(v_codes=dev + 8) == lib.NVFP4_EALIGN
     assert call(k_scales=dev + 4) == lib.NVFP4_EALIGN and call(v_scales=dev + 4) == lib.NVFP4_EALIGN
     assert call(ws=dev + 8) == lib.NVFP4_EALIGN                        # the key-split workspace
+
+
+def test_prefill_workspace_bytes_without_a_device(lib):
+    """The key-split workspace size: 0 for invalid shapes, and 0 where no device reports an SM
+    count (nothing is split then); never an error or a CUDA call that fails loudly."""
+    f = lib.load().nvfp4_kv_attention_prefill_workspace_bytes
+    assert f(0, 24, 21, 880) == 0 and f(7040, 0, 21, 880) == 0 and f(7040, 24, 0, 880) == 0
+    assert f(7040, 24, 21, 0) == 0 and f(7040, 24, 1 << 20, 880) == 0
+    import torch
+    if not torch.cuda.is_available():
+        assert f(7040, 24, 21, 880) == 0

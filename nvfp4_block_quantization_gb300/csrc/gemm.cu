@@ -10,7 +10,9 @@
 // The contraction is a dense block-scaled FP4 GEMM on the 5th-generation
 // tensor cores, written here directly (tcgen05.mma kind::mxf4nvf4, one UE4M3
 // scale per 16 elements of K on each operand, fp32 accumulation in TMEM), in a
-// persistent kernel, one CTA per SM walking 128 x 256 tiles of Y:
+// persistent kernel, one CTA per SM walking 128 x 256 tiles of Y (when the last
+// wave would leave more than half of the SMs idle, each of its tiles runs as two
+// 128 x 128 halves on two CTAs):
 //   - a TMA thread streams 128-byte-swizzled K slices of 256 elements of X and
 //     W codes, with the matching scale tiles (plain bulk copies, issued first on
 //     a barrier of their own), into a 4-stage shared-memory ring that runs on
@@ -154,7 +156,23 @@ struct GemmArgs {
   int M, N, K;
   int kbt;              // scale tiles along K: ceil(K / 64)
   int* err;
+  int n_full;           // tiles [0, n_full) run whole; each later tile as two 128-column halves
 };
+
+// Work unit u of the persistent walk: a whole 128 x 256 tile of Y (W tiles
+// fastest) or one 128-column half of a tile of the last wave.
+struct GemmUnit {
+  int m0, n0;  // first row and column of Y
+  int width;   // columns: up to 256 (a whole tile) or 128 (a half)
+  bool half;
+};
+
+__device__ __forceinline__ GemmUnit gemm_unit(int u, int n_full, int tiles_n, int N) {
+  const bool half = u >= n_full;
+  const int t = half ? n_full + ((u - n_full) >> 1) : u;
+  const int n0 = (t % tiles_n) * kBN + (half ? ((u - n_full) & 1) * 128 : 0);
+  return GemmUnit{(t / tiles_n) * kBM, n0, min(half ? 128 : kBN, N - n0), half};
+}
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
   asm volatile(
@@ -182,8 +200,10 @@ __device__ __forceinline__ void tmem_st12(uint32_t taddr, const uint32_t r[12]) 
 }
 
 
-// Persistent: one CTA per SM walks the 128 x 256 tiles of Y (tile t = blockIdx.x
-// + i gridDim.x, W tiles fastest).  Fourteen warps:
+// Persistent: one CTA per SM walks the work units (u = blockIdx.x + i gridDim.x): the
+// 128 x 256 tiles of Y, W tiles fastest, the last wave's as 128 x 128 halves (a half
+// loads 128 rows of W through its own tensor map and issues N = 128 MMAs; the
+// epilogue warps of columns 128..255 then have nothing to store).  Fourteen warps:
 //   warp 0, one lane   loads: the stage ring runs on across tiles, so the next
 //                      tile's first stages arrive while the epilogue drains;
 //   warp 1, one lane   issues each stage's four MMAs once its scales are in
@@ -211,6 +231,7 @@ constexpr int kGemmThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_x,
                                                                     const __grid_constant__ CUtensorMap map_w,
+                                                                    const __grid_constant__ CUtensorMap map_w_half,
                                                                     GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -230,6 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
   const int tiles_n = (a.N + kBN - 1) / kBN;
   const int tiles = tiles_n * ((a.M + kBM - 1) / kBM);
   const int nkb = (a.K + kBK - 1) / kBK;
+  const int units = a.n_full + 2 * (tiles - a.n_full);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -258,9 +280,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
     if (lane == 0) {
       // ---- loads ----
       uint32_t g = 0;  // stages issued so far (all tiles)
-      for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x) {
-        const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
-        const int n_rt = min(kBN, a.N - n0) > 128 ? 2 : 1;
+      for (int u = blockIdx.x; u < units && !*vfailed; u += gridDim.x) {
+        const GemmUnit un = gemm_unit(u, a.n_full, tiles_n, a.N);
+        const int m0 = un.m0, n0 = un.n0;
+        const int n_rt = un.width > 128 ? 2 : 1;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int s = g % kStages;
           if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1)) { atomicExch(failed, 1); break; }
@@ -274,9 +297,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
           for (int rt = 0; rt < n_rt; ++rt)
             bulk_load(st + kABytes + kBBytes + kSfaBytes + rt * (kSfbBytes / 2),
                       a.sfb + ((size_t)(n0 / 128 + rt) * a.kbt + kt0) * 512, 512u * nkt, &sf_full[s]);
-          mbar_expect_tx(&full[s], kABytes + kBBytes);
+          mbar_expect_tx(&full[s], kABytes + (un.half ? kBBytes / 2 : kBBytes));
           tma_load_2d(st, &map_x, kb * (kBK / 2), m0, &full[s]);
-          tma_load_2d(st + kABytes, &map_w, kb * (kBK / 2), n0, &full[s]);
+          tma_load_2d(st + kABytes, un.half ? &map_w_half : &map_w, kb * (kBK / 2), n0, &full[s]);
         }
       }
       // copies still in flight land before the CTA leaves
@@ -289,8 +312,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
       // ---- MMAs ----
       uint32_t g = 0;
       int i = 0;
-      for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x, ++i) {
-        const int n_tile = min(kBN, a.N - (t % tiles_n) * kBN);
+      for (int u = blockIdx.x; u < units && !*vfailed; u += gridDim.x, ++i) {
+        const int n_tile = gemm_unit(u, a.n_full, tiles_n, a.N).width;
         const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(((n_tile + 15) & ~15) >> 3) << 17) |
                                ((uint32_t)(kBM >> 4) << 24);  // E2M1 x E2M1, UE4M3 scales, K-major, fp32 D
         if (i > 0 && !mbar_wait(acc_empty, (i - 1) & 1)) { atomicExch(failed, 1); break; }
@@ -328,8 +351,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
     // ---- scales: shared memory -> registers -> TMEM ----
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t g = 0;
-    for (int t = blockIdx.x; t < tiles && !*vfailed; t += gridDim.x) {
-      const int n_rt = min(kBN, a.N - (t % tiles_n) * kBN) > 128 ? 2 : 1;
+    for (int u = blockIdx.x; u < units && !*vfailed; u += gridDim.x) {
+      const int n_rt = gemm_unit(u, a.n_full, tiles_n, a.N).width > 128 ? 2 : 1;
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         const int s = g % kStages;
@@ -362,12 +385,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_w4a4_kernel(const __grid
     uint8_t* stg = epi_stage + e * kEpiStageBytes;
     const float alpha = __fmul_rn(*a.gx, *a.gw);
     int i = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, i & 1));  // warp-uniform: tcgen05.ld is .aligned
       if (!ok) { atomicExch(failed, 1); break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
-      const int cols = min(128, a.N - n0 - half * 128);  // this warp's valid columns (a multiple of 16, maybe <= 0)
+      const GemmUnit un = gemm_unit(u, a.n_full, tiles_n, a.N);
+      const int m0 = un.m0, n0 = un.n0;
+      const int cols = min(128, un.width - half * 128);  // this warp's valid columns (a multiple of 16, maybe <= 0)
       uint32_t o[64];  // row `lane`, 128 columns as bf16 pairs
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
 #pragma unroll
@@ -542,9 +566,10 @@ nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, cons
     return NVFP4_EALIGN;
   if (!workspace || !nvfp4::aligned_to(workspace, 256) || workspace_bytes < nvfp4_gemm_workspace_bytes())
     return NVFP4_EWORKSPACE;
-  CUtensorMap mx, mw;
+  CUtensorMap mx, mw, mwh;
   if (!nvfp4::encode_codes(plan->encode, &mx, x_codes, plan->M, plan->K, nvfp4::kBM) ||
-      !nvfp4::encode_codes(plan->encode, &mw, w_codes, plan->N, plan->K, nvfp4::kBN))
+      !nvfp4::encode_codes(plan->encode, &mw, w_codes, plan->N, plan->K, nvfp4::kBN) ||
+      !nvfp4::encode_codes(plan->encode, &mwh, w_codes, plan->N, plan->K, nvfp4::kBN / 2))
     return NVFP4_ECUDA;
   nvfp4::GemmArgs a;
   a.sfa = x_scales_mma;
@@ -558,8 +583,14 @@ nvfp4_status nvfp4_gemm_w4a4(nvfp4_gemm_plan* plan, const uint8_t* x_codes, cons
   a.kbt = (int)((plan->K + 63) / 64);
   a.err = static_cast<int*>(workspace);
   const int64_t tiles = ((plan->N + nvfp4::kBN - 1) / nvfp4::kBN) * ((plan->M + nvfp4::kBM - 1) / nvfp4::kBM);
-  const unsigned grid = (unsigned)(tiles < plan->sms ? tiles : plan->sms);
-  nvfp4::gemm_w4a4_kernel<<<grid, nvfp4::kGemmThreads, nvfp4::kGemmSmem, static_cast<cudaStream_t>(stream)>>>(mx, mw, a);
+  // a last wave on at most half of the SMs runs as 128-column halves (every tile wider than 128)
+  const int64_t r = tiles % plan->sms;
+  const bool split = r > 0 && 2 * r <= plan->sms && (plan->N % nvfp4::kBN == 0 || plan->N % nvfp4::kBN > 128);
+  a.n_full = (int)(split ? tiles - r : tiles);
+  const int64_t units = a.n_full + 2 * (tiles - a.n_full);
+  const unsigned grid = (unsigned)(units < plan->sms ? units : plan->sms);
+  nvfp4::gemm_w4a4_kernel<<<grid, nvfp4::kGemmThreads, nvfp4::kGemmSmem, static_cast<cudaStream_t>(stream)>>>(mx, mw,
+                                                                                                          mwh, a);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ECUDA;
 }
 

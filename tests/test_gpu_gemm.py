@@ -106,11 +106,14 @@ def test_w4a4_small_ragged(nv):
     check(y, ref, sabs, K)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 48, 96), (129, 272, 320), (1, 16, 32), (385, 512, 768)])
+@pytest.mark.parametrize("M,N,K", [(300, 48, 96), (129, 272, 320), (1, 16, 32), (385, 512, 768), (200, 400, 512)])
 def test_w4a4_tails(nv, M, N, K):
     """Edges of the 128 x 256 output tiles and of the 256-element K slices: N = 16 past a tile
     boundary, K not a multiple of 64 (a half-filled last MMA step), M = 1, an odd number of row
-    tiles; every output against the oracle."""
+    tiles; every output against the oracle.  With few tiles the whole grid is one last wave: at
+    N = 512 and 400 every tile runs as two 128-column halves on two CTAs (at N = 400 the last
+    halves are 128 and 16 columns wide); tiles of at most 128 valid columns (N = 48, 16, 272 - 256)
+    keep the grid whole."""
     from oracle import gemm as og
 
     rng = np.random.default_rng(M + N + K)
@@ -126,7 +129,9 @@ def test_w4a4_tails(nv, M, N, K):
 
 def test_w4a4_linear_sizes_sampled_rows(nv):
     """Activations 7040 x 3072 ~ N(0, 1) and a 3072 x 3072 weight ~ N(0, 0.02^2) with 0.1% x30,
-    as the GEMM of a W4A4 linear layer; 64 sampled rows against the oracle."""
+    as the GEMM of a W4A4 linear layer; 64 sampled rows and 4 chosen ones against the oracle (on
+    152 SMs the last 52 of the 660 tiles run as 128-column halves: rows 6400-6527 from column 2048
+    on, and every row from 6528)."""
     from nvfp4_block_quantization_gb300 import workloads as W
     from oracle import gemm as og
 
@@ -135,7 +140,8 @@ def test_w4a4_linear_sizes_sampled_rows(nv):
     Wm = W.weight(0, N, K)
     xq, wq = quantized_operands(nv, X, Wm)
     y = run_gemm(nv, xq, wq, M, N, K)
-    rows = np.sort(np.random.default_rng(5).choice(M, 64, replace=False))
+    rows = np.sort(np.concatenate([np.random.default_rng(5).choice(M, 64, replace=False),
+                                   np.array([6400, 6527, 6528, 7039])]))
     ref, sabs = og.gemm_w4a4(host(xq.codes).reshape(M, K // 2)[rows], host(xq.scales).reshape(M, K // 16)[rows],
                              float(host(xq.tensor_scale)[0]), host(wq.codes), host(wq.scales),
                              float(host(wq.tensor_scale)[0]))

@@ -117,13 +117,14 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
         ve[u] = __ldg(vs + cell * (D / 16) + gl);
       }
     }
-    // then each token in turn: dequantize K, the dot products (shuffle tree over the
-    // group), the online softmax update, dequantize V and accumulate
+    // first the K dot products of all U tokens (independent chains, two per token and query),
+    // with each token's V block scale taken while its slot's tensor scales are current
+    float sc[U][NQ], Sv[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float sc[NQ], kq[16], vq[16];
+      Sv[u] = 0.0f;
 #pragma unroll
-      for (int i = 0; i < NQ; ++i) sc[i] = 0.0f;
+      for (int i = 0; i < NQ; ++i) sc[u][i] = 0.0f;
       if (on[u]) {
         if (sl[u] != mslot) {  // a frame of another slot: its tensor scales (and K means)
           mslot = sl[u];
@@ -148,26 +149,38 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
         }
         // q . k over the block = S_k * (q . Q_k) + q . mean: the scale is common to the block
         const float Sk = __fmul_rn(e4m3_value(ke[u]), gk);
+        Sv[u] = __fmul_rn(e4m3_value(ve[u]), gv);
+        float kq[16];
         decode16(kcode[u], kq);
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
-          float acc = 0.0f;
+          float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc = __fmaf_rn(qv[i][j], kq[j], acc);
-          sc[i] = __fmaf_rn(acc, Sk, cq[i]);
+          for (int j = 0; j < 16; j += 2) {
+            a0 = __fmaf_rn(qv[i][j], kq[j], a0);
+            a1 = __fmaf_rn(qv[i][j + 1], kq[j + 1], a1);
+          }
+          sc[u][i] = __fmaf_rn(__fadd_rn(a0, a1), Sk, cq[i]);
         }
       }
+    }
+    // the dot products' shuffle trees over the group
+#pragma unroll
+    for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int i = 0; i < NQ; ++i)
 #pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1) sc[i] += __shfl_xor_sync(0xffffffffu, sc[i], off);
+        for (int off = G / 2; off > 0; off >>= 1) sc[u][i] += __shfl_xor_sync(0xffffffffu, sc[u][i], off);
+    // then each token in turn: the online softmax update, dequantize V and accumulate
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
       if (on[u]) {
         // p * v = (p * S_v) * Q_v: the scale is folded into the weight
-        const float Sv = __fmul_rn(e4m3_value(ve[u]), gv);
+        float vq[16];
         decode16(vcode[u], vq);
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
-          const float sv = __fmul_rn(sc[i], scale);
+          const float sv = __fmul_rn(sc[u][i], scale);
           if (sv > m[i]) {  // a new running maximum: rescale what has been summed so far
             const float corr = __expf(m[i] - sv);
             l[i] = __fmul_rn(l[i], corr);
@@ -177,7 +190,7 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
           }
           const float p = __expf(sv - m[i]);
           l[i] = __fadd_rn(l[i], p);
-          const float pS = __fmul_rn(p, Sv);
+          const float pS = __fmul_rn(p, Sv[u]);
 #pragma unroll
           for (int j = 0; j < 16; ++j) o[i][j] = __fmaf_rn(pS, vq[j], o[i][j]);
         }

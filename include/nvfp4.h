@@ -350,8 +350,9 @@ nvfp4_status nvfp4_kv_gather_dequant(const uint8_t* codes_pool, const uint8_t* s
  *   k = Q S_k + k_mean[slot][h][d]   (k_mean may be NULL),   v = Q S_v
  *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t
  * all in fp32: over each block q . k is taken as S_k (q . Q) + q . mean and p v
- * as (p S_v) Q; the softmax is online over 256-token ranges, merged exactly as a
- * softmax of the union; out fp32.
+ * as (p S_v) Q; the softmax is online over token ranges (256 to 2048 tokens,
+ * sized so that heads x ranges is one wave of the CTAs the GPU holds at once),
+ * merged exactly as a softmax of the union; out fp32.
  *   q          device [n_q][H][D] fp32, n_q in 1..4, D 64 or 128
  *   k_*, v_*   the pools of nvfp4_kv_gather_dequant (pool_rows rows, n_meta slots;
  *              codes 16-byte aligned, k_mean 16-byte aligned)

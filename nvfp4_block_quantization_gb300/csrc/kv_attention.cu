@@ -17,7 +17,8 @@
 // evaluated as S_k (q . Q_k) + q . mean (the second sum once per slot), and p v as
 // (p S_v) Q_v: the same values up to fp32 rounding order.
 //
-// Split-KV: CTA (h, s) takes the view tokens [s R, (s + 1) R) of head h; a group
+// Split-KV: CTA (h, s) takes the view tokens [s R, (s + 1) R) of head h (R from 256 to
+// 2048 tokens, sized so that the H x S grid is one wave of resident CTAs); a group
 // of D / 16 lanes owns a few tokens per step (one 16-channel scale block per lane
 // and token: one 8-byte code load and one scale byte each, all issued before any
 // is used),
@@ -36,21 +37,34 @@ namespace {
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnMaxQ = 4;
-constexpr int kAttnTokensPerSplit = 256;
+constexpr int kAttnTokensPerSplit = 256;  // the shortest split: the workspace holds ceil(T / 256) partials
+constexpr int kAttnMaxTokensPerSplit = 2048;  // the longest: a lane group's fp32 sums stay at most 128 terms
 
 struct AttnView {
   int64_t row[NVFP4_MAX_VIEW_FRAMES];
   int meta[NVFP4_MAX_VIEW_FRAMES];
 };
 
+// The E2M1 values of four code bytes (eight elements; byte j holds elements 2j in its low nibble
+// and 2j + 1 in its high one), the word split into bytes inside the conversion sequence.
+__device__ __forceinline__ void decode8(uint32_t w, float* out) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+      ".reg .b16 l0, u0, l1, u1, l2, u2, l3, u3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %8;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, b0;\n\tcvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, b2;\n\tcvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+      "mov.b32 {l0, u0}, h0;\n\tmov.b32 {l1, u1}, h1;\n\tmov.b32 {l2, u2}, h2;\n\tmov.b32 {l3, u3}, h3;\n\t"
+      "cvt.f32.f16 %0, l0;\n\tcvt.f32.f16 %1, u0;\n\tcvt.f32.f16 %2, l1;\n\tcvt.f32.f16 %3, u1;\n\t"
+      "cvt.f32.f16 %4, l2;\n\tcvt.f32.f16 %5, u2;\n\tcvt.f32.f16 %6, l3;\n\tcvt.f32.f16 %7, u3;\n\t}"
+      : "=f"(out[0]), "=f"(out[1]), "=f"(out[2]), "=f"(out[3]), "=f"(out[4]), "=f"(out[5]), "=f"(out[6]),
+        "=f"(out[7])
+      : "r"(w));
+}
+
 // The E2M1 values of one token's 16-channel block (one scale block) from its 8 code bytes.
 __device__ __forceinline__ void decode16(uint2 codes, float out[16]) {
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const uint32_t q = e2m1x2_to_f16x2(((p < 4 ? codes.x : codes.y) >> (8 * (p & 3))) & 0xFFu);
-    out[2 * p] = f16lo(q);
-    out[2 * p + 1] = f16hi(q);
-  }
+  decode8(codes.x, out);
+  decode8(codes.y, out + 8);
 }
 
 // Register caps: 128 for one query (16 warps per SM), 168 for two, 255 otherwise.
@@ -58,8 +72,8 @@ template <int D, int NQ>
 __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2)) attn_split_kernel(
     const float* __restrict__ q, const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks,
     const float* __restrict__ kg, const float* __restrict__ kmean, const uint8_t* __restrict__ vc,
-    const uint8_t* __restrict__ vs, const float* __restrict__ vg, int64_t L, int64_t T, int H, float scale,
-    float* __restrict__ part, const __grid_constant__ AttnView view) {
+    const uint8_t* __restrict__ vs, const float* __restrict__ vg, int64_t L, int64_t T, int64_t R, int H,
+    float scale, float* __restrict__ part, const __grid_constant__ AttnView view) {
   constexpr int G = D / 16;         // lanes per token: one 16-channel scale block each
   constexpr int TPW = 32 / G;       // tokens per warp step
   constexpr int W = kAttnThreads / 32;
@@ -81,8 +95,8 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
 #pragma unroll
     for (int j = 0; j < 16; ++j) o[i][j] = 0.0f;
   }
-  const int64_t t_begin = (int64_t)s * kAttnTokensPerSplit;
-  const int64_t t_end = t_begin + kAttnTokensPerSplit < T ? t_begin + kAttnTokensPerSplit : T;
+  const int64_t t_begin = (int64_t)s * R;
+  const int64_t t_end = t_begin + R < T ? t_begin + R : T;
   // U tokens per group per step: their code and scale loads are all issued before
   // any of them is used
   constexpr int U = NQ <= 2 ? 4 : 2;
@@ -232,7 +246,7 @@ __global__ void __launch_bounds__(kAttnThreads, NQ == 1 ? 4 : (NQ == 2 ? 3 : 2))
 
 // out[i][h][d] = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M) over the splits.
 // CTA (h, i): the splits' partials are loaded by the whole CTA into shared
-// memory, kCombineChunk splits at a time (coalesced, all loads in flight), and
+// memory, kCombineChunk splits at a time (coalesced, eight loads in flight per thread), and
 // each chunk is merged into a running (max, sum, weighted V) per channel.
 constexpr int kCombineChunk = 64;
 template <int D>
@@ -245,9 +259,19 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
   for (int c0 = 0; c0 < S; c0 += kCombineChunk) {
     const int n = S - c0 < kCombineChunk ? S - c0 : kCombineChunk;
     __syncthreads();  // the previous chunk has been read
-    for (int x = threadIdx.x; x < n * (D + 2); x += blockDim.x) {
-      const int sj = x / (D + 2), r = x - sj * (D + 2);
-      sp[sj][r] = part[(((size_t)h * S + c0 + sj) * NQ + i) * (D + 2) + r];
+    // eight loads in flight per thread before any is stored
+    for (int x0 = threadIdx.x; x0 < n * (D + 2); x0 += 8 * blockDim.x) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int x = x0 + k * blockDim.x, sj = x / (D + 2), r = x - sj * (D + 2);
+        v[k] = x < n * (D + 2) ? part[(((size_t)h * S + c0 + sj) * NQ + i) * (D + 2) + r] : 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int x = x0 + k * blockDim.x, sj = x / (D + 2), r = x - sj * (D + 2);
+        if (x < n * (D + 2)) sp[sj][r] = v[k];
+      }
     }
     __syncthreads();
     if (d < D) {
@@ -269,11 +293,32 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
   if (d < D) out[(size_t)i * H * D + (size_t)h * D + d] = Os / Ls;
 }
 
+// Tokens per split: the H x S grid fills one wave of the CTAs that fit on the GPU at
+// once (fewer partials for the combine, no partial last wave); a multiple of the
+// 64 tokens a CTA takes per step, between kAttnTokensPerSplit and kAttnMaxTokensPerSplit.
+template <int D, int NQ>
+cudaError_t split_tokens(int64_t T, int H, int64_t* R) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<D, NQ>, kAttnThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t per_head = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) / H);
+  const int64_t r = (T + per_head - 1) / per_head;
+  *R = std::min<int64_t>(kAttnMaxTokensPerSplit, std::max<int64_t>(kAttnTokensPerSplit, (r + 63) / 64 * 64));
+  return cudaSuccess;
+}
+
 template <int D, int NQ>
 cudaError_t launch_attn(const float* q, const uint8_t* kc, const uint8_t* ks, const float* kg, const float* km,
                         const uint8_t* vc, const uint8_t* vs, const float* vg, int64_t L, int64_t T, int H,
-                        float scale, float* part, int S, const AttnView& view, float* out, cudaStream_t st) {
-  attn_split_kernel<D, NQ><<<dim3(H, S), kAttnThreads, 0, st>>>(q, kc, ks, kg, km, vc, vs, vg, L, T, H, scale,
+                        float scale, float* part, const AttnView& view, float* out, cudaStream_t st) {
+  int64_t R = 0;
+  cudaError_t e0 = split_tokens<D, NQ>(T, H, &R);
+  if (e0 != cudaSuccess) return e0;
+  const int S = (int)((T + R - 1) / R);  // at most ceil(T / 256): the caller checked that it fits
+  attn_split_kernel<D, NQ><<<dim3(H, S), kAttnThreads, 0, st>>>(q, kc, ks, kg, km, vc, vs, vg, L, T, R, H, scale,
                                                                 part, view);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -326,15 +371,14 @@ nvfp4_status nvfp4_kv_attention_decode(const float* q, int n_q, const uint8_t* k
     view.meta[i] = frame_meta[i];
   }
   const int64_t T = (int64_t)n_frames * tokens_per_frame;
-  const int64_t S64 = (T + nvfp4::kAttnTokensPerSplit - 1) / nvfp4::kAttnTokensPerSplit;
+  const int64_t S64 = (T + nvfp4::kAttnTokensPerSplit - 1) / nvfp4::kAttnTokensPerSplit;  // most splits
   if (S64 > 65535) return NVFP4_ESHAPE;
-  const int S = (int)S64;
   float* part = static_cast<float*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
 #define NVFP4_ATTN(DD, QQ)                                                                                     \
   e = nvfp4::launch_attn<DD, QQ>(q, k_codes, k_scales, k_g, k_mean, v_codes, v_scales, v_g, tokens_per_frame, T, \
-                                 H, scale, part, S, view, out, st)
+                                 H, scale, part, view, out, st)
   if (D == 128) {
     if (n_q == 1) NVFP4_ATTN(128, 1); else if (n_q == 2) NVFP4_ATTN(128, 2);
     else if (n_q == 3) NVFP4_ATTN(128, 3); else NVFP4_ATTN(128, 4);

@@ -4,7 +4,8 @@ Chunks are quantized into pool slots by the cache manager and the quantizer; que
 attend over each chunk's view.  The GPU evaluates scores and the softmax in fp32: per
 lane and 16-channel block, a fused chain over q . Q_k, times the block scale, plus the
 slot's q . mean (itself a 16-term chain); a shuffle tree over the token's lanes; an online
-softmax over at most 256 tokens per split; then exact merging.  So each output obeys
+softmax per split of 256 to 2048 tokens (each lane group's fp32 sums of at most 128 terms);
+then exact merging.  So each output obeys
     |o - o_ref| <= Vmax * (64 * 2^-24 * A + 1e-5)
 with A = max_t |scale| sum_d |q_d| (|Q S|_td + |mean_d|) and Vmax = max |v| of the head,
 both from the oracle: a score error of at most about 23 units of 2^-24 relative to A moves
